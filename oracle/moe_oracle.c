@@ -1,0 +1,343 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for the forward pass of a Qwen3-style
+ * sparse Mixture-of-Experts block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load or call this library.  It shares
+ * no code, header, table or helper with the CUDA library; the two only see the
+ * same seeded input bytes.
+ *
+ * What it computes follows the block's forward method as printed on the
+ * cnblogs page "大模型-qwen3 MoE 详细解读" (class Qwen3MoeSparseMoeBlock,
+ * __init__ / forward, and the line-by-line commentary that follows it):
+ *
+ *   logits = x · W_routerᵀ                      (gate = Linear(H, E, bias=False))
+ *   p      = softmax(logits) in float          (F.softmax(..., dtype=float))
+ *   w, idx = topk(p, K)                        (sorted, largest first)
+ *   if norm_topk_prob: w /= Σ_k w
+ *   out[t] = Σ_k w_k · MLP_{idx_k}(x_t)        (per-expert loop + index_add_)
+ *
+ * with MLP_e(x) = down_e( silu(gate_e(x)) ⊙ up_e(x) ) -- the gate_proj /
+ * up_proj / down_proj expert of the csdn page "MoE架构深度解析：128专家与8激活的
+ * 智能路由" (section "128个专家网络的组织结构与参数分布", parameter table), and the
+ * load-balance statistic  aux = n · Σ_i f_i · P_i  of that page's section
+ * "负载均衡机制".
+ *
+ * Readings taken where the pages are silent or ambiguous:
+ *  - logits are kept in fp32 (no bf16 rounding) unless ORACLE_BF16_LOGITS;
+ *  - ranking uses the fp32 logits, descending, ties to the lower expert index;
+ *  - routing weights stay fp32 (no cast to bf16);
+ *  - the SwiGLU intermediate a = silu(g)·u is rounded to bf16 (the dtype the
+ *    second projection consumes) unless ORACLE_FP64_INTERMEDIATE;
+ *  - the token-expert pairs are ordered by expert, then token;
+ *  - f_e = counts_e / (T·K) and P_e = mean over tokens of the full softmax.
+ *
+ * Arithmetic: every dot product and sum is accumulated in double, from the
+ * exact values of the bf16 inputs (a bf16×bf16 product is exact in double).
+ * Results are rounded once, to fp32 for logits / weights / aux and to bf16
+ * (round to nearest even) for the block output.  No blocking, fusion or
+ * reordering beyond the definition; OpenMP only splits independent tokens.
+ *
+ * All arrays are host memory, row-major, contiguous.  bf16 values are passed
+ * as their uint16 bit patterns.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BF16_LOGITS 1       /* round logits to bf16 before routing      */
+#define ORACLE_FP64_INTERMEDIATE 2 /* keep silu(g)*u in double (no bf16 round) */
+
+/* ---- number formats --------------------------------------------------- */
+
+/* Exact value of a bf16 bit pattern: bf16 is the top half of an IEEE fp32. */
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double straight to bf16, to nearest, ties to even (no detour
+ * through fp32, which would round twice).  bf16 has 8 significant bits and
+ * the fp32 exponent range; subnormals are spaced 2^-133 apart. */
+uint16_t oracle_f64_to_bf16(double v) {
+    if (isnan(v)) return (uint16_t)0x7FC0;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else if (isinf(a)) {
+        r = INFINITY;
+    } else {
+        int ex;
+        (void)frexp(a, &ex); /* a = fr·2^ex, fr in [0.5, 1) */
+        int ulp_exp = ex - 8;
+        if (ulp_exp < -133) ulp_exp = -133;
+        double q = ldexp(a, -ulp_exp); /* exact: scaling by a power of two */
+        r = ldexp(nearbyint(q), ulp_exp);
+        if (r >= ldexp(1.0, 128)) r = INFINITY;
+    }
+    float f = (float)r; /* exact: r is representable in bf16 */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t b = (uint16_t)(u >> 16);
+    if (neg) b |= 0x8000u;
+    return b;
+}
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ---- step 1: router logits (gate = Linear(H, E, bias=False)) ------------ */
+
+/* logits[t,e] = Σ_h x[t,h]·W_router[e,h], accumulated in double, rounded to
+ * fp32 (or to bf16 then widened, with ORACLE_BF16_LOGITS). */
+int oracle_router_logits(const uint16_t* x, int T, int H, const uint16_t* Wr,
+                         int E, int flags, float* logits) {
+    if (T < 0 || H < 1 || E < 1 || (T > 0 && (!x || !logits)) || !Wr) return 1;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int h = 0; h < H; ++h)
+                s += oracle_bf16_to_f64(x[(size_t)t * H + h]) *
+                     oracle_bf16_to_f64(Wr[(size_t)e * H + h]);
+            float l = (float)s;
+            if (flags & ORACLE_BF16_LOGITS) l = (float)oracle_bf16_to_f64(oracle_f64_to_bf16(s));
+            logits[(size_t)t * E + e] = l;
+        }
+    }
+    return 0;
+}
+
+/* ---- step 2: softmax over all E experts (in double) ---------------------- */
+
+/* probs[t,e] = exp(l_e - max_j l_j) / Σ_j exp(l_j - max_j l_j).  Subtracting
+ * the row maximum does not change the result (softmax is shift-invariant). */
+int oracle_softmax(const float* logits, int T, int E, double* probs) {
+    if (T < 0 || E < 1) return 1;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        double m = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > m) m = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp((double)l[e] - m);
+        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp((double)l[e] - m) / z;
+    }
+    return 0;
+}
+
+/* ---- steps 3-4: top-k selection and optional renormalisation ------------- */
+
+/* "a before b" in the ranking: larger logit first, equal logits -> lower
+ * expert index first.  Float comparison, so -0 == +0. */
+static int ranks_before(const float* l, int a, int b) {
+    if (l[a] > l[b]) return 1;
+    if (l[a] < l[b]) return 0;
+    return a < b;
+}
+
+/* For each token pick the K experts that come first in the ranking, in
+ * ranking order; w_k = p[idx_k], divided by Σ_k p[idx_k] when norm != 0. */
+int oracle_route_from_logits(const float* logits, int T, int E, int K, int norm,
+                             int32_t* topk_idx, float* topk_w) {
+    if (T < 0 || E < 1 || E > 1024 || K < 1 || K > E) return 1;
+    if (T == 0) return 0;
+    double* probs = (double*)malloc((size_t)T * E * sizeof(double));
+    if (!probs) return 2;
+    oracle_softmax(logits, T, E, probs);
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        const double* p = probs + (size_t)t * E;
+        char taken[1024];
+        int32_t sel[1024];
+        memset(taken, 0, (size_t)E);
+        for (int k = 0; k < K; ++k) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || ranks_before(l, e, best)) best = e;
+            }
+            taken[best] = 1;
+            sel[k] = best;
+        }
+        double sum = 0.0;
+        for (int k = 0; k < K; ++k) sum += p[sel[k]];
+        for (int k = 0; k < K; ++k) {
+            topk_idx[(size_t)t * K + k] = sel[k];
+            double w = p[sel[k]];
+            if (norm) w = w / sum;
+            topk_w[(size_t)t * K + k] = (float)w;
+        }
+    }
+    free(probs);
+    return 0;
+}
+
+/* ---- step 5: dispatch (group the token-expert pairs by expert) ---------- */
+
+/* Pairs (t,k) are numbered in the order (expert, token): for each expert in
+ * increasing index, the tokens that chose it in increasing token order.
+ *   counts[e]    = number of pairs routed to e
+ *   offsets[e]   = Σ_{e'<e} counts[e']   (offsets[E] = T·K)
+ *   perm_tok[r]  = token of the pair in row r;  perm_slot[r] = its k-slot
+ *   inv[t*K+k]   = row of pair (t,k)
+ * Unique, because a token selects each expert at most once. */
+int oracle_dispatch(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv) {
+    if (T < 0 || E < 1 || K < 1) return 1;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (size_t i = 0; i < (size_t)T * K; ++i) {
+        int e = topk_idx[i];
+        if (e < 0 || e >= E) return 3;
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t row = 0;
+    for (int e = 0; e < E; ++e)
+        for (int t = 0; t < T; ++t)
+            for (int k = 0; k < K; ++k)
+                if (topk_idx[(size_t)t * K + k] == e) {
+                    perm_tok[row] = t;
+                    perm_slot[row] = k;
+                    inv[(size_t)t * K + k] = row;
+                    ++row;
+                }
+    return 0;
+}
+
+/* ---- step 6: one expert's SwiGLU MLP on one token ----------------------- */
+
+/* y[h] = Σ_i a_i · W_down[e,h,i],  a_i = silu(g_i)·u_i,
+ * g_i = Σ_h x_h·W_gate[e,i,h],  u_i = Σ_h x_h·W_up[e,i,h].
+ * Wg/Wu point at expert e's [I,H] block, Wd at its [H,I] block. */
+int oracle_expert_mlp(const uint16_t* x_row, int H, const uint16_t* Wg, const uint16_t* Wu,
+                      const uint16_t* Wd, int I, int flags, double* y) {
+    double* a = (double*)malloc((size_t)I * sizeof(double));
+    if (!a) return 2;
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double xv = oracle_bf16_to_f64(x_row[h]);
+            g += xv * oracle_bf16_to_f64(Wg[(size_t)i * H + h]);
+            u += xv * oracle_bf16_to_f64(Wu[(size_t)i * H + h]);
+        }
+        double ai = silu(g) * u;
+        if (!(flags & ORACLE_FP64_INTERMEDIATE)) ai = oracle_bf16_to_f64(oracle_f64_to_bf16(ai));
+        a[i] = ai;
+    }
+    for (int h = 0; h < H; ++h) {
+        double s = 0.0;
+        for (int i = 0; i < I; ++i) s += a[i] * oracle_bf16_to_f64(Wd[(size_t)h * I + i]);
+        y[h] = s;
+    }
+    free(a);
+    return 0;
+}
+
+/* ---- step 7: combine (weighted sum over the token's K experts) ---------- */
+
+/* out_row[h] = bf16( Σ_k w_k · MLP_{idx_k}(x_row)[h] ), the sum in double. */
+int oracle_token_output(const uint16_t* x_row, int H, const int32_t* idx_row,
+                        const float* w_row, int K, const uint16_t* Wg, const uint16_t* Wu,
+                        const uint16_t* Wd, int E, int I, int flags, uint16_t* out_row) {
+    double* acc = (double*)calloc((size_t)H, sizeof(double));
+    double* y = (double*)malloc((size_t)H * sizeof(double));
+    if (!acc || !y) { free(acc); free(y); return 2; }
+    int rc = 0;
+    for (int k = 0; k < K && rc == 0; ++k) {
+        int e = idx_row[k];
+        if (e < 0 || e >= E) { rc = 3; break; }
+        size_t blk = (size_t)I * H;
+        rc = oracle_expert_mlp(x_row, H, Wg + (size_t)e * blk, Wu + (size_t)e * blk,
+                               Wd + (size_t)e * blk, I, flags, y);
+        for (int h = 0; h < H; ++h) acc[h] += (double)w_row[k] * y[h];
+    }
+    for (int h = 0; h < H; ++h) out_row[h] = oracle_f64_to_bf16(acc[h]);
+    free(acc);
+    free(y);
+    return rc;
+}
+
+/* ---- step 8: load-balance statistic ------------------------------------- */
+
+/* aux = E · Σ_e f_e · P_e  with  f_e = counts_e / (T·K)  (share of the
+ * token-expert pairs sent to e) and  P_e = (1/T) Σ_t p[t,e]  (mean router
+ * probability of e).  T = 0 gives 0. */
+double oracle_aux(const double* probs, const int32_t* counts, int T, int E, int K) {
+    if (T <= 0) return 0.0;
+    double s = 0.0;
+    for (int e = 0; e < E; ++e) {
+        double P = 0.0;
+        for (int t = 0; t < T; ++t) P += probs[(size_t)t * E + e];
+        P /= (double)T;
+        double f = (double)counts[e] / ((double)T * (double)K);
+        s += f * P;
+    }
+    return (double)E * s;
+}
+
+/* ---- the whole block ---------------------------------------------------- */
+
+/* Full forward.  Routing, dispatch and aux cover all T tokens; the block
+ * output is produced for the n_rows tokens listed in rows (all tokens, in
+ * order, when rows == NULL), into out[n_rows, H].  Any of logits / idx / w /
+ * aux / counts may be NULL.  Returns 0 on success. */
+int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, const uint16_t* Wg,
+                       const uint16_t* Wu, const uint16_t* Wd, int E, int K, int I, int norm,
+                       int flags, const int32_t* rows, int n_rows, uint16_t* out,
+                       float* logits_out, int32_t* idx_out, float* w_out, float* aux_out,
+                       int32_t* counts_out) {
+    if (T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || I < 1) return 1;
+    if (T == 0) {
+        if (aux_out) *aux_out = 0.0f;
+        if (counts_out) for (int e = 0; e < E; ++e) counts_out[e] = 0;
+        return 0;
+    }
+    size_t TE = (size_t)T * E, TK = (size_t)T * K;
+    float* logits = (float*)malloc(TE * sizeof(float));
+    double* probs = (double*)malloc(TE * sizeof(double));
+    int32_t* idx = (int32_t*)malloc(TK * sizeof(int32_t));
+    float* w = (float*)malloc(TK * sizeof(float));
+    int32_t* counts = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    int rc = 0;
+    if (!logits || !probs || !idx || !w || !counts) rc = 2;
+    if (!rc) rc = oracle_router_logits(x, T, H, Wr, E, flags, logits);
+    if (!rc) rc = oracle_softmax(logits, T, E, probs);
+    if (!rc) rc = oracle_route_from_logits(logits, T, E, K, norm, idx, w);
+    if (!rc) {
+        for (size_t i = 0; i < TK; ++i) counts[idx[i]] += 1;
+        if (aux_out) *aux_out = (float)oracle_aux(probs, counts, T, E, K);
+    }
+    if (!rc && out) {
+        int n = rows ? n_rows : T;
+        int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+        for (int j = 0; j < n; ++j) {
+            int t = rows ? rows[j] : j;
+            if (t < 0 || t >= T) { fail |= 1; continue; }
+            if (oracle_token_output(x + (size_t)t * H, H, idx + (size_t)t * K, w + (size_t)t * K, K,
+                                    Wg, Wu, Wd, E, I, flags, out + (size_t)j * H))
+                fail |= 1;
+        }
+        if (fail) rc = 3;
+    }
+    if (!rc) {
+        if (logits_out) memcpy(logits_out, logits, TE * sizeof(float));
+        if (idx_out) memcpy(idx_out, idx, TK * sizeof(int32_t));
+        if (w_out) memcpy(w_out, w, TK * sizeof(float));
+        if (counts_out) memcpy(counts_out, counts, (size_t)E * sizeof(int32_t));
+    }
+    free(logits);
+    free(probs);
+    free(idx);
+    free(w);
+    free(counts);
+    return rc;
+}

@@ -1,0 +1,352 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each pin checks the oracle against what the pages print (worked examples under
+tests/golden/), a closed form, an invariant, a special case that reduces to a
+library routine, or brute force on tiny inputs.  test_pins_catch_planted_mistakes
+rebuilds the oracle with one plausible mistake planted at a time and checks
+that at least one pin fails for each.
+"""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import moe_inputs as mi
+import oracle
+from conftest import GOLDEN
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+# ---- independent helpers (not the oracle's code) ---------------------------
+
+def bf16_bits_to_f64(b):
+    """bf16 bits -> float64 via torch (a library conversion)."""
+    t = torch.from_numpy(np.ascontiguousarray(b, np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def f64_rne_bf16_value(v):
+    """Round float64 values to the nearest bf16 value, ties to even, by integer
+    arithmetic on the float64 bits (normal range only).  Returns float64."""
+    v = np.asarray(v, np.float64)
+    u = v.view(np.uint64)
+    shift = np.uint64(45)  # float64 keeps 52 fraction bits, bf16 keeps 7
+    lsb = (u >> shift) & np.uint64(1)
+    u2 = ((u + (np.uint64(1) << np.uint64(44)) - np.uint64(1) + lsb) >> shift) << shift
+    return u2.view(np.float64)
+
+
+def np_swiglu(x, Wg, Wu, Wd, round_a=True):
+    """float64 numpy expert MLP: down(silu(gate x) * up x); rows of x are tokens."""
+    g = x @ Wg.T
+    u = x @ Wu.T
+    a = g * scipy.special.expit(g) * u
+    if round_a:
+        a = f64_rne_bf16_value(a)
+    return a @ Wd.T
+
+
+def rand_case(T, H, E, K, I, seed, norm=True):
+    cfg = mi.MoEConfig("pin", T, H, E, K, I, norm, seed=seed)
+    inp = mi.make_inputs(cfg, "cpu")
+    return cfg, {k: mi.bits(v) for k, v in inp.items()}
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+# ---- pins --------------------------------------------------------------------
+
+def pin_bf16_rounding():
+    # Against torch's fp32 -> bf16 conversion (round to nearest even) on values
+    # that are exact in fp32 (so torch rounds once), incl. ties and subnormals.
+    rng = np.random.default_rng(1)
+    v = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32),
+        (rng.standard_normal(1000) * 1e-39).astype(np.float32),  # subnormal range
+        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 3.0e38, -3.4e38, 0.0,
+                  -0.0, 2 ** -133, 2 ** -134, 3 * 2 ** -135], np.float32),
+    ])
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f64_to_bf16(v.astype(np.float64))
+    assert np.array_equal(got, ref), np.nonzero(got != ref)
+    back = oracle.bf16_to_f64(ref)
+    assert np.array_equal(back.view(np.uint64), bf16_bits_to_f64(ref).view(np.uint64))
+
+
+def pin_worked_example():
+    g = dict(line.split(None, 1) for line in read_golden("router_top2_worked_example.txt"))
+    logits = np.array([[float(v) for v in g["logits"].split()]], np.float32)
+    K = int(g["K"])
+    idx, w = oracle.route_from_logits(logits, K, norm=False)
+    assert idx[0].tolist() == [int(v) for v in g["topk_idx"].split()]
+    idx, w = oracle.route_from_logits(logits, K, norm=True)
+    assert idx[0].tolist() == [int(v) for v in g["topk_idx"].split()]
+
+
+def pin_topk_bruteforce():
+    # Full sort with the key (logit descending, index ascending), on logits
+    # quantised to create many exact ties.
+    rng = np.random.default_rng(2)
+    for E, K in [(8, 2), (16, 5), (128, 8), (7, 7), (1, 1)]:
+        l = np.round(rng.standard_normal((50, E)) * 4).astype(np.float32) / 4
+        idx, _ = oracle.route_from_logits(l, K, norm=False)
+        for t in range(l.shape[0]):
+            order = np.lexsort((np.arange(E), -l[t].astype(np.float64)))
+            assert idx[t].tolist() == order[:K].tolist(), (E, K, t)
+
+
+def pin_all_equal_logits():
+    for E, K in [(8, 2), (128, 8), (5, 5)]:
+        idx, w = oracle.route_from_logits(np.zeros((3, E), np.float32), K, norm=False)
+        assert (idx == np.arange(K)).all()
+        assert np.allclose(w, 1.0 / E, rtol=0, atol=1e-7)
+
+
+def pin_weights_closed_form():
+    # norm=True: softmax over the kept logits only (top-k then softmax) equals
+    # softmax, top-k, renormalise.  norm=False: the full softmax (scipy).
+    rng = np.random.default_rng(3)
+    for E, K in [(8, 2), (128, 8), (16, 16)]:
+        l = (rng.standard_normal((40, E)) * 2).astype(np.float32)
+        idx, w = oracle.route_from_logits(l, K, norm=True)
+        kept = np.take_along_axis(l.astype(np.float64), idx, axis=1)
+        ref = scipy.special.softmax(kept, axis=1)
+        assert np.abs(w - ref).max() < 1e-6
+        assert np.abs(w.astype(np.float64).sum(1) - 1).max() < 1e-6
+        idx2, w2 = oracle.route_from_logits(l, K, norm=False)
+        assert np.array_equal(idx, idx2)
+        full = scipy.special.softmax(l.astype(np.float64), axis=1)
+        ref2 = np.take_along_axis(full, idx2, axis=1).astype(np.float32)
+        assert np.abs(w2 - ref2).max() <= 1e-7
+
+
+def pin_router_logits():
+    # x·W_routerᵀ in float64 by numpy matmul, rounded to fp32.
+    _, b = rand_case(9, 40, 6, 2, 16, seed=4)
+    l = oracle.router_logits(b["x"], b["W_router"])
+    ref = (bf16_bits_to_f64(b["x"]) @ bf16_bits_to_f64(b["W_router"]).T).astype(np.float32)
+    assert np.abs(l.astype(np.float64) - ref).max() <= 1e-6 * np.abs(ref).max()
+
+
+def pin_dispatch_bruteforce():
+    rng = np.random.default_rng(5)
+    for T, E, K in [(1, 4, 2), (37, 8, 3), (200, 16, 4), (64, 2, 2)]:
+        idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+        d = oracle.dispatch(idx, E)
+        tok = np.repeat(np.arange(T), K)
+        slot = np.tile(np.arange(K), T)
+        key = idx.ravel().astype(np.int64) * T + tok
+        order = np.argsort(key, kind="stable")
+        assert np.array_equal(d["perm_tok"], tok[order])
+        assert np.array_equal(d["perm_slot"], slot[order])
+        assert np.array_equal(d["counts"], np.bincount(idx.ravel(), minlength=E))
+        assert d["offsets"][0] == 0 and d["offsets"][-1] == T * K
+        assert np.array_equal(np.diff(d["offsets"]), d["counts"])
+        inv = d["inv"].ravel()
+        assert np.array_equal(inv[order], np.arange(T * K))  # inv ∘ perm = id
+
+
+def pin_single_expert_is_swiglu():
+    # E = K = 1: the block is one SwiGLU MLP with weight 1.
+    for norm in (False, True):
+        _, b = rand_case(11, 64, 1, 1, 48, seed=6, norm=norm)
+        r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 1, norm)
+        assert (r["idx"] == 0).all() and (r["w"] == 1.0).all()
+        x = bf16_bits_to_f64(b["x"])
+        y = np_swiglu(x, bf16_bits_to_f64(b["W_gate"][0]), bf16_bits_to_f64(b["W_up"][0]),
+                      bf16_bits_to_f64(b["W_down"][0]))
+        ref = f64_rne_bf16_value(y)
+        got = bf16_bits_to_f64(r["out"])
+        ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+        assert (np.abs(got - ref) <= ulp).all()
+        assert np.mean(got == ref) > 0.99
+
+
+def _dense_reference(b, idx, w, E, round_a=True):
+    x = bf16_bits_to_f64(b["x"])
+    T = x.shape[0]
+    G = np.zeros((T, E))
+    for t in range(T):
+        for k in range(idx.shape[1]):
+            G[t, idx[t, k]] += float(w[t, k])
+    acc = np.zeros_like(x)
+    for e in range(E):
+        y = np_swiglu(x, bf16_bits_to_f64(b["W_gate"][e]), bf16_bits_to_f64(b["W_up"][e]),
+                      bf16_bits_to_f64(b["W_down"][e]), round_a)
+        acc += G[:, [e]] * y
+    return acc
+
+
+def pin_dense_equivalence():
+    # out[t] = Σ_e G[t,e]·MLP_e(x_t) with the dense routing matrix G
+    # (k non-zeros per row): every expert on every token, no dispatch.
+    for (T, H, E, K, I, norm) in [(13, 32, 6, 3, 24, True), (20, 64, 8, 2, 32, False)]:
+        _, b = rand_case(T, H, E, K, I, seed=7 + T, norm=norm)
+        r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], K,
+                               norm, flags=oracle.FP64_INTERMEDIATE)
+        ref = f64_rne_bf16_value(_dense_reference(b, r["idx"], r["w"], E, round_a=False))
+        got = bf16_bits_to_f64(r["out"])
+        assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all()
+        assert np.mean(got == ref) > 0.98
+
+
+def pin_soft_router():
+    # K = E with norm: the soft (dense) mixture Σ_e softmax(l)_e·MLP_e(x).
+    _, b = rand_case(10, 32, 4, 4, 16, seed=8)
+    r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 4, True,
+                           flags=oracle.FP64_INTERMEDIATE)
+    x = bf16_bits_to_f64(b["x"])
+    l = (x @ bf16_bits_to_f64(b["W_router"]).T).astype(np.float32).astype(np.float64)
+    p = scipy.special.softmax(l, axis=1)
+    acc = np.zeros_like(x)
+    for e in range(4):
+        acc += p[:, [e]] * np_swiglu(x, bf16_bits_to_f64(b["W_gate"][e]),
+                                     bf16_bits_to_f64(b["W_up"][e]),
+                                     bf16_bits_to_f64(b["W_down"][e]), round_a=False)
+    ref = f64_rne_bf16_value(acc)
+    got = bf16_bits_to_f64(r["out"])
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -6 + 1e-30).all()
+
+
+def pin_token_permutation_equivariance():
+    _, b = rand_case(24, 32, 8, 2, 16, seed=9)
+    r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 2, True)
+    perm = np.random.default_rng(9).permutation(24)
+    r2 = oracle.moe_forward(b["x"][perm], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 2,
+                            True)
+    assert np.array_equal(r2["out"], r["out"][perm])
+    assert np.array_equal(r2["idx"], r["idx"][perm])
+    assert np.array_equal(r2["counts"], r["counts"])
+    assert abs(r2["aux"] - r["aux"]) < 1e-6
+
+
+def pin_aux():
+    L = np.log(3.0)
+    for line in read_golden("aux_hand_examples.txt"):
+        head, vals, want = [s.strip() for s in line.split("|")]
+        _, E, K, T = head.split()
+        E, K, T = int(E), int(K), int(T)
+        l = np.array([L if v == "L" else float(v) for v in vals.split()], np.float32).reshape(T, E)
+        idx, _ = oracle.route_from_logits(l, K, norm=True)
+        counts = np.bincount(idx.ravel(), minlength=E).astype(np.int32)
+        a = oracle.aux(oracle.softmax(l), counts, K)
+        assert abs(a - float(want)) < 1e-6, (line, a)
+    # W_router = 0: uniform probabilities -> aux = 1 whatever the assignment.
+    _, b = rand_case(33, 32, 8, 3, 16, seed=10)
+    r = oracle.moe_forward(b["x"], np.zeros_like(b["W_router"]), b["W_gate"], b["W_up"],
+                           b["W_down"], 3, True, want_out=False)
+    assert abs(r["aux"] - 1.0) < 1e-6
+    # Balanced assignment (each expert gets T·K/E pairs) -> aux = 1 whatever p is.
+    rng = np.random.default_rng(11)
+    E, K, T = 8, 2, 16
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)], np.int32)
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int32)
+    assert (counts == T * K // E).all()
+    p = scipy.special.softmax(rng.standard_normal((T, E)), axis=1)
+    assert abs(oracle.aux(p, counts, K) - 1.0) < 1e-12
+    # Bounds 0 <= aux <= E on random cases.
+    for s in range(3):
+        _, b = rand_case(40, 32, 8, 2, 16, seed=20 + s)
+        r = oracle.moe_forward(b["x"], b["W_router"] * 1, b["W_gate"], b["W_up"], b["W_down"], 2,
+                               True, want_out=False)
+        assert 0.0 <= r["aux"] <= 8.0
+
+
+def pin_param_counts():
+    g = dict(line.split() for line in read_golden("qwen3_param_counts.txt"))
+    H, E, K, I = (int(g[k]) for k in "HEKI")
+    cfg = mi.MoEConfig("q", 1, H, E, K, I, True)
+    # layouts: W_router [E,H], W_gate/W_up [E,I,H], W_down [E,H,I]
+    assert E * H == int(g["router"])
+    assert I * H == int(g["gate_proj"]) == int(g["up_proj"]) == int(g["down_proj"])
+    assert (cfg.E, cfg.I, cfg.H) == (E, I, H)
+
+
+PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equal_logits,
+        pin_weights_closed_form, pin_router_logits, pin_dispatch_bruteforce,
+        pin_single_expert_is_swiglu, pin_dense_equivalence, pin_soft_router,
+        pin_token_permutation_equivariance, pin_aux, pin_param_counts]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+def test_zero_tokens():
+    z = np.zeros((0, 16), np.uint16)
+    Wr = np.zeros((4, 16), np.uint16)
+    W = np.zeros((4, 8, 16), np.uint16)
+    Wd = np.zeros((4, 16, 8), np.uint16)
+    r = oracle.moe_forward(z, Wr, W, W, Wd, 2, True)
+    assert r["out"].shape == (0, 16) and r["aux"] == 0.0 and (r["counts"] == 0).all()
+
+
+def test_near_tie_detector():
+    p = np.array([[0.5, 0.3, 0.3 - 5e-7, 0.1 + 5e-7 - 0.0], [0.4, 0.3, 0.2, 0.1]])
+    assert oracle.near_tie_tokens(p, 2).tolist() == [0]
+    assert oracle.near_tie_tokens(p, 1).tolist() == []
+
+
+# ---- planted mistakes: each must break at least one pin -----------------------
+
+MUTATIONS = {
+    "silu_sign": ("g / (1.0 + exp(-g))", "g / (1.0 + exp(g))"),
+    "norm_dropped": ("if (norm) w = w / sum;", "if (0) w = w / sum;"),
+    "tie_break_reversed": ("    return a < b;", "    return a > b;"),
+    "gate_up_swapped": ("g += xv * oracle_bf16_to_f64(Wg[", "g += xv * oracle_bf16_to_f64(Wu["),
+    "router_transposed": ("oracle_bf16_to_f64(Wr[(size_t)e * H + h])",
+                          "oracle_bf16_to_f64(Wr[(size_t)h * E + e])"),
+    "softmax_no_shift": ("probs[(size_t)t * E + e] = exp((double)l[e] - m) / z;",
+                         "probs[(size_t)t * E + e] = exp((double)l[e]) / z;"),
+    "combine_unweighted": ("acc[h] += (double)w_row[k] * y[h];", "acc[h] += y[h];"),
+    "aux_per_token_share": ("((double)T * (double)K)", "((double)T)"),
+    "dispatch_token_major": ("for (int e = 0; e < E; ++e)\n        for (int t = 0; t < T; ++t)",
+                             "for (int t = 0; t < T; ++t)\n        for (int e = 0; e < E; ++e)"),
+    "bf16_truncates": ("r = ldexp(nearbyint(q), ulp_exp);", "r = ldexp(floor(q), ulp_exp);"),
+    "down_uses_unrounded_gate": ("double ai = silu(g) * u;", "double ai = silu(u) * u;"),
+    "topk_by_smallest": ("    if (l[a] > l[b]) return 1;\n    if (l[a] < l[b]) return 0;",
+                         "    if (l[a] < l[b]) return 1;\n    if (l[a] > l[b]) return 0;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    d = tempfile.mkdtemp(prefix="oracle_mut_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistakes(name, mutant_dir):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    mut = src.replace(old, new)
+    c = os.path.join(mutant_dir, f"{name}.c")
+    so = os.path.join(mutant_dir, f"{name}.so")
+    open(c, "w").write(mut)
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+                           "-o", so, c, "-lm"])
+    failed = []
+    with oracle.use_library(so):
+        for pin in PINS:
+            try:
+                pin()
+            except AssertionError:
+                failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
