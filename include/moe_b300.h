@@ -1,0 +1,170 @@
+/*
+ * moe_b300.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts block
+ * forward.
+ *
+ * The operation is the forward method of the Qwen3-style sparse MoE block as
+ * printed on the cnblogs page "大模型-qwen3 MoE 详细解读" (class
+ * Qwen3MoeSparseMoeBlock): router logits x·W_routerᵀ (a bias-free Linear),
+ * softmax in fp32, top-k, optional renormalisation of the k kept weights
+ * (norm_topk_prob), dispatch of the tokens to their experts, the SwiGLU expert
+ * MLP down(silu(gate(x)) ⊙ up(x)) (the gate_proj / up_proj / down_proj expert
+ * of the csdn page "MoE架构深度解析：128专家与8激活的智能路由", section
+ * "128个专家网络的组织结构与参数分布"), and the routing-weight-scaled combine back
+ * into token order (the index_add_ of the forward).  It also produces the
+ * load-balance statistic aux = n · Σ_i f_i · P_i of the csdn page's section
+ * "负载均衡机制".
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - bf16 tensors are passed as uint16_t bit patterns (moe_bf16).
+ *  - Every pointer is DEVICE memory unless the name ends in _host; arrays are
+ *    contiguous, row-major, and must be 16-byte aligned.  The caller owns them;
+ *    the library never frees or keeps them after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    enqueue work on it and return without waiting (except moe_forward_host);
+ *    outputs are valid once that work completes.  No call synchronises the
+ *    host with the device.
+ *  - Every call returns a moe_status.  All argument checks happen before any
+ *    work is enqueued: a call that returns an error other than MOE_ERR_CUDA
+ *    has enqueued nothing.  No C++ exception crosses this interface.
+ *  - Sizes: T >= 0 tokens, H hidden size, E experts, K experts per token, I
+ *    expert intermediate size.  H and I must be multiples of 64, 1 <= E <= 256,
+ *    1 <= K <= min(E, 16).  T = 0 is a no-op that writes aux = 0.
+ *  - Only NVIDIA Blackwell datacenter GPUs of compute capability 10.3 (B300)
+ *    are supported; other devices give MOE_ERR_UNSUPPORTED_DEVICE.
+ *  - Results are deterministic: the same inputs give bitwise identical outputs
+ *    on every call (no floating-point atomics anywhere).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* a size out of range or a required pointer NULL  */
+    MOE_ERR_ALIGNMENT = 2,          /* a pointer not 16-byte aligned                   */
+    MOE_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3   */
+    MOE_ERR_WORKSPACE = 4,          /* workspace too small, or it could not be grown    */
+    MOE_ERR_CUDA = 5,               /* a CUDA call failed; see moe_last_cuda_error()    */
+    MOE_ERR_TIMEOUT = 6             /* a bounded device-side wait gave up               */
+};
+
+/*
+ * moe_forward -- the whole block forward on the current device.
+ *
+ *   x              [T, H]     bf16   hidden states, one row per token
+ *   W_router       [E, H]     bf16   router weight (nn.Linear(H, E, bias=False))
+ *   W_gate, W_up   [E, I, H]  bf16   per-expert gate_proj / up_proj weights
+ *   W_down         [E, H, I]  bf16   per-expert down_proj weights
+ *   norm_topk_prob            0/1    renormalise the K kept weights to sum to 1
+ *   out            [T, H]     bf16   block output Σ_k w_k · MLP_{idx_k}(x_t)
+ *   router_logits  [T, E]     fp32   x·W_routerᵀ (not rounded to bf16); may be NULL
+ *   topk_idx       [T, K]     int32  selected experts, by descending logit, ties
+ *                                    to the lower expert index; may be NULL
+ *   topk_w         [T, K]     fp32   routing weights (softmax probabilities of
+ *                                    the selected experts, renormalised if
+ *                                    norm_topk_prob); may be NULL
+ *   aux            [1]        fp32   E · Σ_e (counts_e/(T·K)) · mean_t p[t,e];
+ *                                    may be NULL
+ *
+ * Scratch memory comes from a workspace the library owns: one per (device,
+ * stream), grown on demand with stream-ordered allocation and kept until the
+ * process exits.  Use moe_forward_ws to supply your own.
+ */
+int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                int E, int K, int I, int norm_topk_prob, moe_bf16* out,
+                float* router_logits, int32_t* topk_idx, float* topk_w, float* aux,
+                void* stream);
+
+/* Bytes of device workspace moe_forward_ws needs for these sizes (0 on a size
+ * error).  The requirement grows with T·K·(H+I); it does not depend on data. */
+size_t moe_workspace_bytes(int T, int H, int E, int K, int I);
+
+/* moe_forward with caller-provided scratch: `workspace` is device memory of at
+ * least moe_workspace_bytes(T,H,E,K,I) bytes, 256-byte aligned, that no other
+ * work uses until this call's work has completed on `stream`.  Too small ->
+ * MOE_ERR_WORKSPACE.  Every other argument is as for moe_forward. */
+int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                   const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                   int E, int K, int I, int norm_topk_prob, moe_bf16* out,
+                   float* router_logits, int32_t* topk_idx, float* topk_w, float* aux,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* End-to-end call with host activations: copies x_host [T,H] to the device,
+ * runs moe_forward, copies out_host [T,H] (and, when not NULL,
+ * router_logits_host [T,E], topk_idx_host / topk_w_host [T,K], aux_host [1])
+ * back, and waits for the stream, so the host buffers hold the results when
+ * it returns.  The weights are device pointers (a loaded model).  Host buffers
+ * should be page-locked for the copies to run at full speed.  Device staging
+ * for x and the outputs lives in the library-owned workspace of `stream`. */
+int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                     const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                     int E, int K, int I, int norm_topk_prob, moe_bf16* out_host,
+                     float* router_logits_host, int32_t* topk_idx_host, float* topk_w_host,
+                     float* aux_host, void* stream);
+
+/* Per-expert pair counts ("expert utilisation histogram") of the last
+ * moe_forward / moe_forward_host on `stream`, copied into counts_host[E]
+ * (waits for the stream).  MOE_ERR_INVALID_ARG if there was no such call. */
+int moe_last_expert_counts(int32_t* counts_host, int E, void* stream);
+
+/* Device-side status of the last forward that used `workspace` (the
+ * caller's workspace of moe_forward_ws, with the sizes of that call), or, with
+ * workspace == NULL, of the last moe_forward / moe_forward_host on `stream`.
+ * Waits for the stream.  Returns MOE_OK, or MOE_ERR_TIMEOUT if a bounded
+ * device-side wait of that forward gave up (its outputs are then invalid). */
+int moe_device_status(const void* workspace, int T, int H, int E, int K, int I, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_strerror(int status);
+
+/* The cudaError_t value behind the last MOE_ERR_CUDA on this host thread. */
+int moe_last_cuda_error(void);
+
+/* Kernel-path selection for the expert MLPs (process-wide):
+ *   MOE_PATH_AUTO      tensor-core grouped GEMMs when the average expert
+ *                      receives enough rows to fill a tile, else the
+ *                      weight-streaming kernels (decode-sized batches);
+ *   MOE_PATH_STREAMING always the weight-streaming kernels;
+ *   MOE_PATH_TCGEN05   always the tcgen05 grouped GEMMs.
+ * Returns the previous setting, or -1 for an unknown value. */
+enum moe_path { MOE_PATH_AUTO = 0, MOE_PATH_STREAMING = 1, MOE_PATH_TCGEN05 = 2 };
+int moe_set_expert_path(int path);
+
+/* ---- stage entry points (used by the stage-parity tests) --------------- */
+
+/* Steps softmax -> top-k -> renormalise on given fp32 logits [T,E]:
+ * topk_idx [T,K] int32 and topk_w [T,K] fp32, exactly as moe_forward
+ * computes them from its own logits. */
+int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm_topk_prob,
+                              int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Dispatch of given selections topk_idx [T,K] (each row holds K distinct
+ * experts in [0,E)): counts [E], offsets [E+1] (exclusive prefix sum),
+ * perm_tok / perm_slot [T·K] (token and k-slot of each row, rows ordered by
+ * expert then token) and inv [T,K] (row of each pair).  Out-of-range experts
+ * are not checked on the device. */
+int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
+                    void* stream);
+
+/* Combine: out[t,:] = bf16( Σ_{k=0..K-1} Y[inv[t,k], :] ) with fp32 sums in
+ * k order.  Y [T·K, H] bf16 holds the already weighted expert outputs in
+ * dispatch order; inv [T,K]. */
+int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H,
+                    moe_bf16* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,13 @@
+"""B300-native (sm_103a) forward of a Qwen3-style sparse Mixture-of-Experts block.
+
+The compute runs in libmoe_b300.so (C ABI in include/moe_b300.h); this package
+only marshals torch tensors into that ABI.  Build with
+``python -m mixture_experts_layer_98_b300.build``.
+"""
+from .binding import (EXPORTS, LIB_PATH, MOE_PATH_AUTO, MOE_PATH_STREAMING,  # noqa: F401
+                      MOE_PATH_TCGEN05, MoEError, lib, moe_dbg_combine, moe_dbg_permute,
+                      moe_dbg_route_from_logits, moe_device_status, moe_forward,
+                      moe_forward_host, moe_last_expert_counts, moe_set_expert_path,
+                      moe_workspace_bytes)
+
+forward = moe_forward

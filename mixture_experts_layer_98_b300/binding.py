@@ -1,0 +1,228 @@
+"""ctypes binding of libmoe_b300.so: same names as the C ABI (include/moe_b300.h),
+torch tensors in, data pointers and the current CUDA stream out.  Argument
+marshalling only -- every step of the forward runs in the library's kernels.
+There is no fallback: without the built library every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_ALIGNMENT = 2
+MOE_ERR_UNSUPPORTED_DEVICE = 3
+MOE_ERR_WORKSPACE = 4
+MOE_ERR_CUDA = 5
+MOE_ERR_TIMEOUT = 6
+MOE_PATH_AUTO = 0
+MOE_PATH_STREAMING = 1
+MOE_PATH_TCGEN05 = 2
+
+EXPORTS = ["moe_forward", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
+           "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
+           "moe_set_expert_path", "moe_dbg_route_from_logits", "moe_dbg_permute",
+           "moe_dbg_combine"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status, what):
+        msg = lib().moe_strerror(status).decode()
+        if status == MOE_ERR_CUDA:
+            msg += f" (cudaError {lib().moe_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [status {status}]")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run python -m mixture_experts_layer_98_b300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        fwd = [P, i, i, P, P, P, P, i, i, i, i, P, P, P, P, P]
+        L.moe_forward.argtypes = fwd + [P]
+        L.moe_forward_ws.argtypes = fwd + [P, sz, P]
+        L.moe_forward_host.argtypes = fwd + [P]
+        L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.moe_workspace_bytes.restype = sz
+        L.moe_last_expert_counts.argtypes = [P, i, P]
+        L.moe_device_status.argtypes = [P, i, i, i, i, i, P]
+        L.moe_strerror.argtypes = [i]
+        L.moe_strerror.restype = ctypes.c_char_p
+        L.moe_last_cuda_error.argtypes = []
+        L.moe_set_expert_path.argtypes = [i]
+        L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P]
+        L.moe_dbg_permute.argtypes = [P, i, i, i, P, P, P, P, P, P]
+        L.moe_dbg_combine.argtypes = [P, P, i, i, i, P, P]
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _call(rc, what):
+    if rc != MOE_OK:
+        raise MoEError(rc, what)
+
+
+def _shapes(x, W_router, W_gate, W_up, W_down):
+    T, H = x.shape
+    E, I, H2 = W_gate.shape
+    if H2 != H:
+        raise ValueError("W_gate must be [E, I, H]")
+    _dev(x, torch.bfloat16, "x")
+    _dev(W_router, torch.bfloat16, "W_router", (E, H))
+    _dev(W_gate, torch.bfloat16, "W_gate", (E, I, H))
+    _dev(W_up, torch.bfloat16, "W_up", (E, I, H))
+    _dev(W_down, torch.bfloat16, "W_down", (E, H, I))
+    return T, H, E, I
+
+
+def moe_forward(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, out=None,
+                router_logits=None, topk_idx=None, topk_w=None, aux=None, stream=None,
+                workspace=None):
+    """Block forward (moe_forward, or moe_forward_ws when `workspace` is a uint8
+    CUDA tensor).  Output tensors not given are allocated (router_logits,
+    topk_idx, topk_w and aux always are, unless passed as False to skip them).
+    Returns (out, router_logits, topk_idx, topk_w, aux)."""
+    T, H, E, I = _shapes(x, W_router, W_gate, W_up, W_down)
+    dev = x.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if router_logits is None:
+        router_logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    if aux is None:
+        aux = torch.empty((1,), dtype=torch.float32, device=dev)
+    router_logits = None if router_logits is False else router_logits
+    topk_idx = None if topk_idx is False else topk_idx
+    topk_w = None if topk_w is False else topk_w
+    aux = None if aux is False else aux
+    _dev(out, torch.bfloat16, "out", (T, H))
+    _dev(router_logits, torch.float32, "router_logits", (T, E))
+    _dev(topk_idx, torch.int32, "topk_idx", (T, K))
+    _dev(topk_w, torch.float32, "topk_w", (T, K))
+    _dev(aux, torch.float32, "aux", (1,))
+    args = [_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up), _ptr(W_down), E, K, I,
+            int(bool(norm_topk_prob)), _ptr(out), _ptr(router_logits), _ptr(topk_idx),
+            _ptr(topk_w), _ptr(aux)]
+    if workspace is None:
+        _call(lib().moe_forward(*args, _stream(stream)), "moe_forward")
+    else:
+        _dev(workspace, torch.uint8, "workspace")
+        _call(lib().moe_forward_ws(*args, _ptr(workspace), workspace.numel(), _stream(stream)),
+              "moe_forward_ws")
+    return out, router_logits, topk_idx, topk_w, aux
+
+
+def moe_workspace_bytes(T, H, E, K, I):
+    return int(lib().moe_workspace_bytes(T, H, E, K, I))
+
+
+def moe_forward_host(x_host, W_router, W_gate, W_up, W_down, K, norm_topk_prob, out_host,
+                     router_logits_host=None, topk_idx_host=None, topk_w_host=None,
+                     aux_host=None, stream=None):
+    """End-to-end call: host (ideally pinned) x_host [T,H] bf16 in, host outputs
+    filled on return.  Weights are CUDA tensors."""
+    T, H = x_host.shape
+    E, I, _ = W_gate.shape
+    for n, t in (("W_router", W_router), ("W_gate", W_gate), ("W_up", W_up), ("W_down", W_down)):
+        _dev(t, torch.bfloat16, n)
+    for n, t in (("x_host", x_host), ("out_host", out_host), ("router_logits_host",
+                                                            router_logits_host),
+                 ("topk_idx_host", topk_idx_host), ("topk_w_host", topk_w_host),
+                 ("aux_host", aux_host)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    _call(lib().moe_forward_host(_ptr(x_host), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up),
+                                 _ptr(W_down), E, K, I, int(bool(norm_topk_prob)),
+                                 _ptr(out_host), _ptr(router_logits_host), _ptr(topk_idx_host),
+                                 _ptr(topk_w_host), _ptr(aux_host), _stream(stream)),
+          "moe_forward_host")
+    return out_host
+
+
+def moe_last_expert_counts(E, stream=None):
+    c = torch.empty(E, dtype=torch.int32)
+    _call(lib().moe_last_expert_counts(_ptr(c), E, _stream(stream)), "moe_last_expert_counts")
+    return c
+
+
+def moe_device_status(workspace=None, sizes=(0, 64, 1, 1, 64), stream=None):
+    T, H, E, K, I = sizes
+    return int(lib().moe_device_status(_ptr(workspace), T, H, E, K, I, _stream(stream)))
+
+
+def moe_set_expert_path(path):
+    prev = lib().moe_set_expert_path(int(path))
+    if prev < 0:
+        raise ValueError(f"unknown expert path {path}")
+    return prev
+
+
+def moe_dbg_route_from_logits(logits, K, norm_topk_prob, stream=None):
+    T, E = logits.shape
+    _dev(logits, torch.float32, "logits")
+    idx = torch.empty((T, K), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    _call(lib().moe_dbg_route_from_logits(_ptr(logits), T, E, K, int(bool(norm_topk_prob)),
+                                          _ptr(idx), _ptr(w), _stream(stream)),
+          "moe_dbg_route_from_logits")
+    return idx, w
+
+
+def moe_dbg_permute(topk_idx, E, stream=None):
+    T, K = topk_idx.shape
+    _dev(topk_idx, torch.int32, "topk_idx")
+    d = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=d)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=d)
+    perm_tok = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
+    perm_slot = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
+    inv = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
+    _call(lib().moe_dbg_permute(_ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets),
+                                _ptr(perm_tok), _ptr(perm_slot), _ptr(inv), _stream(stream)),
+          "moe_dbg_permute")
+    n = T * K
+    return dict(counts=counts, offsets=offsets, perm_tok=perm_tok[:n], perm_slot=perm_slot[:n],
+                inv=inv[:n].view(T, K))
+
+
+def moe_dbg_combine(Y, inv, stream=None):
+    T, K = inv.shape
+    H = Y.shape[1]
+    _dev(Y, torch.bfloat16, "Y")
+    _dev(inv, torch.int32, "inv")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=Y.device)
+    _call(lib().moe_dbg_combine(_ptr(Y), _ptr(inv), T, K, H, _ptr(out), _stream(stream)),
+          "moe_dbg_combine")
+    return out

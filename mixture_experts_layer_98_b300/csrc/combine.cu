@@ -1,0 +1,61 @@
+// combine.cu -- gather-reduce of the weighted expert outputs into token order.
+//
+// Qwen3MoeSparseMoeBlock.forward (cnblogs page "大模型-qwen3 MoE 详细解读")
+// accumulates each expert's weighted output with index_add_ into a zeroed
+// [tokens, hidden] buffer.  Here each token instead reads its K rows of Y (the
+// weighted expert outputs in dispatch order) through inv and sums them in fp32
+// in k order, then rounds once to bf16: no zero-fill, no atomics, and the
+// result does not depend on scheduling.  16-byte loads and stores.
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ Y,
+                                                      const int32_t* __restrict__ inv, int T,
+                                                      int K, int vpr, uint4* __restrict__ out) {
+    const long long total = (long long)T * vpr;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int t = (int)(i / vpr), c = (int)(i % vpr);
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = 0.f;
+        for (int k = 0; k < K; ++k) {
+            const int row = __ldg(inv + (size_t)t * K + k);
+            const uint4 v = __ldg(Y + (size_t)row * vpr + c);
+            a[0] += bf16_lo(v.x);
+            a[1] += bf16_hi(v.x);
+            a[2] += bf16_lo(v.y);
+            a[3] += bf16_hi(v.y);
+            a[4] += bf16_lo(v.z);
+            a[5] += bf16_hi(v.z);
+            a[6] += bf16_lo(v.w);
+            a[7] += bf16_hi(v.w);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(a[0], a[1]);
+        o.y = pack_bf16x2(a[2], a[3]);
+        o.z = pack_bf16x2(a[4], a[5]);
+        o.w = pack_bf16x2(a[6], a[7]);
+        out[(size_t)t * vpr + c] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
+                           __nv_bfloat16* out, cudaStream_t st) {
+    const int vpr = H / 8;
+    const long long total = (long long)T * vpr;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    combine_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(Y), inv, T, K, vpr,
+                                                reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

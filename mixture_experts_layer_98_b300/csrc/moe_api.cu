@@ -1,0 +1,448 @@
+// moe_api.cu -- the C ABI: argument checks, workspace, and the stream-ordered
+// sequence of kernels for one forward of the sparse MoE block.
+//
+//   router (logits, softmax, top-k, renorm, probability sums)
+//   -> dispatch (counts, offsets, permutation, row tiles, aux, x gather)
+//   -> expert MLPs (tcgen05 grouped GEMMs, or weight streaming for small batches)
+//   -> combine (gather-reduce into token order)
+//
+// No host synchronisation: the expert kernels read the tile count on the device.
+#include <mutex>
+#include <unordered_map>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+static thread_local int g_last_cuda_error = 0;
+static int g_expert_path = MOE_PATH_AUTO;
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* p = base ? base + off : nullptr;
+        off = align_up(off + bytes, 256);
+        return p;
+    };
+    const size_t P = (size_t)s.P();
+    const size_t nch = (size_t)s.nchunks();
+    Workspace w{};
+    w.chunk_counts = (int32_t*)take(nch * s.E * 4);
+    w.chunk_base = (int32_t*)take(nch * s.E * 4);
+    w.counts = (int32_t*)take((size_t)s.E * 4);
+    w.offsets = (int32_t*)take(((size_t)s.E + 1) * 4);
+    w.tiles = (RowTile*)take((size_t)s.max_tiles(kStreamRows) * sizeof(RowTile));
+    w.n_tiles = (int32_t*)take(4);
+    w.status = (int32_t*)take(16);
+    w.p_partial = (float*)take((size_t)s.nrouter() * s.E * 4);
+    w.perm_tok = (int32_t*)take(P * 4);
+    w.perm_slot = (int32_t*)take(P * 4);
+    w.inv = (int32_t*)take(P * 4);
+    w.w_perm = (float*)take(P * 4);
+    w.topk_idx = (int32_t*)take(P * 4);
+    w.topk_w = (float*)take(P * 4);
+    w.x_perm = (__nv_bfloat16*)take(P * s.H * 2);
+    w.hbuf = (__nv_bfloat16*)take(P * s.I * 2);
+    w.ybuf = (__nv_bfloat16*)take(P * s.H * 2);
+    w.bytes = off;
+    if (ws) *ws = w;
+    return off;
+}
+
+static int check_sizes(int T, int H, int E, int K, int I) {
+    if (T < 0 || H < 64 || H % 64 || I < 64 || I % 64) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K > (1LL << 31) - 1) return MOE_ERR_INVALID_ARG;
+    if ((long long)H * 8 * 2 > 200 * 1024 || (long long)I * 8 * 2 > 200 * 1024)
+        return MOE_ERR_INVALID_ARG;  // staged rows of the streaming kernels must fit in smem
+    return MOE_OK;
+}
+
+static bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+static int check_device() {
+    static std::mutex mu;
+    static std::unordered_map<int, int> ok;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return MOE_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = ok.find(dev);
+    if (it == ok.end()) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        it = ok.emplace(dev, (major == 10 && minor == 3) ? 1 : 0).first;
+    }
+    return it->second ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+static int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = (int)e;
+    return MOE_ERR_CUDA;
+}
+
+// ---- library-owned workspaces, one per (device, stream) ---------------------
+struct OwnedWs {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    int32_t* counts = nullptr;  // counts of the last forward on this stream
+    int32_t* status = nullptr;  // status word of the last forward on this stream
+    int E = 0;
+};
+static std::mutex g_ws_mu;
+static std::unordered_map<unsigned long long, OwnedWs> g_ws;
+
+static unsigned long long ws_key(cudaStream_t st) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return ((unsigned long long)(uintptr_t)st) * 64ull + (unsigned long long)dev;
+}
+
+// Returns a workspace of at least `bytes` for `st` (grown with stream-ordered
+// allocation, so earlier work on the stream finishes with the old buffer first).
+static int owned_workspace(cudaStream_t st, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    OwnedWs& w = g_ws[ws_key(st)];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            cudaError_t e = cudaFreeAsync(w.ptr, st);
+            if (e != cudaSuccess) return cuda_status(e);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            w.counts = nullptr;
+            w.status = nullptr;
+        }
+        size_t want = align_up(bytes + bytes / 8, 1 << 20);
+        cudaError_t e = cudaMallocAsync(&w.ptr, want, st);
+        if (e != cudaSuccess) {
+            g_last_cuda_error = (int)e;
+            w.ptr = nullptr;
+            return MOE_ERR_WORKSPACE;
+        }
+        w.bytes = want;
+    }
+    *out = w.ptr;
+    return MOE_OK;
+}
+
+static void remember_counts(cudaStream_t st, const Workspace& ws, int E) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    OwnedWs& w = g_ws[ws_key(st)];
+    w.counts = ws.counts;
+    w.status = ws.status;
+    w.E = E;
+}
+
+static bool use_tcgen05(const Sizes& s) {
+    if (g_expert_path == MOE_PATH_STREAMING) return false;
+    if (g_expert_path == MOE_PATH_TCGEN05) return true;
+    // Tensor-core tiles are 128 rows; below ~32 rows per expert on average the
+    // work is weight-bandwidth bound and streaming reads each weight once.
+    return s.P() >= 32LL * s.E;
+}
+
+// The kernel sequence.  All pointers checked by the caller.
+static int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
+                       const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Sizes& s, int norm,
+                       __nv_bfloat16* out, float* logits, int32_t* idx, float* w, float* aux,
+                       const Workspace& ws, cudaStream_t st) {
+    if (!idx) idx = ws.topk_idx;
+    if (!w) w = ws.topk_w;
+    cudaError_t e = launch_router(x, Wr, s, norm, logits, idx, w, ws.p_partial, ws.status, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    const bool tc = use_tcgen05(s);
+    e = launch_dispatch(idx, w, x, s, ws, tc ? kTcRows : kStreamRows, true, ws.p_partial, aux, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st)
+           : launch_experts_streaming(Wg, Wu, Wd, s, ws, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = launch_combine(ws.ybuf, ws.inv, s.T, s.K, s.H, out, st);
+    return cuda_status(e);
+}
+
+static int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
+                              const void* Wu, const void* Wd, int E, int K, int I, const void* out,
+                              const void* logits, const void* idx, const void* w,
+                              const void* aux) {
+    int rc = check_sizes(T, H, E, K, I);
+    if (rc) return rc;
+    if (!Wr || !Wg || !Wu || !Wd) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !out)) return MOE_ERR_INVALID_ARG;
+    const void* ps[] = {x, Wr, Wg, Wu, Wd, out, logits, idx, w};
+    for (const void* p : ps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    if (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)) return MOE_ERR_ALIGNMENT;
+    return check_device();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_strerror(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (size out of range or NULL pointer)";
+        case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case MOE_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (B300)";
+        case MOE_ERR_WORKSPACE: return "workspace too small or could not be allocated";
+        case MOE_ERR_CUDA: return "CUDA error (see moe_last_cuda_error)";
+        case MOE_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+int moe_set_expert_path(int path) {
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05) return -1;
+    const int prev = g_expert_path;
+    g_expert_path = path;
+    return prev;
+}
+
+size_t moe_workspace_bytes(int T, int H, int E, int K, int I) {
+    if (check_sizes(T, H, E, K, I)) return 0;
+    Sizes s{T, H, E, K, I};
+    return layout_workspace(s, nullptr, nullptr);
+}
+
+int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                   const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down, int E,
+                   int K, int I, int norm_topk_prob, moe_bf16* out, float* router_logits,
+                   int32_t* topk_idx, float* topk_w, float* aux, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    int rc = check_forward_args(x, T, H, W_router, W_gate, W_up, W_down, E, K, I, out,
+                                router_logits, topk_idx, topk_w, aux);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
+        return MOE_OK;
+    }
+    Sizes s{T, H, E, K, I};
+    const size_t need = layout_workspace(s, nullptr, nullptr);
+    if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_ALIGNMENT;
+    Workspace ws;
+    layout_workspace(s, (char*)workspace, &ws);
+    return run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router,
+                       (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                       (const __nv_bfloat16*)W_down, s, norm_topk_prob, (__nv_bfloat16*)out,
+                       router_logits, topk_idx, topk_w, aux, ws, st);
+}
+
+int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router, const moe_bf16* W_gate,
+                const moe_bf16* W_up, const moe_bf16* W_down, int E, int K, int I,
+                int norm_topk_prob, moe_bf16* out, float* router_logits, int32_t* topk_idx,
+                float* topk_w, float* aux, void* stream) {
+    int rc = check_forward_args(x, T, H, W_router, W_gate, W_up, W_down, E, K, I, out,
+                                router_logits, topk_idx, topk_w, aux);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
+        return MOE_OK;
+    }
+    Sizes s{T, H, E, K, I};
+    const size_t need = layout_workspace(s, nullptr, nullptr);
+    void* base = nullptr;
+    rc = owned_workspace(st, need, &base);
+    if (rc) return rc;
+    Workspace ws;
+    layout_workspace(s, (char*)base, &ws);
+    rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router,
+                     (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                     (const __nv_bfloat16*)W_down, s, norm_topk_prob, (__nv_bfloat16*)out,
+                     router_logits, topk_idx, topk_w, aux, ws, st);
+    if (rc == MOE_OK) remember_counts(st, ws, E);
+    return rc;
+}
+
+int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                     const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down, int E,
+                     int K, int I, int norm_topk_prob, moe_bf16* out_host,
+                     float* router_logits_host, int32_t* topk_idx_host, float* topk_w_host,
+                     float* aux_host, void* stream) {
+    int rc = check_sizes(T, H, E, K, I);
+    if (rc) return rc;
+    if (!W_router || !W_gate || !W_up || !W_down) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x_host || !out_host)) return MOE_ERR_INVALID_ARG;
+    const void* dps[] = {W_router, W_gate, W_up, W_down};
+    for (const void* p : dps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        if (aux_host) *aux_host = 0.f;
+        return MOE_OK;
+    }
+    Sizes s{T, H, E, K, I};
+    const size_t need = layout_workspace(s, nullptr, nullptr);
+    const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4, kb = (size_t)T * K * 4;
+    const size_t stage = align_up(xb, 256) * 2 + align_up(lb, 256) + align_up(kb, 256) * 2 + 256;
+    void* base = nullptr;
+    rc = owned_workspace(st, need + stage, &base);
+    if (rc) return rc;
+    Workspace ws;
+    layout_workspace(s, (char*)base, &ws);
+    char* p = (char*)base + need;
+    __nv_bfloat16* x_d = (__nv_bfloat16*)p;
+    p += align_up(xb, 256);
+    __nv_bfloat16* out_d = (__nv_bfloat16*)p;
+    p += align_up(xb, 256);
+    float* logits_d = (float*)p;
+    p += align_up(lb, 256);
+    int32_t* idx_d = (int32_t*)p;
+    p += align_up(kb, 256);
+    float* w_d = (float*)p;
+    p += align_up(kb, 256);
+    float* aux_d = (float*)p;
+    cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, (const __nv_bfloat16*)W_gate,
+                     (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, s, norm_topk_prob,
+                     out_d, router_logits_host ? logits_d : nullptr, idx_d, w_d,
+                     aux_host ? aux_d : nullptr, ws, st);
+    if (rc) return rc;
+    remember_counts(st, ws, E);
+    e = cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && router_logits_host)
+        e = cudaMemcpyAsync(router_logits_host, logits_d, lb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && topk_idx_host)
+        e = cudaMemcpyAsync(topk_idx_host, idx_d, kb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && topk_w_host)
+        e = cudaMemcpyAsync(topk_w_host, w_d, kb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && aux_host)
+        e = cudaMemcpyAsync(aux_host, aux_d, sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
+
+int moe_last_expert_counts(int32_t* counts_host, int E, void* stream) {
+    if (!counts_host || E < 1) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t* src = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find(ws_key(st));
+        if (it == g_ws.end() || !it->second.counts || it->second.E != E)
+            return MOE_ERR_INVALID_ARG;
+        src = it->second.counts;
+    }
+    cudaError_t e = cudaMemcpyAsync(counts_host, src, (size_t)E * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
+
+int moe_device_status(const void* workspace, int T, int H, int E, int K, int I, void* stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t* status = nullptr;
+    if (workspace) {
+        if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+        Sizes s{T, H, E, K, I};
+        Workspace ws;
+        layout_workspace(s, (char*)workspace, &ws);
+        status = ws.status;
+    } else {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find(ws_key(st));
+        if (it == g_ws.end() || !it->second.status) return MOE_OK;
+        status = it->second.status;
+    }
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, status, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    return v == 0 ? MOE_OK : v;
+}
+
+int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm_topk_prob,
+                              int32_t* topk_idx, float* topk_w, void* stream) {
+    if (T < 0 || E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+    if (misaligned(logits) || misaligned(topk_idx) || misaligned(topk_w)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
+    if (rc) return rc;
+    if (T == 0) return MOE_OK;
+    Sizes s{T, 64, E, K, 64};
+    return cuda_status(launch_route_from_logits(logits, s, norm_topk_prob, topk_idx, topk_w,
+                                                nullptr, (cudaStream_t)stream));
+}
+
+int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
+                    void* stream) {
+    if (T < 0 || E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK)
+        return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || (T > 0 && (!topk_idx || !perm_tok || !perm_slot || !inv)))
+        return MOE_ERR_INVALID_ARG;
+    const void* ps[] = {topk_idx, counts, offsets, perm_tok, perm_slot, inv};
+    for (const void* p : ps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, (size_t)E * 4, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, ((size_t)E + 1) * 4, st);
+        return cuda_status(e);
+    }
+    Sizes s{T, 64, E, K, 64};
+    // Private scratch for the chunk tables and tiles (small), stream-ordered.
+    const size_t nch = (size_t)(s.nchunks() > 0 ? s.nchunks() : 1);
+    const size_t tb = (size_t)s.max_tiles(kStreamRows) * sizeof(RowTile);
+    const size_t bytes = align_up(nch * E * 4, 256) * 2 + align_up(tb, 256) + 256;
+    void* base = nullptr;
+    rc = owned_workspace(st, bytes, &base);
+    if (rc) return rc;
+    Workspace ws{};
+    char* p = (char*)base;
+    ws.chunk_counts = (int32_t*)p;
+    p += align_up(nch * E * 4, 256);
+    ws.chunk_base = (int32_t*)p;
+    p += align_up(nch * E * 4, 256);
+    ws.tiles = (RowTile*)p;
+    p += align_up(tb, 256);
+    ws.n_tiles = (int32_t*)p;
+    ws.counts = counts;
+    ws.offsets = offsets;
+    ws.perm_tok = perm_tok;
+    ws.perm_slot = perm_slot;
+    ws.inv = inv;
+    ws.w_perm = nullptr;
+    return cuda_status(
+        launch_dispatch(topk_idx, nullptr, nullptr, s, ws, kStreamRows, false, nullptr, nullptr, st));
+}
+
+int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H, moe_bf16* out,
+                    void* stream) {
+    if (T < 0 || K < 1 || K > kMaxTopK || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!Y || !inv || !out)) return MOE_ERR_INVALID_ARG;
+    if (misaligned(Y) || misaligned(inv) || misaligned(out)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
+    if (rc) return rc;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_combine((const __nv_bfloat16*)Y, inv, T, K, H, (__nv_bfloat16*)out,
+                                      (cudaStream_t)stream));
+}
+
+}  // extern "C"

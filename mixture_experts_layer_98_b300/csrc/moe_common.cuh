@@ -1,0 +1,96 @@
+// moe_common.cuh -- shared definitions of the CUDA library (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_b300.h"
+
+namespace moe {
+
+// ---- limits of this implementation ----------------------------------------
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 16;
+constexpr int kChunkTokens = 256;    // tokens per dispatch chunk (one CTA)
+constexpr int kRouterTokens = 32;    // tokens per router CTA (SIMT router)
+constexpr int kStreamRows = 8;       // rows per tile of the weight-streaming kernels
+constexpr int kTcRows = 128;         // rows per tile of the tcgen05 grouped GEMMs
+
+// One tile of token-expert rows, all routed to one expert: rows
+// [row0, row0 + nrows) of the dispatch order.
+struct __align__(16) RowTile {
+    int expert;
+    int row0;
+    int nrows;
+    int pad;
+};
+
+// Scratch regions carved from one workspace allocation (device pointers).
+struct Workspace {
+    int32_t* chunk_counts;  // [nchunks, E]
+    int32_t* chunk_base;    // [nchunks, E]
+    int32_t* counts;        // [E]
+    int32_t* offsets;       // [E + 1]
+    RowTile* tiles;         // [max_tiles]
+    int32_t* n_tiles;       // [1]
+    int32_t* status;        // [4] device-side error words
+    float* p_partial;       // [n_router_blocks, E]
+    int32_t* perm_tok;      // [P]
+    int32_t* perm_slot;     // [P]
+    int32_t* inv;           // [P]
+    float* w_perm;          // [P]
+    int32_t* topk_idx;      // [T, K] when the caller passes NULL
+    float* topk_w;          // [T, K] when the caller passes NULL
+    __nv_bfloat16* x_perm;  // [P, H]
+    __nv_bfloat16* hbuf;    // [P, I]
+    __nv_bfloat16* ybuf;    // [P, H]
+    size_t bytes;
+};
+
+struct Sizes {
+    int T, H, E, K, I;
+    long long P() const { return (long long)T * K; }
+    int nchunks() const { return (T + kChunkTokens - 1) / kChunkTokens; }
+    int nrouter() const { return (T + kRouterTokens - 1) / kRouterTokens; }
+    long long max_tiles(int rows_per_tile) const {
+        return (P() + rows_per_tile - 1) / rows_per_tile + E;
+    }
+};
+
+// Lays out (and, when base != nullptr, fills) the workspace; returns bytes.
+size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
+
+// ---- kernels' host launchers (each returns cudaError_t of the launch) ------
+cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
+                          int norm, float* logits, int32_t* idx, float* w, float* p_partial,
+                          int32_t* status, cudaStream_t st);
+cudaError_t launch_route_from_logits(const float* logits, const Sizes& s, int norm,
+                                     int32_t* idx, float* w, float* p_partial, cudaStream_t st);
+cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
+                            const Sizes& s, const Workspace& ws, int rows_per_tile,
+                            bool gather_x, const float* p_partial, float* aux,
+                            cudaStream_t st);
+cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                     const __nv_bfloat16* Wd, const Sizes& s,
+                                     const Workspace& ws, cudaStream_t st);
+cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                   const __nv_bfloat16* Wd, const Sizes& s,
+                                   const Workspace& ws, cudaStream_t st);
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
+                           __nv_bfloat16* out, cudaStream_t st);
+
+int num_sms();
+
+// ---- small device helpers --------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace moe

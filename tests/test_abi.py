@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function the header declares, and rejects bad sizes before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mixture_experts_layer_98_b300 import build
+    build.build()
+    import mixture_experts_layer_98_b300 as m
+    return m.lib()
+
+
+def test_header_declares_the_forward():
+    names = declared_functions()
+    assert "moe_forward" in names and "moe_forward_ws" in names
+    assert len(names) >= 10
+
+
+def test_every_declared_symbol_is_exported(L):
+    import mixture_experts_layer_98_b300 as m
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in moe_b300.h but not exported"
+    assert set(m.EXPORTS) == set(declared_functions())
+
+
+def test_strerror(L):
+    for s in range(7):
+        assert L.moe_strerror(s)
+    assert b"unknown" in L.moe_strerror(99)
+
+
+def test_set_expert_path(L):
+    assert L.moe_set_expert_path(7) == -1
+    prev = L.moe_set_expert_path(1)
+    assert L.moe_set_expert_path(prev) == 1
+
+
+def test_workspace_bytes(L):
+    ws = L.moe_workspace_bytes
+    assert ws(4096, 2048, 128, 8, 768) > 4096 * 8 * (2048 * 2 + 768) * 2
+    assert ws(-1, 2048, 128, 8, 768) == 0
+    assert ws(16, 100, 8, 2, 256) == 0        # H not a multiple of 64
+    assert ws(16, 128, 8, 9, 256) == 0        # K > E
+    assert ws(16, 128, 300, 2, 256) == 0      # E > 256
+    assert ws(16, 128, 64, 17, 256) == 0      # K > 16
+    assert ws(1, 128, 8, 2, 256) <= ws(2, 128, 8, 2, 256)
+
+
+@pytest.mark.parametrize("T,H,E,K,I", [(-1, 128, 8, 2, 256), (4, 96, 8, 2, 256),
+                                       (4, 128, 0, 1, 256), (4, 128, 8, 0, 256),
+                                       (4, 128, 8, 2, 100), (4, 128, 4, 5, 256)])
+def test_forward_rejects_bad_sizes_before_any_work(L, T, H, E, K, I):
+    z = ctypes.c_void_p(0)
+    rc = L.moe_forward(z, T, H, z, z, z, z, E, K, I, 1, z, z, z, z, z, z)
+    assert rc == 1  # MOE_ERR_INVALID_ARG, returned before any CUDA call
+
+
+def test_forward_rejects_null_weights(L):
+    z = ctypes.c_void_p(0)
+    assert L.moe_forward(z, 0, 128, z, z, z, z, 8, 2, 256, 1, z, z, z, z, z, z) == 1
+
+
+def test_forward_rejects_misaligned_pointers(L):
+    z = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(0x1000)
+    bad = ctypes.c_void_p(0x1002)
+    assert L.moe_forward(a, 4, 128, a, bad, a, a, 8, 2, 256, 1, a, z, z, z, z, z) == 2
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch):
+    import mixture_experts_layer_98_b300.binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", "/nonexistent/libmoe_b300.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        b.lib()

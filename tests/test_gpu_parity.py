@@ -1,0 +1,224 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Stage tests feed identical inputs to one stage (routing from given logits,
+dispatch from given selections, combine from given expert outputs) and require
+bit-exact integer results.  End-to-end tests run the whole block on every
+configuration of the workload set -- fully where the oracle is quick, on a
+seeded sample of token rows at the full prefill sizes -- through both expert
+paths (tcgen05 grouped GEMMs and weight streaming).
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from parity import compare, gpu_forward, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_ok):
+    import mixture_experts_layer_98_b300 as m
+    from mixture_experts_layer_98_b300 import build
+    build.build()
+    m.lib()
+    yield m
+    m.moe_set_expert_path(m.MOE_PATH_AUTO)
+
+
+@pytest.fixture
+def path(moe, request):
+    prev = moe.moe_set_expert_path(request.param)
+    yield request.param
+    moe.moe_set_expert_path(prev)
+
+
+PATHS = [pytest.param(2, id="tcgen05"), pytest.param(1, id="streaming")]
+
+
+# ---- stage parity -----------------------------------------------------------------
+
+@pytest.mark.parametrize("E,K", [(8, 2), (16, 4), (128, 8), (256, 16), (1, 1), (33, 7),
+                                 (64, 16)])
+@pytest.mark.parametrize("norm", [False, True])
+def test_route_from_logits_bit_exact(moe, E, K, norm):
+    rng = np.random.default_rng(E * 100 + K)
+    T = 300
+    l = (rng.standard_normal((T, E)) * 1.5).astype(np.float32)
+    l[:40] = np.round(l[:40] * 2) / 2  # exact ties
+    l[40:45] = 0.0                     # all equal
+    idx, w = moe.moe_dbg_route_from_logits(torch.from_numpy(l).cuda(), K, norm)
+    ridx, rw = oracle.route_from_logits(l, K, norm)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 1e-5
+
+
+@pytest.mark.parametrize("T,E,K", [(1, 8, 2), (255, 8, 2), (256, 16, 4), (257, 128, 8),
+                                   (4096, 128, 8), (1000, 256, 16), (37, 1, 1), (0, 8, 2)])
+def test_permute_bit_exact(moe, T, E, K):
+    rng = np.random.default_rng(T + E)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32).reshape(T, K)
+    d = moe.moe_dbg_permute(torch.from_numpy(idx).cuda(), E)
+    r = oracle.dispatch(idx, E)
+    assert np.array_equal(d["counts"].cpu().numpy(), r["counts"])
+    assert np.array_equal(d["offsets"].cpu().numpy(), r["offsets"])
+    if T:
+        assert np.array_equal(d["perm_tok"].cpu().numpy(), r["perm_tok"])
+        assert np.array_equal(d["perm_slot"].cpu().numpy(), r["perm_slot"])
+        assert np.array_equal(d["inv"].cpu().numpy(), r["inv"])
+
+
+def test_permute_skewed_all_to_one_expert(moe):
+    T, E, K = 3000, 16, 2
+    idx = np.zeros((T, K), np.int32)
+    idx[:, 1] = 5
+    d = moe.moe_dbg_permute(torch.from_numpy(idx).cuda(), E)
+    r = oracle.dispatch(idx, E)
+    for k in ("counts", "offsets", "perm_tok", "perm_slot"):
+        assert np.array_equal(d[k].cpu().numpy(), r[k]), k
+    assert np.array_equal(d["inv"].cpu().numpy(), r["inv"])
+
+
+@pytest.mark.parametrize("T,K,H", [(1, 1, 64), (77, 8, 2048), (300, 2, 128)])
+def test_combine(moe, T, K, H):
+    g = torch.Generator().manual_seed(T)
+    Y = torch.randn((T * K, H), generator=g).to(torch.bfloat16)
+    inv = torch.randperm(T * K, generator=g).to(torch.int32).view(T, K)
+    out = moe.moe_dbg_combine(Y.cuda(), inv.cuda()).cpu()
+    ref = torch.zeros((T, H), dtype=torch.float64)
+    for k in range(K):  # sum in k order, fp32 like the kernel's contract
+        ref += Y[inv[:, k].long()].to(torch.float64)
+    ref32 = torch.zeros((T, H), dtype=torch.float32)
+    for k in range(K):
+        ref32 += Y[inv[:, k].long()].to(torch.float32)
+    assert torch.equal(out, ref32.to(torch.bfloat16))
+    assert (out.to(torch.float64) - ref).abs().max() <= 2 ** -7 * ref.abs().max() + 1e-30
+
+
+# ---- end to end -------------------------------------------------------------------
+
+def run_case(cfg, rows=None):
+    inp = mi.make_inputs(cfg, "cuda")
+    g = gpu_forward(inp, cfg.K, cfg.norm)
+    b = host_bits(inp)
+    return compare(b, g, cfg.K, cfg.norm, rows=rows)
+
+
+@pytest.mark.parametrize("path", PATHS, indirect=True)
+def test_tiny(moe, path):
+    rep = run_case(mi.CONFIGS["tiny"])
+    assert rep["out_rel"] < 2e-2
+
+
+@pytest.mark.parametrize("path", PATHS, indirect=True)
+@pytest.mark.parametrize("T,H,E,K,I,norm", [
+    (1, 64, 1, 1, 64, False), (3, 128, 2, 1, 128, True), (17, 128, 8, 3, 192, True),
+    (129, 256, 16, 4, 128, False), (129, 128, 128, 8, 64, True), (300, 192, 8, 8, 320, True),
+    (513, 512, 32, 2, 256, True), (64, 128, 4, 4, 256, True)])
+def test_shape_fuzz(moe, path, T, H, E, K, I, norm):
+    cfg = mi.MoEConfig("fuzz", T, H, E, K, I, norm, seed=T + H + E)
+    run_case(cfg)
+
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t4", "decode_t16", "decode_t64"])
+def test_decode_sweep(moe, name):
+    run_case(mi.CONFIGS[name])
+
+
+@pytest.mark.parametrize("path", PATHS[:1], indirect=True)
+def test_prefill_h2048_sampled(moe, path):
+    cfg = mi.CONFIGS["prefill_h2048"]
+    run_case(cfg, rows=mi.sample_rows(cfg.T, 96))
+
+
+@pytest.mark.parametrize("name", ["prefill_h4096", "skew"])
+def test_large_sampled(moe, name):
+    cfg = mi.CONFIGS[name]
+    rep = run_case(cfg, rows=mi.sample_rows(cfg.T, 48))
+    assert rep["out_rel"] < 2e-2
+
+
+def test_zero_tokens(moe):
+    cfg = mi.MoEConfig("zero", 0, 128, 8, 2, 256, True)
+    inp = mi.make_inputs(cfg, "cuda")
+    out, logits, idx, w, aux = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
+                                               inp["W_up"], inp["W_down"], 2, True)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 128) and float(aux.cpu()[0]) == 0.0
+
+
+def test_all_tokens_one_expert(moe):
+    # x[:,0] = 1 with a large router bias column steers every token to experts 3, 6.
+    cfg = mi.MoEConfig("hot", 700, 256, 16, 2, 256, True, seed=3)
+    inp = mi.make_inputs(cfg, "cuda")
+    inp["x"][:, 0] = 1.0
+    inp["W_router"][:, 0] = 0.0
+    inp["W_router"][3, 0] = 30.0
+    inp["W_router"][6, 0] = 20.0
+    g = gpu_forward(inp, 2, True)
+    assert (g["idx"][:, 0] == 3).all() and (g["idx"][:, 1] == 6).all()
+    compare(host_bits(inp), g, 2, True)
+
+
+def test_deterministic(moe):
+    cfg = mi.CONFIGS["prefill_h2048"]
+    inp = mi.make_inputs(cfg, "cuda")
+    a = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                        cfg.K, cfg.norm)
+    a = [t.clone() for t in a]
+    b = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                        cfg.K, cfg.norm)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    assert moe.moe_device_status() == 0
+
+
+def test_forward_ws_and_host_agree(moe):
+    cfg = mi.MoEConfig("ws", 300, 256, 16, 4, 256, True, seed=5)
+    inp = mi.make_inputs(cfg, "cuda")
+    ref = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                          cfg.K, cfg.norm)
+    nbytes = moe.moe_workspace_bytes(cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    got = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                          cfg.K, cfg.norm, workspace=ws)
+    torch.cuda.synchronize()
+    for u, v in zip(ref, got):
+        assert torch.equal(u, v)
+    assert moe.moe_device_status(ws, (cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)) == 0
+    x_h = inp["x"].cpu().pin_memory()
+    out_h = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    lg_h = torch.empty((cfg.T, cfg.E), dtype=torch.float32).pin_memory()
+    aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    moe.moe_forward_host(x_h, inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], cfg.K,
+                         cfg.norm, out_h, router_logits_host=lg_h, aux_host=aux_h)
+    assert torch.equal(out_h, ref[0].cpu())
+    assert torch.equal(lg_h, ref[1].cpu())
+    assert torch.equal(aux_h, ref[4].cpu())
+    # too-small workspace is refused before any work
+    with pytest.raises(moe.MoEError):
+        moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                        cfg.K, cfg.norm, workspace=ws[: nbytes // 2])
+
+
+def test_paths_agree(moe):
+    cfg = mi.MoEConfig("paths", 1000, 512, 32, 4, 384, True, seed=9)
+    inp = mi.make_inputs(cfg, "cuda")
+    res = {}
+    for p in (1, 2):
+        prev = moe.moe_set_expert_path(p)
+        try:
+            res[p] = [t.clone() for t in moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
+                                                         inp["W_up"], inp["W_down"], cfg.K,
+                                                         cfg.norm)]
+        finally:
+            moe.moe_set_expert_path(prev)
+    torch.cuda.synchronize()
+    assert torch.equal(res[1][2], res[2][2])  # same routing
+    a = res[1][0].float()
+    b = res[2][0].float()
+    rms = b.pow(2).mean().sqrt()
+    assert (a - b).abs().max() <= 2e-2 * rms
