@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-MoE block forward on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one whole forward (router, dispatch, expert MLPs, combine, aux) of
+one synthetic batch of the named layer configuration (default: the Qwen3-style
+prefill layer T=4096 H=2048 E=128 K=8 I=768), inputs resident in HBM.  Each
+step is timed on the device with CUDA events on the launch stream; L2 is
+flushed (256 MB write) between steps, outside the events.  With N > 1 (torchrun)
+every rank runs an independent replica on its own batch (weak scaling, no
+collective on the data path); value = all ranks' tokens / max-over-ranks time.
+
+--impl reference times the CPU oracle (the plain fp64 C implementation) on
+bounded token samples of the same workload, on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 B300 and % of roofline (tensor peak or HBM GB/s)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+# the sources each stage's kernels are built from (a recorded DRAM-traffic figure
+# is only reported while these are unchanged)
+STAGE_SOURCES = {
+    "router": ["router.cu", "moe_common.cuh"],
+    "dispatch": ["dispatch.cu", "moe_common.cuh"],
+    "gate_up": ["experts_tc.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
+    "down": ["experts_tc.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
+    "combine": ["combine.cu", "moe_common.cuh"],
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="prefill_h2048", choices=sorted(mi.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--quiet-clocks", action="store_true", help="skip nvidia-smi sampling")
+    return ap.parse_args()
+
+
+# ---- distributed ------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- measured peaks ---------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", 0) or 0),
+                    source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                source="fallback")
+
+
+# ---- algorithmic work per stage: bytes and flops a launch must move or compute -----
+
+def stage_work(cfg, counts):
+    T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
+    P = T * K
+    touched = int((np.asarray(counts) > 0).sum())
+    return {
+        "router": dict(flops=2.0 * T * H * E, bytes=T * H * 2 + E * H * 2 + T * E * 4 + T * K * 8),
+        "dispatch": dict(flops=0.0, bytes=T * K * 8 + P * 16 + P * H * 2 * 2),
+        "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * 2 + P * H * 2 + P * I * 2),
+        "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * 2 + P * I * 2 + P * 4 + P * H * 2),
+        "combine": dict(flops=0.0, bytes=P * H * 2 + P * 4 + T * H * 2),
+    }, touched
+
+
+def block_work(cfg, counts):
+    """Whole-block roofline: routed FLOPs and the bytes of the touched experts'
+    weights plus the block's inputs and outputs (intermediates excluded)."""
+    T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
+    touched = int((np.asarray(counts) > 0).sum())
+    flops = 6.0 * T * K * H * I + 2.0 * T * H * E
+    byts = touched * 3 * H * I * 2 + E * H * 2 + T * H * 2 * 2 + T * E * 4 + T * K * 8 + 4
+    return flops, byts
+
+
+def kernel_source_sha(stage):
+    h = hashlib.sha256()
+    for n in STAGE_SOURCES[stage]:
+        with open(os.path.join(ROOT, "mixture_experts_layer_98_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(stage, config):
+    """DRAM bytes per launch of the stage's kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    e = d.get("entries", {}).get(f"{config}:{stage}")
+    if e is None or e.get("source_sha") != kernel_source_sha(stage):
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# ---- clocks -------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        import datetime
+
+        def ts(r):
+            try:
+                return datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return 0.0
+        inside = [r for r in rows if t0 - 0.1 <= ts(r) <= t1 + 0.1] or rows[-3:]
+        sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ---- CPU oracle baseline ---------------------------------------------------------------
+
+def oracle_sample_rate(cfg, bits, target_s, max_tokens=None):
+    """Time the oracle's full forward on the first n tokens of the batch
+    (n sized for about target_s seconds).  Returns (tokens/s, n, seconds, threads)."""
+    import oracle
+    T = bits["x"].shape[0]
+    per_tok = None
+    for n in (min(4, T), min(32, T)):  # the first call also pays one-time page-in costs
+        t = time.perf_counter()
+        oracle.moe_forward(bits["x"][:n], bits["W_router"], bits["W_gate"], bits["W_up"],
+                           bits["W_down"], cfg.K, cfg.norm)
+        per_tok = max((time.perf_counter() - t) / n, 1e-6)
+    n = int(max(4, min(T, target_s / per_tok)))
+    if max_tokens:
+        n = min(n, max_tokens)
+    t = time.perf_counter()
+    oracle.moe_forward(bits["x"][:n], bits["W_router"], bits["W_gate"], bits["W_up"],
+                       bits["W_down"], cfg.K, cfg.norm)
+    dt = time.perf_counter() - t
+    return n / dt, n, dt, oracle.threads()
+
+
+# ---- the reference arm: the CPU oracle -------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cfg = mi.CONFIGS[args.config]
+    inp = mi.make_inputs(cfg, "cpu")
+    bits = {k: mi.bits(v) for k, v in inp.items()}
+    import oracle
+    # size one step's token sample so that warmup + steps take about 2-3 minutes
+    per_step_s = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    _, n, _, threads = oracle_sample_rate(cfg, bits, per_step_s)
+    for _ in range(args.warmup):
+        oracle.moe_forward(bits["x"][:n], bits["W_router"], bits["W_gate"], bits["W_up"],
+                           bits["W_down"], cfg.K, cfg.norm)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.moe_forward(bits["x"][:n], bits["W_router"], bits["W_gate"], bits["W_up"],
+                           bits["W_down"], cfg.K, cfg.norm)
+        times.append(time.perf_counter() - t)
+    mean = sum(times) / len(times)
+    value = n / mean
+    sample = (f"first {n} of {cfg.T} tokens of {cfg.name} per step (full routing, dispatch, "
+              f"experts and combine for those tokens), fp64 C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(cfg, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg, world):
+    return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} K={cfg.K} I={cfg.I} "
+                        f"norm_topk_prob={str(cfg.norm).lower()}"
+                        + (f" zipf={cfg.zipf}" if cfg.zipf else ""),
+            "T": cfg.T, "H": cfg.H, "E": cfg.E, "K": cfg.K, "I": cfg.I, "norm_topk_prob": cfg.norm,
+            "seed": cfg.seed, "global_batch_tokens": cfg.T * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed between steps (256 MB write, outside the timed events); "
+                  "expert weights alone exceed L2"}
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_layer_98_b300 as moe
+    from mixture_experts_layer_98_b300 import build
+    if rank == 0:
+        build.build()
+    barrier(world)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = mi.CONFIGS[args.config]
+    inp = mi.make_inputs(cfg, dev, seed=cfg.seed + rank)
+    T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    aux = torch.empty((1,), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], K,
+                        cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w, aux=aux)
+
+    # warm-up: at least W steps and at least ~1 s of work so clocks settle
+    t_end = time.time() + 1.0
+    n = 0
+    while n < max(3, args.warmup) or time.time() < t_end:
+        step()
+        n += 1
+        if n % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    counts = moe.moe_last_expert_counts(E).numpy()
+
+    moe.moe_set_stage_timing(True)
+    sampler = ClockSampler(local)
+    if not args.quiet_clocks:
+        sampler.start()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = {k: [] for k in moe.STAGE_NAMES}
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = moe.moe_kernel_launch_count()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        ev0[k].record(stream)
+        step()
+        ev1[k].record(stream)
+        st = moe.moe_stage_times()  # waits for this step
+        for name, v in st.items():
+            stage_ms[name].append(v)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    launches = moe.moe_kernel_launch_count() - launches0
+    moe.moe_set_stage_timing(False)
+    rows = sampler.stop() if not args.quiet_clocks else None
+    clocks = ClockSampler.summarize(rows, t0, t1) if rows is not None else {"reasons": ["unsampled"]}
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    mean_ms = sum(step_ms) / len(step_ms)
+    mean_ms_all = max_over_ranks(mean_ms, world, dev)
+    value = T * world / (mean_ms_all * 1e-3)
+    assert moe.moe_device_status() == 0, "device-side timeout during the benchmark"
+
+    pk = peaks()
+    work, touched = stage_work(cfg, counts)
+    stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+    dom = max(stage_mean, key=stage_mean.get)
+    wk = work[dom]
+    t_s = stage_mean[dom] * 1e-3
+    t_flop = wk["flops"] / (pk["bf16_tflops"] * 1e12)
+    t_byte = wk["bytes"] / (pk["hbm_gbs"] * 1e9)
+    if t_flop >= t_byte:
+        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(dom, cfg.name)
+    roof["kernel"] = dom
+    roof["kernel_ms"] = stage_mean[dom]
+    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
+    roof["peak_source"] = pk["source"] + " (burst figures: the kernel is timed alone per step)"
+    bf, bb = block_work(cfg, counts)
+    t_roof = max(bf / (pk["bf16_tflops"] * 1e12), bb / (pk["hbm_gbs"] * 1e9))
+    block = {"flops": bf, "bytes": bb, "t_roof_us": t_roof * 1e6, "t_us": mean_ms * 1e3,
+             "frac": t_roof / (mean_ms * 1e-3),
+             "tensor_frac": bf / (mean_ms * 1e-3) / (pk["bf16_tflops"] * 1e12),
+             "hbm_frac": bb / (mean_ms * 1e-3) / (pk["hbm_gbs"] * 1e9),
+             "touched_experts": touched}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bits = {k: mi.bits(v) for k, v in inp.items()}
+        rate, n, dt, threads = oracle_sample_rate(cfg, bits, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {n} of {T} tokens of {cfg.name} (full forward for those tokens), "
+                         f"{dt:.1f} s, fp64 C oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(cfg, world), "roofline": roof, "block_roofline": block,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                       "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
+            "stage_ms": {k: round(v, 5) for k, v in stage_mean.items()},
+            "expert_path": "tcgen05" if T * K >= 32 * E else "streaming",
+        }
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev):
+    T, H, E, K = cfg.T, cfg.H, cfg.E, cfg.K
+    x_h = inp["x"].cpu().pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    lg_h = torch.empty((T, E), dtype=torch.float32).pin_memory()
+    aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def call():
+        moe.moe_forward_host(x_h, inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], K,
+                             cfg.norm, out_h, router_logits_host=lg_h, aux_host=aux_h)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    times = []
+    barrier(world)
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        call()  # returns with the results in host memory
+        times.append(time.perf_counter() - t)
+    mean = sum(times) / len(times)
+    mean = max_over_ranks(mean, world, dev)
+    return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+            "d2h_bytes_per_step": T * H * 2 + T * E * 4 + 4, "ms_per_step": mean * 1e3,
+            "api": "moe_forward_host (pinned host x in; out, router_logits, aux out)"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -140,6 +140,32 @@ int moe_last_cuda_error(void);
 enum moe_path { MOE_PATH_AUTO = 0, MOE_PATH_STREAMING = 1, MOE_PATH_TCGEN05 = 2 };
 int moe_set_expert_path(int path);
 
+/* ---- benchmark instrumentation ------------------------------------------ */
+
+/* Stages of one forward, in launch order. */
+enum moe_stage {
+    MOE_STAGE_ROUTER = 0,   /* router GEMM + softmax + top-k + renorm            */
+    MOE_STAGE_DISPATCH = 1, /* histogram, scan, permutation, aux, row gather      */
+    MOE_STAGE_GATE_UP = 2,  /* expert gate/up projections + SiLU·mul             */
+    MOE_STAGE_DOWN = 3,     /* expert down projection × routing weight           */
+    MOE_STAGE_COMBINE = 4,  /* gather-reduce into token order                     */
+    MOE_NUM_STAGES = 5
+};
+
+/* enable != 0: every following forward records a CUDA event at each stage
+ * boundary on its own stream (process-wide; meant for one benchmarking
+ * stream at a time).  Returns MOE_OK, or MOE_ERR_CUDA if the events could not
+ * be created. */
+int moe_set_stage_timing(int enable);
+
+/* Waits for the events of the last forward recorded with stage timing and
+ * writes the device time of each stage in milliseconds to ms[0..n) (n <=
+ * MOE_NUM_STAGES).  MOE_ERR_INVALID_ARG if no forward was timed. */
+int moe_stage_times(float* ms, int n);
+
+/* Number of kernels this library has launched in this process. */
+long long moe_kernel_launch_count(void);
+
 /* ---- stage entry points (used by the stage-parity tests) --------------- */
 
 /* Steps softmax -> top-k -> renormalise on given fp32 logits [T,E]:

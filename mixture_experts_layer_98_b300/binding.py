@@ -24,8 +24,11 @@ MOE_PATH_TCGEN05 = 2
 
 EXPORTS = ["moe_forward", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
-           "moe_set_expert_path", "moe_dbg_route_from_logits", "moe_dbg_permute",
+           "moe_set_expert_path", "moe_set_stage_timing", "moe_stage_times",
+           "moe_kernel_launch_count", "moe_dbg_route_from_logits", "moe_dbg_permute",
            "moe_dbg_combine"]
+MOE_NUM_STAGES = 5
+STAGE_NAMES = ["router", "dispatch", "gate_up", "down", "combine"]
 
 
 class MoEError(RuntimeError):
@@ -61,6 +64,10 @@ def lib():
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_last_cuda_error.argtypes = []
         L.moe_set_expert_path.argtypes = [i]
+        L.moe_set_stage_timing.argtypes = [i]
+        L.moe_stage_times.argtypes = [P, i]
+        L.moe_kernel_launch_count.argtypes = []
+        L.moe_kernel_launch_count.restype = ctypes.c_longlong
         L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P]
         L.moe_dbg_permute.argtypes = [P, i, i, i, P, P, P, P, P, P]
         L.moe_dbg_combine.argtypes = [P, P, i, i, i, P, P]
@@ -187,6 +194,21 @@ def moe_set_expert_path(path):
     if prev < 0:
         raise ValueError(f"unknown expert path {path}")
     return prev
+
+
+def moe_set_stage_timing(enable):
+    _call(lib().moe_set_stage_timing(int(bool(enable))), "moe_set_stage_timing")
+
+
+def moe_stage_times():
+    """Per-stage device milliseconds of the last forward timed with stage timing."""
+    ms = (ctypes.c_float * MOE_NUM_STAGES)()
+    _call(lib().moe_stage_times(ms, MOE_NUM_STAGES), "moe_stage_times")
+    return dict(zip(STAGE_NAMES, [float(v) for v in ms]))
+
+
+def moe_kernel_launch_count():
+    return int(lib().moe_kernel_launch_count())
 
 
 def moe_dbg_route_from_logits(logits, K, norm_topk_prob, stream=None):

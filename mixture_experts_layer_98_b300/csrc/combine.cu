@@ -55,6 +55,7 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, in
     if (blocks < 1) blocks = 1;
     combine_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(Y), inv, T, K, vpr,
                                                 reinterpret_cast<uint4*>(out));
+    count_launches(1);
     return cudaGetLastError();
 }
 

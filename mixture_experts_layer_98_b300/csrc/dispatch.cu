@@ -159,6 +159,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
     dispatch_scatter_kernel<<<nch, kChunkTokens, 0, st>>>(idx, w, s.T, s.E, s.K, ws.chunk_base,
                                                           ws.perm_tok, ws.perm_slot, ws.inv,
                                                           ws.w_perm);
+    count_launches(3);
     if (gather_x && x) {
         const long long P = s.P();
         const int vpr = s.H / 8;
@@ -169,6 +170,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
         gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x),
                                                         ws.perm_tok, P, vpr,
                                                         reinterpret_cast<uint4*>(ws.x_perm));
+        count_launches(1);
     }
     return cudaGetLastError();
 }

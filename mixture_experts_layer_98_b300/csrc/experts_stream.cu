@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
 
 cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                      const __nv_bfloat16* Wd, const Sizes& s,
-                                     const Workspace& ws, cudaStream_t st) {
+                                     const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid) {
     const int sms = num_sms();
     const size_t smem_gu = (size_t)kStreamRows * s.H * 2;
     const size_t smem_dn = (size_t)kStreamRows * s.I * 2;
@@ -191,8 +191,10 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat1
                                                       ws.hbuf, s.H, s.I);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (ev_mid) cudaEventRecord(ev_mid, st);
     down_stream_kernel<<<g_dn, 256, smem_dn, st>>>(ws.hbuf, ws.tiles, ws.n_tiles, Wd, ws.w_perm,
                                                     ws.ybuf, s.H, s.I);
+    count_launches(2);
     return cudaGetLastError();
 }
 

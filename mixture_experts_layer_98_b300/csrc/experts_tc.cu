@@ -342,6 +342,7 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     grouped_gemm_tc_kernel<MODE, BN><<<(int)grid, kThreads, C::kSmemBytes, st>>>(ma, mb0, mb1, p);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -349,7 +350,7 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
 
 cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                    const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, cudaEvent_t ev_mid) {
     const long long P = s.P();
     const long long max_tiles = s.max_tiles(kBM);
     TcParams p{};
@@ -374,6 +375,7 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
                                       max_tiles * p.n_nt, st);
     }
     if (err != cudaSuccess) return err;
+    if (ev_mid) cudaEventRecord(ev_mid, st);
 
     // down: B = W_down rows [n0, n0 + BN) of expert e
     p.num_kb = s.I / kBK;

@@ -7,6 +7,7 @@
 //   -> combine (gather-reduce into token order)
 //
 // No host synchronisation: the expert kernels read the tile count on the device.
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -16,6 +17,18 @@ namespace moe {
 
 static thread_local int g_last_cuda_error = 0;
 static int g_expert_path = MOE_PATH_AUTO;
+static std::atomic<long long> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Stage-boundary events (benchmark instrumentation), MOE_NUM_STAGES + 1 of them.
+static bool g_timing = false;
+static bool g_timed_once = false;
+static cudaEvent_t g_ev[MOE_NUM_STAGES + 1] = {};
+
+static void mark(int boundary, cudaStream_t st) {
+    if (g_timing) cudaEventRecord(g_ev[boundary], st);
+}
 
 int num_sms() {
     int dev = 0, n = 0;
@@ -162,16 +175,24 @@ static int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __
                        const Workspace& ws, cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
+    mark(0, st);
     cudaError_t e = launch_router(x, Wr, s, norm, logits, idx, w, ws.p_partial, ws.status, st);
     if (e != cudaSuccess) return cuda_status(e);
+    mark(1, st);
     const bool tc = use_tcgen05(s);
     e = launch_dispatch(idx, w, x, s, ws, tc ? kTcRows : kStreamRows, true, ws.p_partial, aux, st);
     if (e != cudaSuccess) return cuda_status(e);
-    e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st)
-           : launch_experts_streaming(Wg, Wu, Wd, s, ws, st);
+    mark(2, st);
+    cudaEvent_t mid = g_timing ? g_ev[3] : nullptr;
+    e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid)
+           : launch_experts_streaming(Wg, Wu, Wd, s, ws, st, mid);
     if (e != cudaSuccess) return cuda_status(e);
+    mark(4, st);
     e = launch_combine(ws.ybuf, ws.inv, s.T, s.K, s.H, out, st);
-    return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e);
+    mark(5, st);
+    if (g_timing) g_timed_once = true;
+    return MOE_OK;
 }
 
 static int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
@@ -209,6 +230,30 @@ const char* moe_strerror(int status) {
 }
 
 int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+long long moe_kernel_launch_count(void) { return g_launches.load(); }
+
+int moe_set_stage_timing(int enable) {
+    if (enable && !g_ev[0]) {
+        for (int i = 0; i <= MOE_NUM_STAGES; ++i) {
+            cudaError_t e = cudaEventCreate(&g_ev[i]);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+    }
+    g_timing = enable != 0;
+    return MOE_OK;
+}
+
+int moe_stage_times(float* ms, int n) {
+    if (!ms || n < 1 || n > MOE_NUM_STAGES || !g_timed_once) return MOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaEventSynchronize(g_ev[MOE_NUM_STAGES]);
+    if (e != cudaSuccess) return cuda_status(e);
+    for (int i = 0; i < n; ++i) {
+        e = cudaEventElapsedTime(&ms[i], g_ev[i], g_ev[i + 1]);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return MOE_OK;
+}
 
 int moe_set_expert_path(int path) {
     if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05) return -1;

@@ -71,16 +71,20 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
                             bool gather_x, const float* p_partial, float* aux,
                             cudaStream_t st);
+// ev_mid (may be null) is recorded between the gate/up and the down launch.
 cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                      const __nv_bfloat16* Wd, const Sizes& s,
-                                     const Workspace& ws, cudaStream_t st);
+                                     const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
 cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                    const __nv_bfloat16* Wd, const Sizes& s,
-                                   const Workspace& ws, cudaStream_t st);
+                                   const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
                            __nv_bfloat16* out, cudaStream_t st);
 
 int num_sms();
+
+// Every launcher adds the number of kernels it launched.
+void count_launches(int n);
 
 // ---- small device helpers --------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -221,6 +221,7 @@ cudaError_t launch_router_t(const __nv_bfloat16* x, const __nv_bfloat16* Wr, con
     if (err != cudaSuccess) return err;
     router_simt_kernel<EPL><<<s.nrouter(), 256, smem, st>>>(x, Wr, s.T, s.H, s.E, s.K, norm,
                                                             logits, idx, w, p_partial, status);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -229,6 +230,7 @@ cudaError_t launch_route_t(const float* logits, const Sizes& s, int norm, int32_
                            float* p_partial, cudaStream_t st) {
     route_from_logits_kernel<EPL><<<s.nrouter(), 256, 0, st>>>(logits, s.T, s.E, s.K, norm, idx,
                                                                w, p_partial);
+    count_launches(1);
     return cudaGetLastError();
 }
 

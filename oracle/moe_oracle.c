@@ -243,10 +243,12 @@ int oracle_expert_mlp(const uint16_t* x_row, int H, const uint16_t* Wg, const ui
 
 /* ---- step 7: combine (weighted sum over the token's K experts) ---------- */
 
-/* out_row[h] = bf16( Σ_k w_k · MLP_{idx_k}(x_row)[h] ), the sum in double. */
-int oracle_token_output(const uint16_t* x_row, int H, const int32_t* idx_row,
-                        const float* w_row, int K, const uint16_t* Wg, const uint16_t* Wu,
-                        const uint16_t* Wd, int E, int I, int flags, uint16_t* out_row) {
+/* out_row[h] = bf16( Σ_k w_k · MLP_{idx_k}(x_row)[h] ), the sum in double.
+ * out_f64_row (may be NULL) receives the sum before that final rounding. */
+int oracle_token_output_ex(const uint16_t* x_row, int H, const int32_t* idx_row,
+                           const float* w_row, int K, const uint16_t* Wg, const uint16_t* Wu,
+                           const uint16_t* Wd, int E, int I, int flags, uint16_t* out_row,
+                           double* out_f64_row) {
     double* acc = (double*)calloc((size_t)H, sizeof(double));
     double* y = (double*)malloc((size_t)H * sizeof(double));
     if (!acc || !y) { free(acc); free(y); return 2; }
@@ -259,10 +261,20 @@ int oracle_token_output(const uint16_t* x_row, int H, const int32_t* idx_row,
                                Wd + (size_t)e * blk, I, flags, y);
         for (int h = 0; h < H; ++h) acc[h] += (double)w_row[k] * y[h];
     }
-    for (int h = 0; h < H; ++h) out_row[h] = oracle_f64_to_bf16(acc[h]);
+    for (int h = 0; h < H; ++h) {
+        if (out_row) out_row[h] = oracle_f64_to_bf16(acc[h]);
+        if (out_f64_row) out_f64_row[h] = acc[h];
+    }
     free(acc);
     free(y);
     return rc;
+}
+
+int oracle_token_output(const uint16_t* x_row, int H, const int32_t* idx_row,
+                        const float* w_row, int K, const uint16_t* Wg, const uint16_t* Wu,
+                        const uint16_t* Wd, int E, int I, int flags, uint16_t* out_row) {
+    return oracle_token_output_ex(x_row, H, idx_row, w_row, K, Wg, Wu, Wd, E, I, flags, out_row,
+                                  NULL);
 }
 
 /* ---- step 8: load-balance statistic ------------------------------------- */
@@ -287,13 +299,14 @@ double oracle_aux(const double* probs, const int32_t* counts, int T, int E, int 
 
 /* Full forward.  Routing, dispatch and aux cover all T tokens; the block
  * output is produced for the n_rows tokens listed in rows (all tokens, in
- * order, when rows == NULL), into out[n_rows, H].  Any of logits / idx / w /
- * aux / counts may be NULL.  Returns 0 on success. */
+ * order, when rows == NULL), into out[n_rows, H] (bf16) and, when out_f64 is
+ * not NULL, out_f64[n_rows, H] (the same values before the bf16 rounding).
+ * Any of logits / idx / w / aux / counts may be NULL.  Returns 0 on success. */
 int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, const uint16_t* Wg,
                        const uint16_t* Wu, const uint16_t* Wd, int E, int K, int I, int norm,
                        int flags, const int32_t* rows, int n_rows, uint16_t* out,
-                       float* logits_out, int32_t* idx_out, float* w_out, float* aux_out,
-                       int32_t* counts_out) {
+                       double* out_f64, float* logits_out, int32_t* idx_out, float* w_out,
+                       float* aux_out, int32_t* counts_out) {
     if (T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || I < 1) return 1;
     if (T == 0) {
         if (aux_out) *aux_out = 0.0f;
@@ -315,15 +328,17 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
         for (size_t i = 0; i < TK; ++i) counts[idx[i]] += 1;
         if (aux_out) *aux_out = (float)oracle_aux(probs, counts, T, E, K);
     }
-    if (!rc && out) {
+    if (!rc && (out || out_f64)) {
         int n = rows ? n_rows : T;
         int fail = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
         for (int j = 0; j < n; ++j) {
             int t = rows ? rows[j] : j;
             if (t < 0 || t >= T) { fail |= 1; continue; }
-            if (oracle_token_output(x + (size_t)t * H, H, idx + (size_t)t * K, w + (size_t)t * K, K,
-                                    Wg, Wu, Wd, E, I, flags, out + (size_t)j * H))
+            if (oracle_token_output_ex(x + (size_t)t * H, H, idx + (size_t)t * K,
+                                       w + (size_t)t * K, K, Wg, Wu, Wd, E, I, flags,
+                                       out ? out + (size_t)j * H : NULL,
+                                       out_f64 ? out_f64 + (size_t)j * H : NULL))
                 fail |= 1;
         }
         if (fail) rc = 3;

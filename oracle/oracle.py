@@ -36,10 +36,11 @@ class _Lib:
         lib.oracle_dispatch.argtypes = [P, i, i, i, P, P, P, P, P]
         lib.oracle_expert_mlp.argtypes = [P, i, P, P, P, i, i, P]
         lib.oracle_token_output.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P]
+        lib.oracle_token_output_ex.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P, P]
         lib.oracle_aux.argtypes = [P, P, i, i, i]
         lib.oracle_aux.restype = ctypes.c_double
         lib.oracle_moe_forward.argtypes = [P, i, i, P, P, P, P, i, i, i, i, i, P, i, P, P, P,
-                                           P, P, P]
+                                           P, P, P, P]
         self.c = lib
 
 
@@ -168,17 +169,20 @@ def expert_mlp(x_row, Wg_e, Wu_e, Wd_e, flags=0):
     return y
 
 
-def token_output(x_row, idx_row, w_row, Wg, Wu, Wd, flags=0):
-    """bf16(Σ_k w_k·MLP_{idx_k}(x_row)) -> uint16 [H] for an explicit selection."""
+def token_output(x_row, idx_row, w_row, Wg, Wu, Wd, flags=0, unrounded=False):
+    """bf16(Σ_k w_k·MLP_{idx_k}(x_row)) -> uint16 [H] for an explicit selection;
+    with unrounded=True also the float64 sum before rounding: (bits, f64)."""
     x_row = _c(x_row, np.uint16)
     idx_row = _c(idx_row, np.int32)
     w_row = _c(w_row, np.float32)
     Wg, Wu, Wd = (_c(a, np.uint16) for a in (Wg, Wu, Wd))
     E, I, H = Wg.shape
     out = np.empty(H, np.uint16)
-    _check(_L().oracle_token_output(_p(x_row), H, _p(idx_row), _p(w_row), idx_row.shape[0],
-                                    _p(Wg), _p(Wu), _p(Wd), E, I, flags, _p(out)), "token_output")
-    return out
+    f64 = np.empty(H, np.float64) if unrounded else None
+    _check(_L().oracle_token_output_ex(_p(x_row), H, _p(idx_row), _p(w_row), idx_row.shape[0],
+                                       _p(Wg), _p(Wu), _p(Wd), E, I, flags, _p(out), _p(f64)),
+           "token_output")
+    return (out, f64) if unrounded else out
 
 
 def aux(probs, counts, K):
@@ -190,10 +194,11 @@ def aux(probs, counts, K):
 
 
 def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True):
-    """The whole block.  Returns dict(out, logits, idx, w, aux, counts).
+    """The whole block.  Returns dict(out, out_f64, logits, idx, w, aux, counts).
 
     out is bf16 bits [n_rows, H] for the listed token rows (all tokens when
-    rows is None); routing, dispatch counts and aux always cover every token.
+    rows is None) and out_f64 the same values before the final bf16 rounding;
+    routing, dispatch counts and aux always cover every token.
     """
     x = _c(x, np.uint16)
     Wr, Wg, Wu, Wd = (_c(a, np.uint16) for a in (Wr, Wg, Wu, Wd))
@@ -206,15 +211,17 @@ def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True):
     else:
         n = T
     out = np.empty((n, H), np.uint16) if want_out else None
+    out_f64 = np.empty((n, H), np.float64) if want_out else None
     logits = np.empty((T, E), np.float32)
     idx = np.empty((T, K), np.int32)
     w = np.empty((T, K), np.float32)
     counts = np.empty(E, np.int32)
     a = np.zeros(1, np.float32)
     _check(_L().oracle_moe_forward(_p(x), T, H, _p(Wr), _p(Wg), _p(Wu), _p(Wd), E, K, I,
-                                   int(bool(norm)), flags, _p(rows), n, _p(out), _p(logits),
-                                   _p(idx), _p(w), _p(a), _p(counts)), "forward")
-    return dict(out=out, logits=logits, idx=idx, w=w, aux=float(a[0]), counts=counts)
+                                   int(bool(norm)), flags, _p(rows), n, _p(out), _p(out_f64),
+                                   _p(logits), _p(idx), _p(w), _p(a), _p(counts)), "forward")
+    return dict(out=out, out_f64=out_f64, logits=logits, idx=idx, w=w, aux=float(a[0]),
+                counts=counts)
 
 
 def near_tie_tokens(probs, K, gap=1e-6):

@@ -59,7 +59,7 @@ def test_route_from_logits_bit_exact(moe, E, K, norm):
                                    (4096, 128, 8), (1000, 256, 16), (37, 1, 1), (0, 8, 2)])
 def test_permute_bit_exact(moe, T, E, K):
     rng = np.random.default_rng(T + E)
-    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32).reshape(T, K)
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)], np.int32).reshape(T, K)
     d = moe.moe_dbg_permute(torch.from_numpy(idx).cuda(), E)
     r = oracle.dispatch(idx, E)
     assert np.array_equal(d["counts"].cpu().numpy(), r["counts"])
@@ -109,7 +109,7 @@ def run_case(cfg, rows=None):
 @pytest.mark.parametrize("path", PATHS, indirect=True)
 def test_tiny(moe, path):
     rep = run_case(mi.CONFIGS["tiny"])
-    assert rep["out_rel"] < 2e-2
+    assert rep["out_excess"] <= 0
 
 
 @pytest.mark.parametrize("path", PATHS, indirect=True)
@@ -137,7 +137,7 @@ def test_prefill_h2048_sampled(moe, path):
 def test_large_sampled(moe, name):
     cfg = mi.CONFIGS[name]
     rep = run_case(cfg, rows=mi.sample_rows(cfg.T, 48))
-    assert rep["out_rel"] < 2e-2
+    assert rep["out_excess"] <= 0
 
 
 def test_zero_tokens(moe):

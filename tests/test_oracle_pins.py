@@ -169,11 +169,14 @@ def pin_single_expert_is_swiglu():
         x = bf16_bits_to_f64(b["x"])
         y = np_swiglu(x, bf16_bits_to_f64(b["W_gate"][0]), bf16_bits_to_f64(b["W_up"][0]),
                       bf16_bits_to_f64(b["W_down"][0]))
+        assert np.abs(r["out_f64"] - y).max() <= 1e-6 * np.abs(y).max()
         ref = f64_rne_bf16_value(y)
         got = bf16_bits_to_f64(r["out"])
         ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
         assert (np.abs(got - ref) <= ulp).all()
         assert np.mean(got == ref) > 0.99
+        # the delivered bf16 output is the round-to-nearest-even of the unrounded sum
+        assert np.array_equal(got, f64_rne_bf16_value(r["out_f64"]))
 
 
 def _dense_reference(b, idx, w, E, round_a=True):
@@ -198,10 +201,15 @@ def pin_dense_equivalence():
         _, b = rand_case(T, H, E, K, I, seed=7 + T, norm=norm)
         r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], K,
                                norm, flags=oracle.FP64_INTERMEDIATE)
-        ref = f64_rne_bf16_value(_dense_reference(b, r["idx"], r["w"], E, round_a=False))
+        ref = _dense_reference(b, r["idx"], r["w"], E, round_a=False)
+        assert np.abs(r["out_f64"] - ref).max() <= 1e-12 * np.abs(ref).max()
         got = bf16_bits_to_f64(r["out"])
-        assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all()
-        assert np.mean(got == ref) > 0.98
+        assert (np.abs(got - f64_rne_bf16_value(ref)) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all()
+        # with the default bf16 rounding of the SwiGLU intermediate
+        r2 = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], K,
+                                norm)
+        ref2 = _dense_reference(b, r2["idx"], r2["w"], E, round_a=True)
+        assert np.abs(r2["out_f64"] - ref2).max() <= 1e-6 * np.abs(ref2).max()
 
 
 def pin_soft_router():
@@ -217,8 +225,9 @@ def pin_soft_router():
         acc += p[:, [e]] * np_swiglu(x, bf16_bits_to_f64(b["W_gate"][e]),
                                      bf16_bits_to_f64(b["W_up"][e]),
                                      bf16_bits_to_f64(b["W_down"][e]), round_a=False)
-    ref = f64_rne_bf16_value(acc)
+    assert np.abs(r["out_f64"] - acc).max() <= 1e-6 * np.abs(acc).max()
     got = bf16_bits_to_f64(r["out"])
+    ref = f64_rne_bf16_value(acc)
     assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -6 + 1e-30).all()
 
 
