@@ -85,6 +85,34 @@ int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                 float* router_logits, int32_t* topk_idx, float* topk_w, float* aux,
                 void* stream);
 
+/* moe_forward for callers that cannot allocate device memory.  The pages have
+ * no counterpart of this entry point; it exists for integrations where
+ * allocating on the call path is not allowed: a runtime that fixed its memory
+ * budget up front, host code that must not take the allocator's locks or wait
+ * on its implicit synchronisation, or an embedding whose device memory belongs
+ * to another runtime.  Arguments and results are exactly those of
+ * moe_forward; the caller still provides every input and output buffer.
+ *
+ * Scratch: a 32 MiB array that is part of the loaded library (a __device__
+ * variable), so nothing is allocated by the call.  Every GPU that loads the
+ * library holds those 32 MiB until the process exits.  Sizes whose
+ * moe_workspace_bytes(T,H,E,K,I) exceeds 32 MiB are rejected with
+ * MOE_ERR_WORKSPACE before any work (e.g. the H=4096, E=128, K=8, I=1536
+ * layer fits up to T = 215 tokens).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents (nothing in it needs to start at zero: each call writes
+ * every part before reading it).  Calls whose work overlaps on the GPU --
+ * concurrent streams, or host threads racing on one device -- race on the
+ * array; serialise them. */
+int moe_forward_noalloc(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                        const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                        int E, int K, int I, int norm_topk_prob, moe_bf16* out,
+                        float* router_logits, int32_t* topk_idx, float* topk_w, float* aux,
+                        void* stream);
+
 /* Bytes of device workspace moe_forward_ws needs for these sizes (0 on a size
  * error).  The requirement grows with T·K·(H+I); it does not depend on data. */
 size_t moe_workspace_bytes(int T, int H, int E, int K, int I);

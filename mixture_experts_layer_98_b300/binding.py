@@ -22,7 +22,7 @@ MOE_PATH_AUTO = 0
 MOE_PATH_STREAMING = 1
 MOE_PATH_TCGEN05 = 2
 
-EXPORTS = ["moe_forward", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
+EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
            "moe_set_expert_path", "moe_set_stage_timing", "moe_stage_times",
            "moe_kernel_launch_count", "moe_dbg_route_from_logits", "moe_dbg_permute",
@@ -56,6 +56,7 @@ def lib():
         L.moe_forward.argtypes = fwd + [P]
         L.moe_forward_ws.argtypes = fwd + [P, sz, P]
         L.moe_forward_host.argtypes = fwd + [P]
+        L.moe_forward_noalloc.argtypes = fwd + [P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
         L.moe_last_expert_counts.argtypes = [P, i, P]

@@ -102,7 +102,7 @@ static int check_device() {
     return it->second ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
 }
 
-static int cuda_status(cudaError_t e) {
+int cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return MOE_OK;
     g_last_cuda_error = (int)e;
     return MOE_ERR_CUDA;
@@ -169,7 +169,7 @@ static bool use_tcgen05(const Sizes& s) {
 }
 
 // The kernel sequence.  All pointers checked by the caller.
-static int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
+int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
                        const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Sizes& s, int norm,
                        __nv_bfloat16* out, float* logits, int32_t* idx, float* w, float* aux,
                        const Workspace& ws, cudaStream_t st) {
@@ -195,7 +195,7 @@ static int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __
     return MOE_OK;
 }
 
-static int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
+int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
                               const void* Wu, const void* Wd, int E, int K, int I, const void* out,
                               const void* logits, const void* idx, const void* w,
                               const void* aux) {

@@ -83,6 +83,20 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, in
 
 int num_sms();
 
+
+// MOE_OK for cudaSuccess, else records the error for moe_last_cuda_error and
+// returns MOE_ERR_CUDA (moe_api.cu).
+int cuda_status(cudaError_t e);
+
+// The forward's argument checks and its kernel sequence (moe_api.cu).
+int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
+                       const void* Wu, const void* Wd, int E, int K, int I, const void* out,
+                       const void* logits, const void* idx, const void* w, const void* aux);
+int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
+                const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Sizes& s, int norm,
+                __nv_bfloat16* out, float* logits, int32_t* idx, float* w, float* aux,
+                const Workspace& ws, cudaStream_t st);
+
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);
 
