@@ -45,16 +45,23 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
     return acc;
 }
 
-// Stages rows [row0, row0+nrows) of a [P, D] bf16 matrix into shared memory.
-__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ src, int row0,
-                                           int nrows, int D, uint4* dst) {
+// Stages rows [row0, row0+nrows) of a [P, D] bf16 matrix into shared memory;
+// with perm != null, dispatch row r is row perm[r] of src (a gather from x).
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ src,
+                                           const int32_t* __restrict__ perm, int row0, int nrows,
+                                           int D, uint4* dst) {
     const int vpr = D / 8;
-    const uint4* s = reinterpret_cast<const uint4*>(src) + (size_t)row0 * vpr;
-    for (int i = threadIdx.x; i < nrows * vpr; i += blockDim.x) dst[i] = s[i];
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+    for (int i = threadIdx.x; i < nrows * vpr; i += blockDim.x) {
+        const int m = i / vpr, c = i % vpr;
+        const size_t r = perm ? (size_t)perm[row0 + m] : (size_t)(row0 + m);
+        dst[i] = s[r * vpr + c];
+    }
 }
 
 __global__ void __launch_bounds__(256) gateup_stream_kernel(
-    const __nv_bfloat16* __restrict__ x_perm, const RowTile* __restrict__ tiles,
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm_tok,
+    const RowTile* __restrict__ tiles,
     const int32_t* __restrict__ n_tiles_p, const __nv_bfloat16* __restrict__ Wg,
     const __nv_bfloat16* __restrict__ Wu, __nv_bfloat16* __restrict__ h, int H, int I) {
     extern __shared__ uint4 xs[];  // [kStreamRows][H/8]
@@ -66,7 +73,7 @@ __global__ void __launch_bounds__(256) gateup_stream_kernel(
         const RowTile tl = tiles[item / nblk];
         const int i0 = (int)(item % nblk) * kRowsPerItem + wid * kRowsPerWarp;
         __syncthreads();
-        stage_rows(x_perm, tl.row0, tl.nrows, H, xs);
+        stage_rows(x, perm_tok, tl.row0, tl.nrows, H, xs);
         __syncthreads();
         float g[kRowsPerWarp][kStreamRows], u[kRowsPerWarp][kStreamRows];
 #pragma unroll
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
         const RowTile tl = tiles[item / nblk];
         const int n0 = (int)(item % nblk) * kRowsPerItem + wid * kRowsPerWarp;
         __syncthreads();
-        stage_rows(hbuf, tl.row0, tl.nrows, I, hs);
+        stage_rows(hbuf, nullptr, tl.row0, tl.nrows, I, hs);
         __syncthreads();
         float acc[kRowsPerWarp][kStreamRows];
 #pragma unroll
@@ -168,17 +175,16 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
 
 }  // namespace
 
-cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                     const __nv_bfloat16* Wd, const Sizes& s,
-                                     const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid) {
+cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16* Wg,
+                                     const __nv_bfloat16* Wu, const __nv_bfloat16* Wd,
+                                     const Sizes& s, const Workspace& ws, cudaStream_t st,
+                                     cudaEvent_t ev_mid) {
     const int sms = num_sms();
     const size_t smem_gu = (size_t)kStreamRows * s.H * 2;
     const size_t smem_dn = (size_t)kStreamRows * s.I * 2;
-    cudaError_t err = cudaFuncSetAttribute(gateup_stream_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
+    cudaError_t err = ensure_smem((const void*)gateup_stream_kernel, (int)smem_gu);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(down_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_dn);
+    err = ensure_smem((const void*)down_stream_kernel, (int)smem_dn);
     if (err != cudaSuccess) return err;
     // Upper bound on the items; the kernels read the real tile count on the device.
     const long long max_tiles = s.max_tiles(kStreamRows);
@@ -187,8 +193,8 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat1
     const long long cap = (long long)sms * 4;
     const int g_gu = (int)(items_gu < cap ? items_gu : cap);
     const int g_dn = (int)(items_dn < cap ? items_dn : cap);
-    gateup_stream_kernel<<<g_gu, 256, smem_gu, st>>>(ws.x_perm, ws.tiles, ws.n_tiles, Wg, Wu,
-                                                      ws.hbuf, s.H, s.I);
+    gateup_stream_kernel<<<g_gu, 256, smem_gu, st>>>(x, ws.perm_tok, ws.tiles, ws.n_tiles, Wg,
+                                                      Wu, ws.hbuf, s.H, s.I);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (ev_mid) cudaEventRecord(ev_mid, st);

@@ -26,8 +26,6 @@
 // Every wait is bounded (2 s); on expiry the CTA records MOE_ERR_TIMEOUT in
 // the workspace status word, drains its in-flight copies and MMAs, frees TMEM
 // and exits.
-#include <cudaTypedefs.h>
-
 #include "moe_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -296,47 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side ----------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] -> tensor map with a box of box_rows x 64
-// columns, 128-byte swizzle, zero fill outside the matrix.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int MODE, int BN>
 cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const void* B0,
                       const void* B1, uint64_t b_rows, const TcParams& p, long long max_items,
                       cudaStream_t st) {
     using C = TcCfg<MODE, BN>;
     CUtensorMap ma, mb0, mb1;
-    if (!make_map(&ma, A, a_rows, a_cols, kBM) || !make_map(&mb0, B0, b_rows, a_cols, BN / 2) ||
-        !make_map(&mb1, B1, b_rows, a_cols, BN / 2))
+    if (!make_tma_2d(&ma, A, a_rows, a_cols, kBM) ||
+        !make_tma_2d(&mb0, B0, b_rows, a_cols, BN / 2) ||
+        !make_tma_2d(&mb1, B1, b_rows, a_cols, BN / 2))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, BN>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::kSmemBytes);
+    cudaError_t err = ensure_smem((const void*)grouped_gemm_tc_kernel<MODE, BN>, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     long long grid = num_sms();
     if (grid > max_items) grid = max_items;
@@ -359,7 +327,7 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
     p.status = ws.status;
     p.w_perm = ws.w_perm;
 
-    // gate/up: B = [BN/2 gate rows ; BN/2 up rows] of expert e
+    // gate/up: A = x_perm rows of the tile; B = [BN/2 gate rows ; BN/2 up rows] of expert e
     p.num_kb = s.H / kBK;
     p.b_rows_per_expert = s.I;
     p.out = ws.hbuf;
@@ -377,7 +345,7 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
     if (err != cudaSuccess) return err;
     if (ev_mid) cudaEventRecord(ev_mid, st);
 
-    // down: B = W_down rows [n0, n0 + BN) of expert e
+    // down: A = h rows of the tile; B = W_down rows [n0, n0 + BN) of expert e
     p.num_kb = s.I / kBK;
     p.b_rows_per_expert = s.H;
     p.out = ws.ybuf;

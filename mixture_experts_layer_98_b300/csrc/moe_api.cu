@@ -2,7 +2,7 @@
 // sequence of kernels for one forward of the sparse MoE block.
 //
 //   router (logits, softmax, top-k, renorm, probability sums)
-//   -> dispatch (counts, offsets, permutation, row tiles, aux, x gather)
+//   -> dispatch (counts, offsets, permutation, row tiles, aux, row gather)
 //   -> expert MLPs (tcgen05 grouped GEMMs, or weight streaming for small batches)
 //   -> combine (gather-reduce into token order)
 //
@@ -30,11 +30,31 @@ static void mark(int boundary, cudaStream_t st) {
     if (g_timing) cudaEventRecord(g_ev[boundary], st);
 }
 
+static std::mutex g_attr_mu;
+
 int num_sms() {
-    int dev = 0, n = 0;
+    static int cache[64] = {};
+    int dev = 0;
     cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
+    if (n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+cudaError_t ensure_smem(const void* func, int bytes) {
+    static std::unordered_map<unsigned long long, int> done;  // (device, func) -> bytes set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long key = (unsigned long long)(uintptr_t)func * 64ull + (unsigned)dev;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[key] = bytes;
+    return e;
 }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -61,6 +81,7 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
     w.perm_slot = (int32_t*)take(P * 4);
     w.inv = (int32_t*)take(P * 4);
     w.w_perm = (float*)take(P * 4);
+    w.logits = (float*)take((size_t)s.T * s.E * 4);
     w.topk_idx = (int32_t*)take(P * 4);
     w.topk_w = (float*)take(P * 4);
     w.x_perm = (__nv_bfloat16*)take(P * s.H * 2);
@@ -176,16 +197,24 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
     mark(0, st);
-    cudaError_t e = launch_router(x, Wr, s, norm, logits, idx, w, ws.p_partial, ws.status, st);
+    // Tensor-core router from one full 128-token tile up (E <= 128); else the CUDA-core
+    // router, whose logits kernel spreads the experts over many CTAs.
+    const bool router_tc = s.T >= 128 && router_tc_supported(s);
+    cudaError_t e = router_tc
+                        ? launch_router_tc(x, Wr, s, norm, logits, idx, w, ws.p_partial, ws.status, st)
+                        : launch_router(x, Wr, s, norm, logits, ws.logits, idx, w, ws.p_partial,
+                                        ws.status, st);
     if (e != cudaSuccess) return cuda_status(e);
+    const int n_partials = router_tc ? router_tc_partials(s.T) : s.nrouter();
     mark(1, st);
     const bool tc = use_tcgen05(s);
-    e = launch_dispatch(idx, w, x, s, ws, tc ? kTcRows : kStreamRows, true, ws.p_partial, aux, st);
+    e = launch_dispatch(idx, w, tc ? x : nullptr, s, ws, tc ? kTcRows : kStreamRows, ws.p_partial,
+                        n_partials, aux, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
     cudaEvent_t mid = g_timing ? g_ev[3] : nullptr;
     e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid)
-           : launch_experts_streaming(Wg, Wu, Wd, s, ws, st, mid);
+           : launch_experts_streaming(x, Wg, Wu, Wd, s, ws, st, mid);
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
     e = launch_combine(ws.ybuf, ws.inv, s.T, s.K, s.H, out, st);
@@ -475,7 +504,7 @@ int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* count
     ws.inv = inv;
     ws.w_perm = nullptr;
     return cuda_status(
-        launch_dispatch(topk_idx, nullptr, nullptr, s, ws, kStreamRows, false, nullptr, nullptr, st));
+        launch_dispatch(topk_idx, nullptr, nullptr, s, ws, kStreamRows, nullptr, 0, nullptr, st));
 }
 
 int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H, moe_bf16* out,

@@ -1,6 +1,7 @@
 // moe_common.cuh -- shared definitions of the CUDA library (sm_103a only).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -40,9 +41,10 @@ struct Workspace {
     int32_t* perm_slot;     // [P]
     int32_t* inv;           // [P]
     float* w_perm;          // [P]
+    float* logits;          // [T, E] when the caller passes NULL
     int32_t* topk_idx;      // [T, K] when the caller passes NULL
     float* topk_w;          // [T, K] when the caller passes NULL
-    __nv_bfloat16* x_perm;  // [P, H]
+    __nv_bfloat16* x_perm;  // [P, H] (tcgen05 path)
     __nv_bfloat16* hbuf;    // [P, I]
     __nv_bfloat16* ybuf;    // [P, H]
     size_t bytes;
@@ -62,26 +64,49 @@ struct Sizes {
 size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ------
+// CUDA-core router: expert-split logits kernel + per-token routing kernel;
+// writes s.nrouter() rows of probability sums.  logits_scratch [T,E] is used
+// when logits == null.
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, int32_t* idx, float* w, float* p_partial,
-                          int32_t* status, cudaStream_t st);
+                          int norm, float* logits, float* logits_scratch, int32_t* idx, float* w,
+                          float* p_partial, int32_t* status, cudaStream_t st);
+// tcgen05 router (128-token tiles); writes router_tc_partials(T) rows of
+// probability sums.
+cudaError_t launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
+                             int norm, float* logits, int32_t* idx, float* w, float* p_partial,
+                             int32_t* status, cudaStream_t st);
+int router_tc_partials(int T);
+bool router_tc_supported(const Sizes& s);  // E <= 128
 cudaError_t launch_route_from_logits(const float* logits, const Sizes& s, int norm,
                                      int32_t* idx, float* w, float* p_partial, cudaStream_t st);
+// p_partial holds n_partials rows of per-expert probability sums (for aux).
+// x != null: also gather x_perm[row] = x[perm_tok[row]].
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
-                            bool gather_x, const float* p_partial, float* aux,
-                            cudaStream_t st);
+                            const float* p_partial, int n_partials, float* aux, cudaStream_t st);
 // ev_mid (may be null) is recorded between the gate/up and the down launch.
-cudaError_t launch_experts_streaming(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                     const __nv_bfloat16* Wd, const Sizes& s,
-                                     const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
+// The streaming kernels stage their input rows from x through ws.perm_tok;
+// the tcgen05 kernels read the gathered rows from ws.x_perm.
+cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16* Wg,
+                                     const __nv_bfloat16* Wu, const __nv_bfloat16* Wd,
+                                     const Sizes& s, const Workspace& ws, cudaStream_t st,
+                                     cudaEvent_t ev_mid);
 cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                    const __nv_bfloat16* Wd, const Sizes& s,
                                    const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
                            __nv_bfloat16* out, cudaStream_t st);
 
-int num_sms();
+int num_sms();  // of the current device (cached)
+
+// Raises func's dynamic shared-memory limit to at least `bytes` on the current
+// device (once per device and kernel; later calls are a cached no-op).
+cudaError_t ensure_smem(const void* func, int bytes);
+
+// Row-major bf16 matrix [rows, cols] -> 2-D TMA map with a box of box_rows x 64
+// columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
+bool make_tma_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
 
 
 // MOE_OK for cudaSuccess, else records the error for moe_last_cuda_error and

@@ -1,4 +1,5 @@
-// router.cu -- router GEMM fused with fp32 softmax, top-k and renormalisation.
+// router.cu -- CUDA-core router (decode-sized batches, and E > 128): logits,
+// then fp32 softmax, top-k and renormalisation.
 //
 // Follows the routing steps of Qwen3MoeSparseMoeBlock.forward (cnblogs page
 // "大模型-qwen3 MoE 详细解读"): router_logits = gate(hidden_states) with a
@@ -7,15 +8,14 @@
 //
 // Ranking is done on the fp32 logits (the same order as on the probabilities,
 // without exp rounding creating ties), descending, ties to the lower expert
-// index.  Each CTA also writes, per expert, the sum of the probabilities of its
-// tokens (in token order) for the load-balance statistic.
+// index.  The routing CTAs also write, per expert, the sum of the
+// probabilities of their tokens (in token order) for the load-balance
+// statistic.
 #include "moe_common.cuh"
 
 namespace moe {
 
 namespace {
-
-constexpr int kHC = 32;  // hidden-dimension chunk staged in shared memory
 
 // (value, expert, prob) of the best candidate: larger value first, then the
 // lower expert index.
@@ -108,78 +108,60 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
     }
 }
 
-// x [T,H] bf16, Wr [E,H] bf16 -> logits, idx, w, per-CTA probability sums.
-// CTA = 256 threads = 8 token groups of 4 tokens; lane -> experts lane+32q.
-template <int EPL>
-__global__ void __launch_bounds__(256) router_simt_kernel(
+constexpr int kSplitWarps = 8;   // experts per logits CTA (one warp each)
+constexpr int kSplitTokens = 8;  // tokens per logits CTA (staged in shared memory)
+
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b, float acc) {
+    acc = fmaf(bf16_lo(a.x), bf16_lo(b.x), acc);
+    acc = fmaf(bf16_hi(a.x), bf16_hi(b.x), acc);
+    acc = fmaf(bf16_lo(a.y), bf16_lo(b.y), acc);
+    acc = fmaf(bf16_hi(a.y), bf16_hi(b.y), acc);
+    acc = fmaf(bf16_lo(a.z), bf16_lo(b.z), acc);
+    acc = fmaf(bf16_hi(a.z), bf16_hi(b.z), acc);
+    acc = fmaf(bf16_lo(a.w), bf16_lo(b.w), acc);
+    acc = fmaf(bf16_hi(a.w), bf16_hi(b.w), acc);
+    return acc;
+}
+
+// logits[t,e] = x[t]·W_router[e] in fp32.  Grid (ceil(T/8), ceil(E/8)): a CTA
+// stages 8 token rows in shared memory and each of its 8 warps streams one
+// router row with 16-byte loads, so even a single token spreads the router
+// weights over E/8 SMs.  The first CTA also clears the forward's status word.
+__global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wr, int T, int H,
-    int E, int K, int norm, float* __restrict__ logits, int32_t* __restrict__ idx,
-    float* __restrict__ w, float* __restrict__ p_partial, int32_t* __restrict__ status) {
-    extern __shared__ float sm[];
-    if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0;  // first kernel of a forward
-    float* xs = sm;                             // [32][kHC + 1]
-    float* wsm = xs + kRouterTokens * (kHC + 1);  // [kHC][E]
-    float* ls = wsm + kHC * E;                  // [32][E] logits, then probabilities
-    const int tid = threadIdx.x, lane = tid & 31, tg = tid >> 5;
-    const int t0 = blockIdx.x * kRouterTokens;
-
-    float acc[4][EPL];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) acc[j][q] = 0.f;
-
-    for (int h0 = 0; h0 < H; h0 += kHC) {
-        for (int i = tid; i < kRouterTokens * kHC; i += 256) {
-            const int t = i / kHC, c = i % kHC;
-            xs[t * (kHC + 1) + c] =
-                (t0 + t < T) ? __bfloat162float(x[(size_t)(t0 + t) * H + h0 + c]) : 0.f;
-        }
-        for (int i = tid; i < E * kHC; i += 256) {
-            const int e = i / kHC, c = i % kHC;
-            wsm[c * E + e] = __bfloat162float(Wr[(size_t)e * H + h0 + c]);
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int c = 0; c < kHC; ++c) {
-            float xv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) xv[j] = xs[(tg * 4 + j) * (kHC + 1) + c];
-#pragma unroll
-            for (int q = 0; q < EPL; ++q) {
-                const int e = lane + 32 * q;
-                const float wv = (e < E) ? wsm[c * E + e] : 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[j][q] = fmaf(xv[j], wv, acc[j][q]);
-            }
-        }
-        __syncthreads();
-    }
-
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int t = t0 + tg * 4 + j;
-        if (t >= T) continue;  // warp-uniform
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-            const int e = lane + 32 * q;
-            if (e < E && logits) logits[(size_t)t * E + e] = acc[j][q];
-        }
-        route_token<EPL>(acc[j], E, K, norm, idx + (size_t)t * K, w + (size_t)t * K,
-                         ls + (tg * 4 + j) * E);
-    }
+    int E, float* __restrict__ logits, int32_t* __restrict__ status) {
+    extern __shared__ uint4 xs[];  // [kSplitTokens][H/8]
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+    const int vpr = H / 8;
+    const int t0 = blockIdx.x * kSplitTokens;
+    const int nt = min(kSplitTokens, T - t0);
+    const uint4* xg = reinterpret_cast<const uint4*>(x) + (size_t)t0 * vpr;
+    for (int i = threadIdx.x; i < nt * vpr; i += blockDim.x) xs[i] = __ldg(xg + i);
     __syncthreads();
-    if (p_partial) {
-        const int nt = min(kRouterTokens, T - t0);
-        for (int e = tid; e < E; e += 256) {
-            float s = 0.f;
-            for (int t = 0; t < nt; ++t) s += ls[t * E + e];
-            p_partial[(size_t)blockIdx.x * E + e] = s;
-        }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.y * kSplitWarps + warp;
+    if (e >= E) return;
+    const uint4* wr = reinterpret_cast<const uint4*>(Wr) + (size_t)e * vpr;
+    float acc[kSplitTokens];
+#pragma unroll
+    for (int m = 0; m < kSplitTokens; ++m) acc[m] = 0.f;
+#pragma unroll 4
+    for (int c = lane; c < vpr; c += 32) {
+        const uint4 wv = __ldg(wr + c);
+#pragma unroll
+        for (int m = 0; m < kSplitTokens; ++m)
+            if (m < nt) acc[m] = dot8_bf16(wv, xs[m * vpr + c], acc[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < kSplitTokens; ++m) {
+        float v = acc[m];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == m && m < nt) logits[(size_t)(t0 + m) * E + e] = v;
     }
 }
 
-// Routing only, from given logits (same per-token code as the fused kernel).
+// Routing from logits: one warp per token, kRouterTokens tokens per CTA.
 // CTA = 256 threads, one warp per token, kRouterTokens tokens per CTA.
 template <int EPL>
 __global__ void __launch_bounds__(256) route_from_logits_kernel(
@@ -211,21 +193,6 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(
 }
 
 template <int EPL>
-cudaError_t launch_router_t(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                            int norm, float* logits, int32_t* idx, float* w, float* p_partial,
-                            int32_t* status, cudaStream_t st) {
-    const size_t smem =
-        sizeof(float) * (kRouterTokens * (kHC + 1) + kHC * s.E + kRouterTokens * s.E);
-    cudaError_t err = cudaFuncSetAttribute(router_simt_kernel<EPL>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    router_simt_kernel<EPL><<<s.nrouter(), 256, smem, st>>>(x, Wr, s.T, s.H, s.E, s.K, norm,
-                                                            logits, idx, w, p_partial, status);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
-template <int EPL>
 cudaError_t launch_route_t(const float* logits, const Sizes& s, int norm, int32_t* idx, float* w,
                            float* p_partial, cudaStream_t st) {
     route_from_logits_kernel<EPL><<<s.nrouter(), 256, 0, st>>>(logits, s.T, s.E, s.K, norm, idx,
@@ -237,13 +204,19 @@ cudaError_t launch_route_t(const float* logits, const Sizes& s, int norm, int32_
 }  // namespace
 
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, int32_t* idx, float* w, float* p_partial,
-                          int32_t* status, cudaStream_t st) {
-    const int epl = (s.E + 31) / 32;
-    if (epl <= 1) return launch_router_t<1>(x, Wr, s, norm, logits, idx, w, p_partial, status, st);
-    if (epl <= 2) return launch_router_t<2>(x, Wr, s, norm, logits, idx, w, p_partial, status, st);
-    if (epl <= 4) return launch_router_t<4>(x, Wr, s, norm, logits, idx, w, p_partial, status, st);
-    return launch_router_t<8>(x, Wr, s, norm, logits, idx, w, p_partial, status, st);
+                          int norm, float* logits, float* logits_scratch, int32_t* idx, float* w,
+                          float* p_partial, int32_t* status, cudaStream_t st) {
+    float* lg = logits ? logits : logits_scratch;
+    const int smem = kSplitTokens * s.H * 2;
+    cudaError_t err = ensure_smem((const void*)router_logits_split_kernel, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((s.T + kSplitTokens - 1) / kSplitTokens, (s.E + kSplitWarps - 1) / kSplitWarps);
+    router_logits_split_kernel<<<grid, kSplitWarps * 32, smem, st>>>(x, Wr, s.T, s.H, s.E, lg,
+                                                                     status);
+    count_launches(1);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_route_from_logits(lg, s, norm, idx, w, p_partial, st);
 }
 
 cudaError_t launch_route_from_logits(const float* logits, const Sizes& s, int norm, int32_t* idx,

@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -53,17 +47,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// timeout_ns of wall time, or as soon as *abort becomes non-zero; returns
-// false in both cases (and sets *abort on a timeout).
+// about timeout_ns of wall time (measured with the SM cycle counter at the
+// maximum 2.032 GHz clock, so a slower clock only lengthens the limit), or as
+// soon as *abort becomes non-zero; returns false in both cases (and sets
+// *abort on a timeout).  The clock is read only every 64 polls: the fast path
+// is a bare try_wait.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    const long long limit = (long long)(timeout_ns * 2.032);
+    const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0u) {
             if (*abort) return false;
-            if (globaltimer() - t0 > timeout_ns) {
+            if (clock64() - t0 > limit) {
                 *abort = 1;
                 return false;
             }

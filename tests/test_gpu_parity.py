@@ -222,3 +222,34 @@ def test_paths_agree(moe):
     b = res[2][0].float()
     rms = b.pow(2).mean().sqrt()
     assert (a - b).abs().max() <= 2e-2 * rms
+
+
+@pytest.mark.parametrize("T", [64, 300])  # SIMT router below 128 tokens, tcgen05 router above
+@pytest.mark.parametrize("norm", [False, True])
+def test_router_exact_ties_zero_weights(moe, T, norm):
+    # W_router = 0: every logit is exactly 0 on both sides -> experts 0..K-1,
+    # weights 1/E (or 1/K renormalised), aux = 1
+    cfg = mi.MoEConfig("zeros", T, 256, 16, 4, 128, norm, seed=11)
+    inp = mi.make_inputs(cfg, "cuda")
+    inp["W_router"].zero_()
+    g = gpu_forward(inp, cfg.K, norm)
+    assert (g["idx"] == np.arange(cfg.K)).all()
+    assert np.abs(g["w"] - (1.0 / cfg.K if norm else 1.0 / cfg.E)).max() < 1e-6
+    assert abs(g["aux"] - 1.0) < 1e-5
+    compare(host_bits(inp), g, cfg.K, norm)
+
+
+@pytest.mark.parametrize("T", [100, 700])
+def test_router_exact_ties_duplicate_rows(moe, T):
+    # experts 2j and 2j+1 share a router row, so their logits tie exactly:
+    # whenever 2j+1 is selected, 2j must be selected right before it
+    cfg = mi.MoEConfig("dups", T, 512, 32, 6, 128, True, seed=12)
+    inp = mi.make_inputs(cfg, "cuda")
+    inp["W_router"][1::2] = inp["W_router"][0::2]
+    g = gpu_forward(inp, cfg.K, cfg.norm)
+    for t in range(T):
+        row = g["idx"][t].tolist()
+        for k, e in enumerate(row):
+            if e % 2 == 1:
+                assert k > 0 and row[k - 1] == e - 1, (t, row)
+    compare(host_bits(inp), g, cfg.K, cfg.norm)
