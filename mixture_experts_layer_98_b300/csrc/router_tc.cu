@@ -17,8 +17,10 @@
 //              k-block's partial logits into fp32 registers (round to nearest),
 //              then writes the logits, keeps a sorted top-KMAX list while
 //              taking the row maximum, computes the exp-sum and the weights, and
-//              finally the column sums of the probabilities over the tile
-//              (through a shared-memory transpose, in a fixed order)
+//              finally the column sums of the probabilities over the tile; the
+//              row is staged in shared memory (reusing the drained stage ring)
+//              so these passes run as compact rolled loops, and the column sums
+//              are one expert per thread over the rows in order
 // Accumulating in TMEM over only 64 products per k-block and summing the
 // k-blocks in registers keeps the logits within ~1e-6 relative of the exact
 // dot product; one accumulation chain over all of H drifts by ~1e-5 at
@@ -38,7 +40,7 @@ constexpr int kRK = 64;
 constexpr int kRStages = 4;
 constexpr int kRThreads = 192;
 constexpr uint64_t kRTimeoutNs = 2000000000ull;
-constexpr int kRedBytes = 4 * 32 * 33 * 4 + 4 * kMaxExperts * 4;  // transpose + warp column sums
+constexpr int kRowPitch = 129;  // floats per staged logits row (odd: conflict-free columns)
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -57,8 +59,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float* tbuf = reinterpret_cast<float*>(smem + kRStages * kStageBytes);  // [4][32][33]
-    float* colsum = tbuf + 4 * 32 * 33;                                      // [4][kMaxExperts]
     __shared__ __align__(8) uint64_t full_bar[kRStages];
     __shared__ __align__(8) uint64_t empty_bar[kRStages];
     __shared__ __align__(8) uint64_t tfull_bar[2];
@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
     } else {
         // ---------------- epilogue: one token per thread ----------------
-        const int ew = warp - 2;  // 0..3
         const int q = warp & 3;   // TMEM lane quadrant
         const int r = q * 32 + lane;
         const int t = t0 + r;
@@ -192,6 +191,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty_bar[buf]);
         }
+        // The mainloop is over (every MMA has completed, so the stage buffers are
+        // free): park the row in shared memory and run the epilogue passes as
+        // rolled loops -- fully unrolled they would be tens of KB of straight-line
+        // code executed once, bound by instruction fetch.
+        float* rows = reinterpret_cast<float*>(smem);  // [128][kRowPitch]
+        float* myrow = rows + r * kRowPitch;
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < N; ++j) myrow[j] = acc[j];
+        }
+        __syncwarp();
         if (ok) {
             // logits out, row max, sorted top-KMAX: experts arrive in increasing
             // index, so a new logit equal to the last kept one ranks after it;
@@ -204,46 +214,30 @@ __global__ void __launch_bounds__(kRThreads, 1)
                 ti[j] = 0x7fffffff;
             }
             float m = -INFINITY;
-            if (valid && logits) {
-                if ((E & 3) == 0) {
-                    float4* dst = reinterpret_cast<float4*>(logits + (size_t)t * E);
+#pragma unroll 1
+            for (int e = 0; e < E; ++e) {
+                const float l = myrow[e];
+                if (valid && logits) logits[(size_t)t * E + e] = l;
+                m = fmaxf(m, l);
+                if (l > tv[KMAX - 1]) {
+                    float cv = l;
+                    int ce = e;
 #pragma unroll
-                    for (int j = 0; j < N / 4; ++j)
-                        if (4 * j < E)
-                            dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2],
-                                                 acc[4 * j + 3]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < N; ++e)
-                        if (e < E) logits[(size_t)t * E + e] = acc[e];
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < N; ++e) {
-                if (e < E) {
-                    const float l = acc[e];
-                    m = fmaxf(m, l);
-                    if (l > tv[KMAX - 1]) {
-                        float cv = l;
-                        int ce = e;
-#pragma unroll
-                        for (int s = 0; s < KMAX; ++s) {
-                            if (cv > tv[s] || (cv == tv[s] && ce < ti[s])) {
-                                const float fv = tv[s];
-                                const int fe = ti[s];
-                                tv[s] = cv;
-                                ti[s] = ce;
-                                cv = fv;
-                                ce = fe;
-                            }
+                    for (int s2 = 0; s2 < KMAX; ++s2) {
+                        if (cv > tv[s2] || (cv == tv[s2] && ce < ti[s2])) {
+                            const float fv = tv[s2];
+                            const int fe = ti[s2];
+                            tv[s2] = cv;
+                            ti[s2] = ce;
+                            cv = fv;
+                            ce = fe;
                         }
                     }
                 }
             }
             float ssum = 0.f;
-#pragma unroll
-            for (int e = 0; e < N; ++e)
-                if (e < E) ssum += expf(acc[e] - m);
+#pragma unroll 1
+            for (int e = 0; e < E; ++e) ssum += expf(myrow[e] - m);
             const float inv_s = 1.0f / ssum;
             float wsum = 0.f;
 #pragma unroll
@@ -253,26 +247,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
                     if (j < K) {
-                        const float p = expf(tv[j] - m) * inv_s;
+                        const float pj = expf(tv[j] - m) * inv_s;
                         idx[(size_t)t * K + j] = ti[j];
-                        wout[(size_t)t * K + j] = norm ? p / wsum : p;
+                        wout[(size_t)t * K + j] = norm ? pj / wsum : pj;
                     }
                 }
             }
-            // column sums of p over this warp's 32 rows (fixed order)
-            float* tb = tbuf + ew * 32 * 33;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    tb[lane * 33 + j] =
-                        (valid && c * 32 + j < E) ? expf(acc[c * 32 + j] - m) * inv_s : 0.f;
-                __syncwarp();
-                float cs = 0.f;
-                for (int rr = 0; rr < 32; ++rr) cs += tb[rr * 33 + lane];
-                colsum[ew * kMaxExperts + c * 32 + lane] = cs;
-            }
+            // the row now holds this token's probabilities (zero for padding rows)
+#pragma unroll 1
+            for (int e = 0; e < E; ++e) myrow[e] = valid ? expf(myrow[e] - m) * inv_s : 0.f;
         } else if (lane == 0) {
             atomicExch(status, MOE_ERR_TIMEOUT);
         }
@@ -280,11 +263,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
         ptx::tc_fence_before();
         epi_bar();
         if (!abort_s) {
+            // column sums: thread e adds expert e's probability over the 128 rows in order
             const int tid = threadIdx.x - 64;  // 0..127
-            for (int e = tid; e < E; e += 128)
-                p_partial[(size_t)blockIdx.x * E + e] =
-                    ((colsum[e] + colsum[kMaxExperts + e]) + colsum[2 * kMaxExperts + e]) +
-                    colsum[3 * kMaxExperts + e];
+            for (int e = tid; e < E; e += 128) {
+                float cs = 0.f;
+#pragma unroll 8
+                for (int rr = 0; rr < kRM; ++rr) cs += rows[rr * kRowPitch + e];
+                p_partial[(size_t)blockIdx.x * E + e] = cs;
+            }
         }
     }
 
@@ -298,7 +284,8 @@ template <int NCH, int KMAX>
 cudaError_t launch_router_tc_t(const CUtensorMap& mx, const CUtensorMap& mw, const Sizes& s,
                                int norm, float* logits, int32_t* idx, float* w, float* p_partial,
                                int32_t* status, cudaStream_t st) {
-    const int smem = kRStages * (kRM * kRK * 2 + NCH * 32 * kRK * 2) + kRedBytes + 1024;
+    const int ring = kRStages * (kRM * kRK * 2 + NCH * 32 * kRK * 2);
+    const int smem = (ring > kRM * kRowPitch * 4 ? ring : kRM * kRowPitch * 4) + 1024;
     cudaError_t err = ensure_smem((const void*)router_tc_kernel<NCH, KMAX>, smem);
     if (err != cudaSuccess) return err;
     const int grid = (s.T + kRM - 1) / kRM;
