@@ -5,9 +5,12 @@
 
 A step is one whole forward (router, dispatch, expert MLPs, combine, aux) of
 one synthetic batch of the named layer configuration (default: the Qwen3-style
-prefill layer T=4096 H=2048 E=128 K=8 I=768), inputs resident in HBM.  Each
-step is timed on the device with CUDA events on the launch stream; L2 is
-flushed (256 MB write) between steps, outside the events.  With N > 1 (torchrun)
+prefill layer T=4096 H=2048 E=128 K=8 I=768), inputs resident in HBM.  The K
+timed steps are enqueued back to back (no host wait inside the timed region);
+each is timed on the device with CUDA events on the launch stream, and the
+library records per-step stage-boundary events on the same stream (the live
+per-kernel times of the roofline).  L2 is flushed (256 MB write) between
+steps, outside the events.  With N > 1 (torchrun)
 every rank runs an independent replica on its own batch (weak scaling, no
 collective on the data path); value = all ranks' tokens / max-over-ranks time.
 
@@ -321,13 +324,18 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     counts = moe.moe_last_expert_counts(E).numpy()
 
-    moe.moe_set_stage_timing(True)
+    # Per-step event sets: the library records the next forward's stage
+    # boundaries on the launch stream, so the K steps run back to back with no
+    # host wait inside the timed region (the host stays ahead of the GPU).
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(moe.STAGE_NAMES) + 1)]
+           for _ in range(args.steps)]
+    for e in ev0 + ev1 + [e for row in evs for e in row]:
+        e.record(stream)  # creates the CUDA events
     sampler = ClockSampler(local)
     if not args.quiet_clocks:
         sampler.start()
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = {k: [] for k in moe.STAGE_NAMES}
     barrier(world)
     torch.cuda.synchronize()
     launches0 = moe.moe_kernel_launch_count()
@@ -335,18 +343,17 @@ def run_ours(args, world, rank, local):
     for k in range(args.steps):
         flush.zero_()
         ev0[k].record(stream)
+        moe.moe_set_next_stage_events(evs[k])
         step()
         ev1[k].record(stream)
-        st = moe.moe_stage_times()  # waits for this step
-        for name, v in st.items():
-            stage_ms[name].append(v)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
     launches = moe.moe_kernel_launch_count() - launches0
-    moe.moe_set_stage_timing(False)
     rows = sampler.stop() if not args.quiet_clocks else None
     clocks = ClockSampler.summarize(rows, t0, t1) if rows is not None else {"reasons": ["unsampled"]}
+    stage_ms = {name: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
+                for i, name in enumerate(moe.STAGE_NAMES)}
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     mean_ms = sum(step_ms) / len(step_ms)
     mean_ms_all = max_over_ranks(mean_ms, world, dev)

@@ -186,6 +186,13 @@ enum moe_stage {
  * be created. */
 int moe_set_stage_timing(int enable);
 
+/* Benchmark variant of stage timing without host waits: `events` points to
+ * MOE_NUM_STAGES + 1 cudaEvent_t created by the caller; the next forward (and
+ * only that one) records them at its stage boundaries on its stream.  Pass a
+ * fresh set before each forward and read them with cudaEventElapsedTime
+ * after synchronising.  NULL cancels a pending set. */
+int moe_set_next_stage_events(void* const* events);
+
 /* Waits for the events of the last forward recorded with stage timing and
  * writes the device time of each stage in milliseconds to ms[0..n) (n <=
  * MOE_NUM_STAGES).  MOE_ERR_INVALID_ARG if no forward was timed. */

@@ -8,7 +8,8 @@ from .binding import (EXPORTS, LIB_PATH, MOE_PATH_AUTO, MOE_PATH_STREAMING,  # n
                       MOE_PATH_TCGEN05, MoEError, lib, moe_dbg_combine, moe_dbg_permute,
                       moe_dbg_route_from_logits, moe_device_status, moe_forward,
                       moe_forward_host, moe_kernel_launch_count, moe_last_expert_counts,
-                      moe_set_expert_path, moe_set_stage_timing, moe_stage_times,
+                      moe_set_expert_path, moe_set_next_stage_events, moe_set_stage_timing,
+                      moe_stage_times,
                       moe_workspace_bytes, STAGE_NAMES)
 
 forward = moe_forward

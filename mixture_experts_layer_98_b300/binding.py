@@ -24,7 +24,8 @@ MOE_PATH_TCGEN05 = 2
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
-           "moe_set_expert_path", "moe_set_stage_timing", "moe_stage_times",
+           "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
+           "moe_stage_times",
            "moe_kernel_launch_count", "moe_dbg_route_from_logits", "moe_dbg_permute",
            "moe_dbg_combine"]
 MOE_NUM_STAGES = 5
@@ -67,6 +68,7 @@ def lib():
         L.moe_set_expert_path.argtypes = [i]
         L.moe_set_stage_timing.argtypes = [i]
         L.moe_stage_times.argtypes = [P, i]
+        L.moe_set_next_stage_events.argtypes = [P]
         L.moe_kernel_launch_count.argtypes = []
         L.moe_kernel_launch_count.restype = ctypes.c_longlong
         L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P]
@@ -199,6 +201,13 @@ def moe_set_expert_path(path):
 
 def moe_set_stage_timing(enable):
     _call(lib().moe_set_stage_timing(int(bool(enable))), "moe_set_stage_timing")
+
+
+def moe_set_next_stage_events(events):
+    """events: MOE_NUM_STAGES + 1 torch.cuda.Event objects (already recorded once,
+    so their CUDA events exist) for the next forward's stage boundaries."""
+    arr = (ctypes.c_void_p * (MOE_NUM_STAGES + 1))(*[e.cuda_event for e in events])
+    _call(lib().moe_set_next_stage_events(arr), "moe_set_next_stage_events")
 
 
 def moe_stage_times():

@@ -12,9 +12,11 @@ namespace moe {
 
 namespace {
 
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ Y,
-                                                      const int32_t* __restrict__ inv, int T,
-                                                      int K, int vpr, uint4* __restrict__ out) {
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* Y,
+                                                      const int32_t* inv, int T,
+                                                      int K, int vpr, uint4* out) {
+    pdl_trigger();
+    pdl_wait();
     const long long total = (long long)T * vpr;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -23,8 +25,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = 0.f;
         for (int k = 0; k < K; ++k) {
-            const int row = __ldg(inv + (size_t)t * K + k);
-            const uint4 v = __ldg(Y + (size_t)row * vpr + c);
+            // plain (coherent) loads: inv and Y are written by earlier kernels of the
+            // forward, which may still have been running when this grid launched
+            const int row = inv[(size_t)t * K + k];
+            const uint4 v = Y[(size_t)row * vpr + c];
             a[0] += bf16_lo(v.x);
             a[1] += bf16_hi(v.x);
             a[2] += bf16_lo(v.y);
@@ -53,10 +57,11 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, in
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    combine_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(Y), inv, T, K, vpr,
-                                                reinterpret_cast<uint4*>(out));
+    cudaError_t e = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                               reinterpret_cast<const uint4*>(Y), inv, T, K, vpr,
+                               reinterpret_cast<uint4*>(out));
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

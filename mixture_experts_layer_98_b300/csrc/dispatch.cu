@@ -30,9 +30,11 @@ namespace {
 constexpr int kWords = kChunkTokens / 32;
 
 __global__ void __launch_bounds__(kChunkTokens) dispatch_count_kernel(
-    const int32_t* __restrict__ idx, int T, int E, int K, int32_t* __restrict__ chunk_counts) {
+    const int32_t* idx, int T, int E, int K, int32_t* chunk_counts) {
+    pdl_trigger();
     __shared__ int cnt[kMaxExperts];
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    pdl_wait();
     __syncthreads();
     const int t = blockIdx.x * kChunkTokens + threadIdx.x;
     if (t < T)
@@ -42,7 +44,8 @@ __global__ void __launch_bounds__(kChunkTokens) dispatch_count_kernel(
         chunk_counts[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// Inclusive prefix sum of v over the CTA's kMaxExperts threads (8 warps).
+// Inclusive prefix sum of v over all threads of the CTA, in thread order
+// (warp_tot holds one int per warp).  Every thread must call it.
 __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -58,16 +61,38 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tot) {
     return v + add;
 }
 
-// One CTA of kMaxExperts threads; thread e owns expert e.
+constexpr int kScanThreads = 4 * kMaxExperts;
+
+// One CTA of 4 * kMaxExperts threads.  First, four threads per expert add up
+// the routing CTAs' probability sums (rows j, j+4, ... each); then thread e
+// (e < E) owns expert e and computes
 //   chunk_base[c,e] = pairs of expert e in chunks before c (within-expert prefix)
 //   counts[e], offsets[0..E], the row-tile table and n_tiles, and aux.
-__global__ void __launch_bounds__(kMaxExperts) dispatch_scan_kernel(
-    const int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_base, int nchunks, int T,
-    int E, int K, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    RowTile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int rows_per_tile,
-    const float* __restrict__ p_partial, int nrouter, float* __restrict__ aux) {
-    __shared__ int warp_tot[kMaxExperts / 32];
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
+    const int32_t* chunk_counts, int32_t* chunk_base, int nchunks, int T,
+    int E, int K, int32_t* counts, int32_t* offsets,
+    RowTile* tiles, int32_t* n_tiles, int rows_per_tile,
+    const float* p_partial, int nrouter, float* aux) {
+    __shared__ int warp_tot[kScanThreads / 32];
     __shared__ float term_s[kMaxExperts];
+    __shared__ float psum_s[4][kMaxExperts];
+    pdl_trigger();
+    pdl_wait();
+    if (aux) {
+        const int pe = threadIdx.x % kMaxExperts, pj = threadIdx.x / kMaxExperts;
+        if (pe < E) {
+            float a0 = 0.f, a1 = 0.f;
+            int b = pj;
+            for (; b + 4 < nrouter; b += 8) {
+                a0 += p_partial[(size_t)b * E + pe];
+                a1 += p_partial[(size_t)(b + 4) * E + pe];
+            }
+            if (b < nrouter) a0 += p_partial[(size_t)b * E + pe];
+            psum_s[pj][pe] = a0 + a1;
+        }
+        __syncthreads();
+    }
+    // threads past kMaxExperts own no expert but still take part in the barriers
     const int e = threadIdx.x;
     const bool own = e < E;
     int run = 0;
@@ -111,16 +136,7 @@ __global__ void __launch_bounds__(kMaxExperts) dispatch_scan_kernel(
             tiles[tbase + j] = tl;
         }
         if (aux) {
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-            int b = 0;
-            for (; b + 4 <= nrouter; b += 4) {  // four interleaved partial sums, combined in order
-                p0 += p_partial[(size_t)(b + 0) * E + e];
-                p1 += p_partial[(size_t)(b + 1) * E + e];
-                p2 += p_partial[(size_t)(b + 2) * E + e];
-                p3 += p_partial[(size_t)(b + 3) * E + e];
-            }
-            for (; b < nrouter; ++b) p0 += p_partial[(size_t)b * E + e];
-            const float psum = (p0 + p1) + (p2 + p3);
+            const float psum = ((psum_s[0][e] + psum_s[1][e]) + psum_s[2][e]) + psum_s[3][e];
             const float f = (float)run / ((float)T * (float)K);
             term_s[e] = f * (psum / (float)T);
         }
@@ -137,40 +153,41 @@ __global__ void __launch_bounds__(kMaxExperts) dispatch_scan_kernel(
     }
 }
 
+constexpr int kScatterThreads = 1024;
+
 // Row of each pair: offsets[e] + chunk_base[c,e] + (tokens of this chunk
-// before t that chose e), the last from per-expert token bitmaps.
-__global__ void __launch_bounds__(kChunkTokens) dispatch_scatter_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int E, int K,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ chunk_base,
-    int32_t* __restrict__ perm_tok, int32_t* __restrict__ perm_slot, int32_t* __restrict__ inv,
-    float* __restrict__ w_perm) {
+// before t that chose e), the last from per-expert token bitmaps.  One CTA per
+// chunk; its threads walk the chunk's pairs (token-major), so each thread
+// handles about K / 4 pairs.
+__global__ void __launch_bounds__(kScatterThreads) dispatch_scatter_kernel(
+    const int32_t* idx, const float* w, int T, int E, int K,
+    const int32_t* offsets, const int32_t* chunk_base,
+    int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
+    float* w_perm) {
     __shared__ uint32_t sel[kMaxExperts * kWords];
     __shared__ int base_s[kMaxExperts];
+    pdl_trigger();
     for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) sel[i] = 0u;
+    pdl_wait();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         base_s[e] = offsets[e] + chunk_base[(size_t)blockIdx.x * E + e];
     __syncthreads();
-    const int tl = threadIdx.x, word = tl >> 5, bit = tl & 31;
-    const int t = blockIdx.x * kChunkTokens + tl;
-    int ev[kMaxTopK];
-    if (t < T) {
-#pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k)
-            if (k < K) ev[k] = idx[(size_t)t * K + k];
-#pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k)
-            if (k < K) atomicOr(&sel[ev[k] * kWords + word], 1u << bit);
+    const int t0 = blockIdx.x * kChunkTokens;
+    const int npairs = min(kChunkTokens, T - t0) * K;
+    const int32_t* cidx = idx + (size_t)t0 * K;
+    for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+        const int tl = i / K;
+        atomicOr(&sel[cidx[i] * kWords + (tl >> 5)], 1u << (tl & 31));
     }
     __syncthreads();
-    if (t >= T) return;
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-        if (k >= K) break;
-        const int e = ev[k];
+    for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+        const int tl = i / K, k = i - tl * K, word = tl >> 5, bit = tl & 31;
+        const int e = cidx[i];
         const uint32_t* sb = sel + e * kWords;
         int rank = __popc(sb[word] & ((1u << bit) - 1u));
         for (int j = 0; j < word; ++j) rank += __popc(sb[j]);
         const int row = base_s[e] + rank;
+        const int t = t0 + tl;
         perm_tok[row] = t;
         if (perm_slot) perm_slot[row] = k;
         inv[(size_t)t * K + k] = row;
@@ -179,16 +196,22 @@ __global__ void __launch_bounds__(kChunkTokens) dispatch_scatter_kernel(
 }
 
 // x_perm[row, :] = x[perm_tok[row], :]; one warp per row, 16-byte vectors.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
-                                                          const int32_t* __restrict__ perm_tok,
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
+                                                          const int32_t* perm_tok,
                                                           long long P, int vec_per_row,
-                                                          uint4* __restrict__ x_perm) {
+                                                          uint4* x_perm) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     for (long long r = warp; r < P; r += nwarps) {
         const uint4* src = x + (size_t)perm_tok[r] * vec_per_row;
         uint4* dst = x_perm + (size_t)r * vec_per_row;
+        // x is the caller's input: whatever wrote it finished before the router
+        // (the forward's first kernel) passed its dependency wait, long before
+        // this grid launched, so it is constant for this grid's whole lifetime
+        // and the read-only path is allowed here.
         for (int c = lane; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
     }
 }
@@ -199,26 +222,30 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
                             const float* p_partial, int n_partials, float* aux, cudaStream_t st) {
     const int nch = s.nchunks();
-    dispatch_count_kernel<<<nch, kChunkTokens, 0, st>>>(idx, s.T, s.E, s.K, ws.chunk_counts);
-    dispatch_scan_kernel<<<1, kMaxExperts, 0, st>>>(
+    cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kChunkTokens), 0, st, idx,
+                               s.T, s.E, s.K, ws.chunk_counts);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, st,
         ws.chunk_counts, ws.chunk_base, nch, s.T, s.E, s.K, ws.counts, ws.offsets, ws.tiles,
         ws.n_tiles, rows_per_tile, p_partial, n_partials, aux);
-    dispatch_scatter_kernel<<<nch, kChunkTokens, 0, st>>>(idx, w, s.T, s.E, s.K, ws.offsets,
-                                                          ws.chunk_base, ws.perm_tok, ws.perm_slot,
-                                                          ws.inv, ws.w_perm);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scatter_kernel, dim3(nch), dim3(kScatterThreads), 0, st, idx, w, s.T,
+                   s.E, s.K, (const int32_t*)ws.offsets, (const int32_t*)ws.chunk_base,
+                   ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm);
     count_launches(3);
+    if (e != cudaSuccess) return e;
     if (x) {
         const long long P = s.P();
         long long blocks = (P + 7) / 8;
         const long long cap = (long long)num_sms() * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x),
-                                                        ws.perm_tok, P, s.H / 8,
-                                                        reinterpret_cast<uint4*>(ws.x_perm));
+        e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                       reinterpret_cast<const uint4*>(x), (const int32_t*)ws.perm_tok, P, s.H / 8,
+                       reinterpret_cast<uint4*>(ws.x_perm));
         count_launches(1);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

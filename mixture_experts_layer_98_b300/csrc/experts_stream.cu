@@ -25,9 +25,10 @@ constexpr int kRowsPerWarp = 2;                     // weight rows per warp per 
 constexpr int kWarps = 8;
 constexpr int kRowsPerItem = kRowsPerWarp * kWarps;  // 16 weight rows per item
 
+// Streaming 16-byte load of weights: coherent, not kept in L1.
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -47,8 +48,8 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
 
 // Stages rows [row0, row0+nrows) of a [P, D] bf16 matrix into shared memory;
 // with perm != null, dispatch row r is row perm[r] of src (a gather from x).
-__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ src,
-                                           const int32_t* __restrict__ perm, int row0, int nrows,
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16* src,
+                                           const int32_t* perm, int row0, int nrows,
                                            int D, uint4* dst) {
     const int vpr = D / 8;
     const uint4* s = reinterpret_cast<const uint4*>(src);
@@ -60,11 +61,13 @@ __device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ src
 }
 
 __global__ void __launch_bounds__(256) gateup_stream_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm_tok,
-    const RowTile* __restrict__ tiles,
-    const int32_t* __restrict__ n_tiles_p, const __nv_bfloat16* __restrict__ Wg,
-    const __nv_bfloat16* __restrict__ Wu, __nv_bfloat16* __restrict__ h, int H, int I) {
+    const __nv_bfloat16* x, const int32_t* perm_tok,
+    const RowTile* tiles,
+    const int32_t* n_tiles_p, const __nv_bfloat16* Wg,
+    const __nv_bfloat16* Wu, __nv_bfloat16* h, int H, int I) {
     extern __shared__ uint4 xs[];  // [kStreamRows][H/8]
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int vpr = H / 8;
     const int nblk = I / kRowsPerItem;
@@ -122,10 +125,12 @@ __global__ void __launch_bounds__(256) gateup_stream_kernel(
 }
 
 __global__ void __launch_bounds__(256) down_stream_kernel(
-    const __nv_bfloat16* __restrict__ hbuf, const RowTile* __restrict__ tiles,
-    const int32_t* __restrict__ n_tiles_p, const __nv_bfloat16* __restrict__ Wd,
-    const float* __restrict__ w_perm, __nv_bfloat16* __restrict__ Y, int H, int I) {
+    const __nv_bfloat16* hbuf, const RowTile* tiles,
+    const int32_t* n_tiles_p, const __nv_bfloat16* Wd,
+    const float* w_perm, __nv_bfloat16* Y, int H, int I) {
     extern __shared__ uint4 hs[];  // [kStreamRows][I/8]
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int vpr = I / 8;
     const int nblk = H / kRowsPerItem;
@@ -193,15 +198,17 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16
     const long long cap = (long long)sms * 4;
     const int g_gu = (int)(items_gu < cap ? items_gu : cap);
     const int g_dn = (int)(items_dn < cap ? items_dn : cap);
-    gateup_stream_kernel<<<g_gu, 256, smem_gu, st>>>(x, ws.perm_tok, ws.tiles, ws.n_tiles, Wg,
-                                                      Wu, ws.hbuf, s.H, s.I);
-    err = cudaGetLastError();
+    err = launch_pdl(gateup_stream_kernel, dim3(g_gu), dim3(256), smem_gu, st, x,
+                     (const int32_t*)ws.perm_tok, (const RowTile*)ws.tiles,
+                     (const int32_t*)ws.n_tiles, Wg, Wu, ws.hbuf, s.H, s.I);
+    count_launches(1);
     if (err != cudaSuccess) return err;
     if (ev_mid) cudaEventRecord(ev_mid, st);
-    down_stream_kernel<<<g_dn, 256, smem_dn, st>>>(ws.hbuf, ws.tiles, ws.n_tiles, Wd, ws.w_perm,
-                                                    ws.ybuf, s.H, s.I);
-    count_launches(2);
-    return cudaGetLastError();
+    err = launch_pdl(down_stream_kernel, dim3(g_dn), dim3(256), smem_dn, st,
+                     (const __nv_bfloat16*)ws.hbuf, (const RowTile*)ws.tiles,
+                     (const int32_t*)ws.n_tiles, Wd, (const float*)ws.w_perm, ws.ybuf, s.H, s.I);
+    count_launches(1);
+    return err;
 }
 
 }  // namespace moe

@@ -102,10 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(&tmem_base_s, C::kTmemCols);
         ptx::tmem_relinquish();
     }
+    pdl_trigger();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
+    pdl_wait();  // the prologue above overlaps the previous kernel's tail
     const int total = (*p.n_tiles) * p.n_nt;
 
     if (warp == 0) {
@@ -309,9 +311,10 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
     long long grid = num_sms();
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
-    grouped_gemm_tc_kernel<MODE, BN><<<(int)grid, kThreads, C::kSmemBytes, st>>>(ma, mb0, mb1, p);
+    err = launch_pdl(grouped_gemm_tc_kernel<MODE, BN>, dim3((unsigned)grid), dim3(kThreads),
+                     C::kSmemBytes, st, ma, mb0, mb1, p);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace

@@ -26,8 +26,24 @@ static bool g_timing = false;
 static bool g_timed_once = false;
 static cudaEvent_t g_ev[MOE_NUM_STAGES + 1] = {};
 
+static cudaEvent_t g_next_ev[MOE_NUM_STAGES + 1] = {};
+static bool g_next_set = false;
+static thread_local cudaEvent_t t_cur_ev[MOE_NUM_STAGES + 1] = {};  // events of this forward
+
+// Records the stage-boundary event `boundary` of the current forward, if any.
 static void mark(int boundary, cudaStream_t st) {
-    if (g_timing) cudaEventRecord(g_ev[boundary], st);
+    if (t_cur_ev[boundary]) cudaEventRecord(t_cur_ev[boundary], st);
+}
+
+// Picks the events this forward records: a one-shot caller set, else the
+// library's own set when stage timing is on, else none.
+static void begin_marks() {
+    if (g_next_set) {
+        for (int i = 0; i <= MOE_NUM_STAGES; ++i) t_cur_ev[i] = g_next_ev[i];
+        g_next_set = false;
+    } else {
+        for (int i = 0; i <= MOE_NUM_STAGES; ++i) t_cur_ev[i] = g_timing ? g_ev[i] : nullptr;
+    }
 }
 
 static std::mutex g_attr_mu;
@@ -81,7 +97,7 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
     w.perm_slot = (int32_t*)take(P * 4);
     w.inv = (int32_t*)take(P * 4);
     w.w_perm = (float*)take(P * 4);
-    w.logits = (float*)take((size_t)s.T * s.E * 4);
+    w.logit_parts = (float*)take((size_t)kRouterMaxSplits * s.T * s.E * 4);
     w.topk_idx = (int32_t*)take(P * 4);
     w.topk_w = (float*)take(P * 4);
     w.x_perm = (__nv_bfloat16*)take(P * s.H * 2);
@@ -196,23 +212,31 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
                        const Workspace& ws, cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
+    begin_marks();
     mark(0, st);
-    // Tensor-core router from one full 128-token tile up (E <= 128); else the CUDA-core
-    // router, whose logits kernel spreads the experts over many CTAs.
+    // Tensor-core router logits from one full 128-token tile up (E <= 128), else the
+    // CUDA-core logits kernel; then the per-token routing kernel either way.
     const bool router_tc = s.T >= 128 && router_tc_supported(s);
-    cudaError_t e = router_tc
-                        ? launch_router_tc(x, Wr, s, norm, logits, idx, w, ws.p_partial, ws.status, st)
-                        : launch_router(x, Wr, s, norm, logits, ws.logits, idx, w, ws.p_partial,
-                                        ws.status, st);
+    cudaError_t e;
+    if (router_tc) {
+        const int nsplit = router_tc_splits(s);
+        e = launch_router_tc(x, Wr, s, nsplit, ws.logit_parts, ws.status, st);
+        if (e == cudaSuccess)
+            e = launch_route_from_logits(ws.logit_parts, nsplit, logits, s, norm, idx, w,
+                                         ws.p_partial, st);
+    } else {
+        e = launch_router(x, Wr, s, norm, logits, ws.logit_parts, idx, w, ws.p_partial, ws.status,
+                          st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
-    const int n_partials = router_tc ? router_tc_partials(s.T) : s.nrouter();
+    const int n_partials = s.nrouter();
     mark(1, st);
     const bool tc = use_tcgen05(s);
     e = launch_dispatch(idx, w, tc ? x : nullptr, s, ws, tc ? kTcRows : kStreamRows, ws.p_partial,
                         n_partials, aux, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
-    cudaEvent_t mid = g_timing ? g_ev[3] : nullptr;
+    cudaEvent_t mid = t_cur_ev[3];
     e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid)
            : launch_experts_streaming(x, Wg, Wu, Wd, s, ws, st, mid);
     if (e != cudaSuccess) return cuda_status(e);
@@ -270,6 +294,19 @@ int moe_set_stage_timing(int enable) {
         }
     }
     g_timing = enable != 0;
+    return MOE_OK;
+}
+
+int moe_set_next_stage_events(void* const* events) {
+    if (!events) {
+        g_next_set = false;
+        return MOE_OK;
+    }
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i) {
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+        g_next_ev[i] = (cudaEvent_t)events[i];
+    }
+    g_next_set = true;
     return MOE_OK;
 }
 
@@ -458,8 +495,8 @@ int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm
     if (rc) return rc;
     if (T == 0) return MOE_OK;
     Sizes s{T, 64, E, K, 64};
-    return cuda_status(launch_route_from_logits(logits, s, norm_topk_prob, topk_idx, topk_w,
-                                                nullptr, (cudaStream_t)stream));
+    return cuda_status(launch_route_from_logits(logits, 1, nullptr, s, norm_topk_prob, topk_idx,
+                                                topk_w, nullptr, (cudaStream_t)stream));
 }
 
 int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,

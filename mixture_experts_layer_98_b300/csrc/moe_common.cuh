@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe_b300.h"
 
 namespace moe {
@@ -17,6 +19,7 @@ constexpr int kChunkTokens = 256;    // tokens per dispatch chunk (one CTA)
 constexpr int kRouterTokens = 32;    // tokens per router CTA (SIMT router)
 constexpr int kStreamRows = 8;       // rows per tile of the weight-streaming kernels
 constexpr int kTcRows = 128;         // rows per tile of the tcgen05 grouped GEMMs
+constexpr int kRouterMaxSplits = 4;  // slices of H the tensor-core router may split into
 
 // One tile of token-expert rows, all routed to one expert: rows
 // [row0, row0 + nrows) of the dispatch order.
@@ -41,7 +44,7 @@ struct Workspace {
     int32_t* perm_slot;     // [P]
     int32_t* inv;           // [P]
     float* w_perm;          // [P]
-    float* logits;          // [T, E] when the caller passes NULL
+    float* logit_parts;     // [kRouterMaxSplits, T, E] partial logits
     int32_t* topk_idx;      // [T, K] when the caller passes NULL
     float* topk_w;          // [T, K] when the caller passes NULL
     __nv_bfloat16* x_perm;  // [P, H] (tcgen05 path)
@@ -70,15 +73,17 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
                           int norm, float* logits, float* logits_scratch, int32_t* idx, float* w,
                           float* p_partial, int32_t* status, cudaStream_t st);
-// tcgen05 router (128-token tiles); writes router_tc_partials(T) rows of
-// probability sums.
+// tcgen05 router logits: nsplit slices of H, partial logits [nsplit][T][E]
+// into parts (then launch_route_from_logits with those parts).
 cudaError_t launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                             int norm, float* logits, int32_t* idx, float* w, float* p_partial,
-                             int32_t* status, cudaStream_t st);
-int router_tc_partials(int T);
+                             int nsplit, float* parts, int32_t* status, cudaStream_t st);
+int router_tc_splits(const Sizes& s);
 bool router_tc_supported(const Sizes& s);  // E <= 128
-cudaError_t launch_route_from_logits(const float* logits, const Sizes& s, int norm,
-                                     int32_t* idx, float* w, float* p_partial, cudaStream_t st);
+// Softmax, top-k, renorm and per-32-token probability sums (s.nrouter() rows)
+// from the sum of nparts partial-logit arrays; logits_out (may be null) gets the sum.
+cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,
+                                     const Sizes& s, int norm, int32_t* idx, float* w,
+                                     float* p_partial, cudaStream_t st);
 // p_partial holds n_partials rows of per-expert probability sums (for aux).
 // x != null: also gather x_perm[row] = x[perm_tok[row]].
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
@@ -124,6 +129,39 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
 
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);
+
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel of a forward is launched with programmatic stream serialization:
+// it may start while the previous kernel on the stream is still finishing, so
+// it must call pdl_wait() before it reads anything an earlier kernel (or the
+// caller's earlier work) wrote, and it calls pdl_trigger() early so that the
+// next kernel's launch overlaps its own tail.  Dependent CTAs are launched only
+// after every CTA of the running grid has triggered or exited.  Because a
+// grid's lifetime now overlaps its predecessors', no kernel may use
+// non-coherent (ld.global.nc / __ldg) loads: their contract is that the data
+// stays unchanged for the whole lifetime of the reading grid.  That is also why
+// no kernel pointer is declared __restrict__: with `const T* __restrict__` the
+// compiler is free to turn ordinary loads into non-coherent ones.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- small device helpers --------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

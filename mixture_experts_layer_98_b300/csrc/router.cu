@@ -17,28 +17,15 @@ namespace moe {
 
 namespace {
 
-// (value, expert, prob) of the best candidate: larger value first, then the
-// lower expert index.
-struct Cand {
-    float v;
-    int e;
-    float p;
-};
-
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-    return a.v > b.v || (a.v == b.v && a.e < b.e);
+// Order-preserving map of a float to uint32 (larger float -> larger key);
+// -0 is folded to +0 first, so equal floats give equal keys.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ Cand warp_best(Cand c) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        Cand o;
-        o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
-        o.e = __shfl_xor_sync(0xffffffffu, c.e, off);
-        o.p = __shfl_xor_sync(0xffffffffu, c.p, off);
-        if (better(o, c)) c = o;
-    }
-    return c;
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -80,26 +67,34 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
         p[q] = ex[q] * inv_s;
         if (probs && lane + 32 * q < E) probs[lane + 32 * q] = p[q];
     }
-    uint32_t taken = 0;
+    // K rounds of a warp-wide arg-max: the largest key, then the lowest expert
+    // index among the lanes holding it (two redux.sync per round).  The
+    // winner's probability is recomputed from its value in every lane.
+    uint32_t key[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) key[q] = (lane + 32 * q < E) ? order_key(l[q]) : 0u;
     float wsum = 0.f;
     int my_e = -1;
     float my_p = 0.f;
     for (int k = 0; k < K; ++k) {
-        Cand c{-INFINITY, 0x7fffffff, 0.f};
+        uint32_t bk = 0u;
+        int be = 0x7fffffff;
 #pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-            const int e = lane + 32 * q;
-            if (e < E && !(taken & (1u << q))) {
-                Cand o{l[q], e, p[q]};
-                if (c.e == 0x7fffffff || better(o, c)) c = o;
+        for (int q = 0; q < EPL; ++q)  // experts of a lane come in increasing index
+            if (key[q] > bk) {
+                bk = key[q];
+                be = lane + 32 * q;
             }
-        }
-        c = warp_best(c);
-        if ((c.e & 31) == lane) taken |= 1u << (c.e >> 5);
-        wsum += c.p;  // same value and order in every lane
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int we = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)be : 0x7fffffffu);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q)  // taken
+            if (we == lane + 32 * q) key[q] = 0u;
+        const float pk = expf(key_value(mk) - m) * inv_s;
+        wsum += pk;  // same value and order in every lane
         if (lane == k) {
-            my_e = c.e;
-            my_p = c.p;
+            my_e = we;
+            my_p = pk;
         }
     }
     if (lane < K) {
@@ -128,15 +123,17 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b, float
 // router row with 16-byte loads, so even a single token spreads the router
 // weights over E/8 SMs.  The first CTA also clears the forward's status word.
 __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wr, int T, int H,
-    int E, float* __restrict__ logits, int32_t* __restrict__ status) {
+    const __nv_bfloat16* x, const __nv_bfloat16* Wr, int T, int H,
+    int E, float* logits, int32_t* status) {
     extern __shared__ uint4 xs[];  // [kSplitTokens][H/8]
+    pdl_trigger();
+    pdl_wait();
     if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
     const int vpr = H / 8;
     const int t0 = blockIdx.x * kSplitTokens;
     const int nt = min(kSplitTokens, T - t0);
     const uint4* xg = reinterpret_cast<const uint4*>(x) + (size_t)t0 * vpr;
-    for (int i = threadIdx.x; i < nt * vpr; i += blockDim.x) xs[i] = __ldg(xg + i);
+    for (int i = threadIdx.x; i < nt * vpr; i += blockDim.x) xs[i] = xg[i];
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = blockIdx.y * kSplitWarps + warp;
@@ -147,7 +144,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
     for (int m = 0; m < kSplitTokens; ++m) acc[m] = 0.f;
 #pragma unroll 4
     for (int c = lane; c < vpr; c += 32) {
-        const uint4 wv = __ldg(wr + c);
+        const uint4 wv = wr[c];
 #pragma unroll
         for (int m = 0; m < kSplitTokens; ++m)
             if (m < nt) acc[m] = dot8_bf16(wv, xs[m * vpr + c], acc[m]);
@@ -161,30 +158,42 @@ __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
     }
 }
 
-// Routing from logits: one warp per token, kRouterTokens tokens per CTA.
-// CTA = 256 threads, one warp per token, kRouterTokens tokens per CTA.
+// Routing from logits: one warp per token, kRouterTokens tokens (warps) per
+// CTA, so a 4096-token batch keeps 4096 warps in flight.  The
+// logits are the sum, in slice order, of nparts partial-logit arrays
+// (parts + s * part_stride, [T, E] each); logits_out (may be null) receives
+// that sum.
 template <int EPL>
-__global__ void __launch_bounds__(256) route_from_logits_kernel(
-    const float* __restrict__ logits, int T, int E, int K, int norm, int32_t* __restrict__ idx,
-    float* __restrict__ w, float* __restrict__ p_partial) {
+__global__ void __launch_bounds__(kRouterTokens * 32) route_from_logits_kernel(
+    const float* parts, int nparts, size_t part_stride, float* logits_out, int T, int E, int K,
+    int norm, int32_t* idx, float* w, float* p_partial) {
     __shared__ float ls[kRouterTokens * kMaxExperts];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int t0 = blockIdx.x * kRouterTokens;
-    for (int j = wid; j < kRouterTokens; j += 8) {
-        const int t = t0 + j;
-        if (t >= T) break;
+    const int j = wid;  // one warp per token
+    const int t = t0 + j;
+    if (t < T) {  // warp-uniform
         float l[EPL];
 #pragma unroll
         for (int q = 0; q < EPL; ++q) {
             const int e = lane + 32 * q;
-            l[q] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+            if (e < E) {
+                float v = parts[(size_t)t * E + e];
+                for (int sidx = 1; sidx < nparts; ++sidx) v += parts[sidx * part_stride + (size_t)t * E + e];
+                l[q] = v;
+                if (logits_out) logits_out[(size_t)t * E + e] = v;
+            } else {
+                l[q] = -INFINITY;
+            }
         }
         route_token<EPL>(l, E, K, norm, idx + (size_t)t * K, w + (size_t)t * K, ls + j * E);
     }
     __syncthreads();
     if (p_partial) {
         const int nt = min(kRouterTokens, T - t0);
-        for (int e = tid; e < E; e += 256) {
+        for (int e = tid; e < E; e += blockDim.x) {
             float s = 0.f;
             for (int t = 0; t < nt; ++t) s += ls[t * E + e];
             p_partial[(size_t)blockIdx.x * E + e] = s;
@@ -193,12 +202,13 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(
 }
 
 template <int EPL>
-cudaError_t launch_route_t(const float* logits, const Sizes& s, int norm, int32_t* idx, float* w,
-                           float* p_partial, cudaStream_t st) {
-    route_from_logits_kernel<EPL><<<s.nrouter(), 256, 0, st>>>(logits, s.T, s.E, s.K, norm, idx,
-                                                               w, p_partial);
+cudaError_t launch_route_t(const float* parts, int nparts, float* logits_out, const Sizes& s,
+                           int norm, int32_t* idx, float* w, float* p_partial, cudaStream_t st) {
+    cudaError_t e = launch_pdl(route_from_logits_kernel<EPL>, dim3(s.nrouter()),
+                               dim3(kRouterTokens * 32), 0, st, parts, nparts, (size_t)s.T * s.E,
+                               logits_out, s.T, s.E, s.K, norm, idx, w, p_partial);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
@@ -211,21 +221,21 @@ cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const
     cudaError_t err = ensure_smem((const void*)router_logits_split_kernel, smem);
     if (err != cudaSuccess) return err;
     dim3 grid((s.T + kSplitTokens - 1) / kSplitTokens, (s.E + kSplitWarps - 1) / kSplitWarps);
-    router_logits_split_kernel<<<grid, kSplitWarps * 32, smem, st>>>(x, Wr, s.T, s.H, s.E, lg,
-                                                                     status);
+    err = launch_pdl(router_logits_split_kernel, grid, dim3(kSplitWarps * 32), smem, st, x, Wr, s.T,
+                     s.H, s.E, lg, status);
     count_launches(1);
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return launch_route_from_logits(lg, s, norm, idx, w, p_partial, st);
+    return launch_route_from_logits(lg, 1, nullptr, s, norm, idx, w, p_partial, st);
 }
 
-cudaError_t launch_route_from_logits(const float* logits, const Sizes& s, int norm, int32_t* idx,
-                                     float* w, float* p_partial, cudaStream_t st) {
+cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,
+                                     const Sizes& s, int norm, int32_t* idx, float* w,
+                                     float* p_partial, cudaStream_t st) {
     const int epl = (s.E + 31) / 32;
-    if (epl <= 1) return launch_route_t<1>(logits, s, norm, idx, w, p_partial, st);
-    if (epl <= 2) return launch_route_t<2>(logits, s, norm, idx, w, p_partial, st);
-    if (epl <= 4) return launch_route_t<4>(logits, s, norm, idx, w, p_partial, st);
-    return launch_route_t<8>(logits, s, norm, idx, w, p_partial, st);
+    if (epl <= 1) return launch_route_t<1>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
+    if (epl <= 2) return launch_route_t<2>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
+    if (epl <= 4) return launch_route_t<4>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
+    return launch_route_t<8>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
 }
 
 }  // namespace moe
