@@ -6,11 +6,13 @@
 A step is one whole forward (router, dispatch, expert MLPs, combine, aux) of
 one synthetic batch of the named layer configuration (default: the Qwen3-style
 prefill layer T=4096 H=2048 E=128 K=8 I=768), inputs resident in HBM.  The K
-timed steps are enqueued back to back (no host wait inside the timed region);
-each is timed on the device with CUDA events on the launch stream, and the
-library records per-step stage-boundary events on the same stream (the live
-per-kernel times of the roofline).  L2 is flushed (256 MB write) between
-steps, outside the events.  With N > 1 (torchrun)
+timed steps are enqueued back to back (no host wait inside the timed region)
+and each is timed on the device with CUDA events on the launch stream; L2 is
+flushed (256 MB write) between steps, outside the events.  A second pass of K
+steps has the library record stage-boundary events on the same stream, giving
+the live per-kernel times of the roofline object and the stage split (those
+events serialise the boundaries they sit on, so they stay out of the first
+pass).  With N > 1 (torchrun)
 every rank runs an independent replica on its own batch (weak scaling, no
 collective on the data path); value = all ranks' tokens / max-over-ranks time.
 
@@ -44,8 +46,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 STAGE_SOURCES = {
     "router": ["router.cu", "moe_common.cuh"],
     "dispatch": ["dispatch.cu", "moe_common.cuh"],
-    "gate_up": ["experts_tc.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
-    "down": ["experts_tc.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
+    "gate_up": ["experts_tc.cu", "experts_wt.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
+    "down": ["experts_tc.cu", "experts_wt.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
     "combine": ["combine.cu", "moe_common.cuh"],
 }
 
@@ -62,6 +64,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--quiet-clocks", action="store_true", help="skip nvidia-smi sampling")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of the forward captured as a CUDA graph (decode serving)")
+    ap.add_argument("--expert-path", default="auto", choices=["auto", "streaming", "tcgen05", "tcgen05_wt"],
+                    help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args()
 
 
@@ -308,10 +314,35 @@ def run_ours(args, world, rank, local):
     aux = torch.empty((1,), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3}[args.expert_path])
 
-    def step():
+    def eager():
         moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], K,
                         cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w, aux=aux)
+
+    eager()
+    torch.cuda.synchronize()
+    counts = moe.moe_last_expert_counts(E).numpy()
+    n0 = moe.moe_kernel_launch_count()
+    eager()
+    launches_per_step = moe.moe_kernel_launch_count() - n0
+    step = eager
+    if args.graph:
+        # A serving loop replays the captured forward: the caller owns the
+        # workspace, and the host enqueues one graph launch per step.
+        ws = torch.empty(moe.moe_workspace_bytes(T, H, E, K, I), dtype=torch.uint8, device=dev)
+
+        def fwd_ws():
+            moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                            K, cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w,
+                            aux=aux, workspace=ws)
+
+        fwd_ws()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fwd_ws()
+        step = graph.replay
 
     # warm-up: at least W steps and at least ~1 s of work so clocks settle
     t_end = time.time() + 1.0
@@ -322,17 +353,13 @@ def run_ours(args, world, rank, local):
         if n % 50 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
-    counts = moe.moe_last_expert_counts(E).numpy()
 
-    # Per-step event sets: the library records the next forward's stage
-    # boundaries on the launch stream, so the K steps run back to back with no
-    # host wait inside the timed region (the host stays ahead of the GPU).
+    # Timed region: K steps enqueued back to back (no host wait inside), each
+    # bracketed by CUDA events on the launch stream, L2 flushed between steps
+    # outside the events.  No stage events here: an event recorded between two
+    # kernels serialises that boundary and would hide the programmatic overlap.
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(moe.STAGE_NAMES) + 1)]
-           for _ in range(args.steps)]
-    for e in ev0 + ev1 + [e for row in evs for e in row]:
-        e.record(stream)  # creates the CUDA events
     sampler = ClockSampler(local)
     if not args.quiet_clocks:
         sampler.start()
@@ -343,15 +370,31 @@ def run_ours(args, world, rank, local):
     for k in range(args.steps):
         flush.zero_()
         ev0[k].record(stream)
-        moe.moe_set_next_stage_events(evs[k])
         step()
         ev1[k].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
     launches = moe.moe_kernel_launch_count() - launches0
+    if args.graph:  # graph replays bypass the library's launch counter
+        launches = launches_per_step * args.steps
     rows = sampler.stop() if not args.quiet_clocks else None
     clocks = ClockSampler.summarize(rows, t0, t1) if rows is not None else {"reasons": ["unsampled"]}
+
+    # Second timed pass, same workload: per-step stage-boundary events recorded
+    # by the library on the launch stream give each kernel's live duration (the
+    # roofline's kernel time and the stage split).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(moe.STAGE_NAMES) + 1)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # creates the CUDA events
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        moe.moe_set_next_stage_events(evs[k])
+        eager()
+    torch.cuda.synchronize()
     stage_ms = {name: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
                 for i, name in enumerate(moe.STAGE_NAMES)}
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
@@ -405,14 +448,28 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_block(cfg, world), "roofline": roof, "block_roofline": block,
+            "config": dict(config_block(cfg, world),
+                           launch="CUDA graph replay" if args.graph else "eager launches"),
+            "roofline": roof, "block_roofline": block,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                        "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
             "stage_ms": {k: round(v, 5) for k, v in stage_mean.items()},
-            "expert_path": "tcgen05" if T * K >= 32 * E else "streaming",
+            "expert_path": expert_path_name(args.expert_path, cfg),
         }
         print(json.dumps(line), flush=True)
+
+
+def expert_path_name(flag, cfg):
+    """Which expert kernels the library runs for this flag and shape."""
+    wt_ok = cfg.I % 128 == 0 and cfg.H % 256 == 0
+    if flag == "auto":
+        if cfg.T * cfg.K >= 32 * cfg.E:
+            return "tcgen05"
+        return "tcgen05_wt" if wt_ok else "streaming"
+    if flag == "tcgen05_wt" and not wt_ok:
+        return "streaming"
+    return flag
 
 
 def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev):

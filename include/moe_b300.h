@@ -159,13 +159,25 @@ const char* moe_strerror(int status);
 int moe_last_cuda_error(void);
 
 /* Kernel-path selection for the expert MLPs (process-wide):
- *   MOE_PATH_AUTO      tensor-core grouped GEMMs when the average expert
- *                      receives enough rows to fill a tile, else the
- *                      weight-streaming kernels (decode-sized batches);
- *   MOE_PATH_STREAMING always the weight-streaming kernels;
- *   MOE_PATH_TCGEN05   always the tcgen05 grouped GEMMs.
+ *   MOE_PATH_AUTO         tcgen05 grouped GEMMs with token rows on the MMA's
+ *                         M side when the average expert receives >= 32 rows
+ *                         (P >= 32*E); below that the tcgen05 kernels with the
+ *                         expert weights on the M side, or, for shapes those
+ *                         cannot tile, the weight-streaming kernels;
+ *   MOE_PATH_STREAMING    always the weight-streaming CUDA-core kernels;
+ *   MOE_PATH_TCGEN05      always the token-rows-as-M tcgen05 grouped GEMMs;
+ *   MOE_PATH_TCGEN05_WT   always the weights-as-M tcgen05 kernels where the
+ *                         shape allows (I % 128 == 0 and H % 256 == 0), else
+ *                         the weight-streaming kernels.
+ * Every path computes the same function; results agree within the fp32
+ * accumulation-order tolerance (not bitwise across paths).
  * Returns the previous setting, or -1 for an unknown value. */
-enum moe_path { MOE_PATH_AUTO = 0, MOE_PATH_STREAMING = 1, MOE_PATH_TCGEN05 = 2 };
+enum moe_path {
+    MOE_PATH_AUTO = 0,
+    MOE_PATH_STREAMING = 1,
+    MOE_PATH_TCGEN05 = 2,
+    MOE_PATH_TCGEN05_WT = 3
+};
 int moe_set_expert_path(int path);
 
 /* ---- benchmark instrumentation ------------------------------------------ */

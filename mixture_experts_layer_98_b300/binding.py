@@ -21,6 +21,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_PATH_AUTO = 0
 MOE_PATH_STREAMING = 1
 MOE_PATH_TCGEN05 = 2
+MOE_PATH_TCGEN05_WT = 3
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",

@@ -197,12 +197,20 @@ static void remember_counts(cudaStream_t st, const Workspace& ws, int E) {
     w.E = E;
 }
 
-static bool use_tcgen05(const Sizes& s) {
-    if (g_expert_path == MOE_PATH_STREAMING) return false;
-    if (g_expert_path == MOE_PATH_TCGEN05) return true;
-    // Tensor-core tiles are 128 rows; below ~32 rows per expert on average the
-    // work is weight-bandwidth bound and streaming reads each weight once.
-    return s.P() >= 32LL * s.E;
+enum class ExpertPath { kStreaming, kTokensM, kWeightsM };
+
+static ExpertPath expert_path(const Sizes& s) {
+    const bool wt_ok = experts_wt_supported(s);
+    switch (g_expert_path) {
+        case MOE_PATH_STREAMING: return ExpertPath::kStreaming;
+        case MOE_PATH_TCGEN05: return ExpertPath::kTokensM;
+        case MOE_PATH_TCGEN05_WT: return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
+        default: break;
+    }
+    // Token rows fill 128-row tiles from ~32 rows per expert on average up;
+    // below that the weights go on the MMA's M side (every stage is weights).
+    if (s.P() >= 32LL * s.E) return ExpertPath::kTokensM;
+    return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
 }
 
 // The kernel sequence.  All pointers checked by the caller.
@@ -231,14 +239,21 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
     if (e != cudaSuccess) return cuda_status(e);
     const int n_partials = s.nrouter();
     mark(1, st);
-    const bool tc = use_tcgen05(s);
-    e = launch_dispatch(idx, w, tc ? x : nullptr, s, ws, tc ? kTcRows : kStreamRows, ws.p_partial,
-                        n_partials, aux, st);
+    const ExpertPath path = expert_path(s);
+    const int tile_rows = path == ExpertPath::kTokensM   ? kTcRows
+                          : path == ExpertPath::kWeightsM ? kWtRows
+                                                          : kStreamRows;
+    // The tensor-core paths read gathered rows (x_perm); streaming reads x.
+    e = launch_dispatch(idx, w, path == ExpertPath::kStreaming ? nullptr : x, s, ws, tile_rows,
+                        ws.p_partial, n_partials, aux, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
     cudaEvent_t mid = t_cur_ev[3];
-    e = tc ? launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid)
-           : launch_experts_streaming(x, Wg, Wu, Wd, s, ws, st, mid);
+    switch (path) {
+        case ExpertPath::kTokensM: e = launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid); break;
+        case ExpertPath::kWeightsM: e = launch_experts_wt(Wg, Wu, Wd, s, ws, st, mid); break;
+        default: e = launch_experts_streaming(x, Wg, Wu, Wd, s, ws, st, mid); break;
+    }
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
     e = launch_combine(ws.ybuf, ws.inv, s.T, s.K, s.H, out, st);
@@ -322,7 +337,7 @@ int moe_stage_times(float* ms, int n) {
 }
 
 int moe_set_expert_path(int path) {
-    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05) return -1;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05_WT) return -1;
     const int prev = g_expert_path;
     g_expert_path = path;
     return prev;

@@ -19,6 +19,7 @@ constexpr int kChunkTokens = 256;    // tokens per dispatch chunk (one CTA)
 constexpr int kRouterTokens = 32;    // tokens per router CTA (SIMT router)
 constexpr int kStreamRows = 8;       // rows per tile of the weight-streaming kernels
 constexpr int kTcRows = 128;         // rows per tile of the tcgen05 grouped GEMMs
+constexpr int kWtRows = 64;          // rows per tile of the weights-as-M tcgen05 kernels
 constexpr int kRouterMaxSplits = 4;  // slices of H the tensor-core router may split into
 
 // One tile of token-expert rows, all routed to one expert: rows
@@ -99,6 +100,13 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16
 cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                    const __nv_bfloat16* Wd, const Sizes& s,
                                    const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
+// Small batches: the expert weights are the MMA's M side (128 weight rows per
+// MMA) and a tile's <= kWtRows token rows its N side; reads ws.x_perm.
+// Needs I % 128 == 0 and H % 256 == 0 (experts_wt_supported).
+bool experts_wt_supported(const Sizes& s);
+cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                              const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
+                              cudaStream_t st, cudaEvent_t ev_mid);
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
                            __nv_bfloat16* out, cudaStream_t st);
 
