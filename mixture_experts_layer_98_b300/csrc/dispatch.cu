@@ -21,7 +21,15 @@
 //             bitmaps -> perm_tok, perm_slot, inv, w_perm
 //   gather  : x_perm[row] = x[perm_tok[row]] for the tensor-core expert GEMMs
 //             (16-byte vectors); the streaming kernels read x through perm_tok
+//
+// A batch of at most one chunk (256 tokens) runs count, scan and scatter as
+// one CTA (dispatch_small_kernel); at most 32 tokens, that CTA also routes
+// them (softmax, top-k, renorm from the partial logits) and, up to 128 KB of
+// rows, gathers them, so a decode step has one kernel between the router
+// logits and the expert GEMMs.  It produces the same rows, tiles and aux bit
+// for bit as the chunked kernels.
 #include "moe_common.cuh"
+#include "routing.cuh"
 
 namespace moe {
 
@@ -195,6 +203,152 @@ __global__ void __launch_bounds__(kScatterThreads) dispatch_scatter_kernel(
     }
 }
 
+constexpr int kSmallThreads = 1024;
+static_assert(kSmallThreads == kScanThreads, "block_inclusive_scan's warp_tot size");
+static_assert(kRouteDispatchTokens <= kSmallThreads / 32, "one warp per routed token");
+
+// One CTA for T <= kChunkTokens (ROUTE: T <= kRouteDispatchTokens):
+//   ROUTE: warp t routes token t from the sum of nparts partial logits (in
+//          slice order), writing logits_out (may be null), idx, w and its
+//          probability row to shared memory;
+//   counts per expert and per-expert token bitmaps (shared-memory atomics);
+//   thread e < E: counts, offsets, tile table, aux term (probability sums as
+//          the chunked path forms them: from the routing rows in token order
+//          (ROUTE) or from p_partial's nrouter rows);
+//   scatter: row = offsets[e] + tokens before t that chose e.
+template <int EPL, bool ROUTE>
+__global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
+    const float* parts, int nparts, float* logits_out, int norm, int32_t* idx, float* w,
+    const float* p_partial, int nrouter, int T, int E, int K, int rows_per_tile,
+    int32_t* counts, int32_t* offsets, RowTile* tiles, int32_t* n_tiles, int32_t* perm_tok,
+    int32_t* perm_slot, int32_t* inv, float* w_perm, float* aux, const uint4* x,
+    uint4* x_perm, int vec_per_row) {
+    // ROUTE: probability rows [T][E]; otherwise [4][kMaxExperts] partial sums
+    __shared__ float prob_s[kRouteDispatchTokens * kMaxExperts];
+    __shared__ int tok_s[ROUTE ? kRouteDispatchTokens * kMaxTopK : 1];  // token of each row
+    __shared__ uint32_t sel[kMaxExperts * kWords];
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int base_s[kMaxExperts];
+    __shared__ float term_s[kMaxExperts];
+    __shared__ int warp_tot[kSmallThreads / 32];
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < E * kWords; i += blockDim.x) sel[i] = 0u;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+    pdl_wait();
+    if (ROUTE) {
+        if (warp < T) {  // warp-uniform: one warp per token
+            const int t = warp;
+            float l[EPL];
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) {
+                const int e = lane + 32 * q;
+                if (e < E) {
+                    float v = parts[(size_t)t * E + e];
+                    for (int sl = 1; sl < nparts; ++sl) v += parts[((size_t)sl * T + t) * E + e];
+                    l[q] = v;
+                    if (logits_out) logits_out[(size_t)t * E + e] = v;
+                } else {
+                    l[q] = -INFINITY;
+                }
+            }
+            route_token<EPL>(l, E, K, norm, idx + (size_t)t * K, w + (size_t)t * K,
+                             prob_s + t * E);
+        }
+    } else if (aux) {
+        // four threads per expert add up rows j, j+4, ... of p_partial
+        const int pe = tid % kMaxExperts, pj = tid / kMaxExperts;
+        if (pe < E) {
+            float a0 = 0.f, a1 = 0.f;
+            int b = pj;
+            for (; b + 4 < nrouter; b += 8) {
+                a0 += p_partial[(size_t)b * E + pe];
+                a1 += p_partial[(size_t)(b + 4) * E + pe];
+            }
+            if (b < nrouter) a0 += p_partial[(size_t)b * E + pe];
+            prob_s[pj * kMaxExperts + pe] = a0 + a1;
+        }
+    }
+    __syncthreads();  // routing results (global idx/w written by this CTA) visible
+    const int P = T * K;
+    for (int i = tid; i < P; i += blockDim.x) {
+        const int t = i / K;
+        const int e = idx[i];
+        atomicAdd(&cnt[e], 1);
+        atomicOr(&sel[e * kWords + (t >> 5)], 1u << (t & 31));
+    }
+    __syncthreads();
+    const int e = tid;
+    const bool own = e < E;
+    const int run = own ? cnt[e] : 0;
+    const int nt = own ? (run + rows_per_tile - 1) / rows_per_tile : 0;
+    const int off_incl = block_inclusive_scan(run, warp_tot);
+    const int toff_incl = block_inclusive_scan(nt, warp_tot);
+    const int base = off_incl - run;
+    const int tbase = toff_incl - nt;
+    if (own) {
+        counts[e] = run;
+        offsets[e] = base;
+        base_s[e] = base;
+        if (e == E - 1) {
+            offsets[E] = off_incl;
+            *n_tiles = toff_incl;
+        }
+        for (int j = 0; j < nt; ++j) {
+            RowTile tl;
+            tl.expert = e;
+            tl.row0 = base + j * rows_per_tile;
+            tl.nrows = min(rows_per_tile, run - j * rows_per_tile);
+            tl.pad = 0;
+            tiles[tbase + j] = tl;
+        }
+        if (aux) {
+            float psum;
+            if (ROUTE) {
+                psum = 0.f;
+                for (int t = 0; t < T; ++t) psum += prob_s[t * E + e];
+            } else {
+                psum = ((prob_s[e] + prob_s[kMaxExperts + e]) + prob_s[2 * kMaxExperts + e]) +
+                       prob_s[3 * kMaxExperts + e];
+            }
+            const float f = (float)run / ((float)T * (float)K);
+            term_s[e] = f * (psum / (float)T);
+        }
+    }
+    __syncthreads();
+    if (aux && tid < 32) {  // fixed-order reduction over the experts
+        float v = 0.f;
+        for (int j = tid; j < E; j += 32) v += term_s[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (tid == 0) *aux = (float)E * v;
+    }
+    for (int i = tid; i < P; i += blockDim.x) {
+        const int t = i / K, k = i - t * K, word = t >> 5, bit = t & 31;
+        const int ex = idx[i];
+        const uint32_t* sb = sel + ex * kWords;
+        int rank = __popc(sb[word] & ((1u << bit) - 1u));
+        for (int j = 0; j < word; ++j) rank += __popc(sb[j]);
+        const int row = base_s[ex] + rank;
+        perm_tok[row] = t;
+        if (perm_slot) perm_slot[row] = k;
+        inv[i] = row;
+        if (w_perm) w_perm[row] = w[i];
+        if (ROUTE) tok_s[row] = t;
+    }
+    if (ROUTE && x) {
+        // Small batches gather here: x_perm[row] = x[token of row].  x is the
+        // caller's input, finished before the forward's first kernel passed
+        // its dependency wait, so the read-only path is allowed.
+        __syncthreads();
+        const int n = P * vec_per_row;
+        for (int v = tid; v < n; v += blockDim.x) {
+            const int row = v / vec_per_row, c = v - row * vec_per_row;
+            x_perm[(size_t)row * vec_per_row + c] = __ldg(x + (size_t)tok_s[row] * vec_per_row + c);
+        }
+    }
+}
+
 // x_perm[row, :] = x[perm_tok[row], :]; one warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
                                                           const int32_t* perm_tok,
@@ -216,36 +370,86 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
     }
 }
 
+cudaError_t launch_gather(const __nv_bfloat16* x, const Sizes& s, const Workspace& ws,
+                          cudaStream_t st) {
+    const long long P = s.P();
+    long long blocks = (P + 7) / 8;
+    const long long cap = (long long)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                               reinterpret_cast<const uint4*>(x), (const int32_t*)ws.perm_tok, P,
+                               s.H / 8, reinterpret_cast<uint4*>(ws.x_perm));
+    count_launches(1);
+    return e;
+}
+
+template <int EPL>
+cudaError_t launch_small(const float* parts, int nparts, float* logits_out, int norm,
+                         int32_t* idx, float* w, const Sizes& s, const Workspace& ws,
+                         int rows_per_tile, float* aux, const __nv_bfloat16* x,
+                         cudaStream_t st) {
+    cudaError_t e = launch_pdl(dispatch_small_kernel<EPL, true>, dim3(1), dim3(kSmallThreads), 0,
+                               st, parts, nparts, logits_out, norm, idx, w, (const float*)nullptr,
+                               0, s.T, s.E, s.K, rows_per_tile, ws.counts, ws.offsets, ws.tiles,
+                               ws.n_tiles, ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm, aux,
+                               reinterpret_cast<const uint4*>(x),
+                               reinterpret_cast<uint4*>(ws.x_perm), s.H / 8);
+    count_launches(1);
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
                             const float* p_partial, int n_partials, float* aux, cudaStream_t st) {
     const int nch = s.nchunks();
-    cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kChunkTokens), 0, st, idx,
-                               s.T, s.E, s.K, ws.chunk_counts);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, st,
-        ws.chunk_counts, ws.chunk_base, nch, s.T, s.E, s.K, ws.counts, ws.offsets, ws.tiles,
-        ws.n_tiles, rows_per_tile, p_partial, n_partials, aux);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(dispatch_scatter_kernel, dim3(nch), dim3(kScatterThreads), 0, st, idx, w, s.T,
-                   s.E, s.K, (const int32_t*)ws.offsets, (const int32_t*)ws.chunk_base,
-                   ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm);
-    count_launches(3);
-    if (e != cudaSuccess) return e;
-    if (x) {
-        const long long P = s.P();
-        long long blocks = (P + 7) / 8;
-        const long long cap = (long long)num_sms() * 8;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
-        e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                       reinterpret_cast<const uint4*>(x), (const int32_t*)ws.perm_tok, P, s.H / 8,
-                       reinterpret_cast<uint4*>(ws.x_perm));
+    cudaError_t e;
+    if (nch == 1) {
+        e = launch_pdl(dispatch_small_kernel<1, false>, dim3(1), dim3(kSmallThreads), 0, st,
+                       (const float*)nullptr, 0, (float*)nullptr, 0, const_cast<int32_t*>(idx),
+                       const_cast<float*>(w), p_partial, n_partials, s.T, s.E, s.K,
+                       rows_per_tile, ws.counts, ws.offsets, ws.tiles, ws.n_tiles, ws.perm_tok,
+                       ws.perm_slot, ws.inv, ws.w_perm, aux, (const uint4*)nullptr,
+                       (uint4*)nullptr, 0);
         count_launches(1);
+    } else {
+        e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kChunkTokens), 0, st, idx, s.T, s.E,
+                       s.K, ws.chunk_counts);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, st,
+            ws.chunk_counts, ws.chunk_base, nch, s.T, s.E, s.K, ws.counts, ws.offsets, ws.tiles,
+            ws.n_tiles, rows_per_tile, p_partial, n_partials, aux);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(dispatch_scatter_kernel, dim3(nch), dim3(kScatterThreads), 0, st, idx, w,
+                       s.T, s.E, s.K, (const int32_t*)ws.offsets, (const int32_t*)ws.chunk_base,
+                       ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm);
+        count_launches(3);
     }
-    return e;
+    if (e != cudaSuccess) return e;
+    return x ? launch_gather(x, s, ws, st) : cudaSuccess;
+}
+
+cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* logits_out,
+                                        int norm, int32_t* idx, float* w,
+                                        const __nv_bfloat16* x, const Sizes& s,
+                                        const Workspace& ws, int rows_per_tile, float* aux,
+                                        cudaStream_t st) {
+    if (s.T > kRouteDispatchTokens) return cudaErrorInvalidValue;
+    // Up to 128 KB of gathered rows are copied by the routing CTA itself (one
+    // or two decode tokens); more go to the gather kernel, which spreads them
+    // over the SMs.
+    const bool in_cta = x && s.P() * s.H * 2 <= (128 << 10);
+    const __nv_bfloat16* xk = in_cta ? x : nullptr;
+    const int epl = (s.E + 31) / 32;
+    cudaError_t e;
+    if (epl <= 1) e = launch_small<1>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else if (epl <= 2) e = launch_small<2>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else if (epl <= 4) e = launch_small<4>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else e = launch_small<8>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    if (e != cudaSuccess) return e;
+    return x && !in_cta ? launch_gather(x, s, ws, st) : cudaSuccess;
 }
 
 }  // namespace moe

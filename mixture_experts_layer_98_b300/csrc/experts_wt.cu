@@ -22,8 +22,15 @@
 //             Y[row0 + j, n0 + i] = bf16(w[row0 + j] · D)
 //
 // One work item is (row tile, block of weight rows): 128 gate rows with the
-// same 128 up rows, or 256 down rows.  Persistent, warp-specialised CTA (one
-// per SM, 192 threads):
+// same 128 up rows, or 256 down rows.  When a batch has fewer items than
+// about one per SM (a single decode token touches 8 experts: 96 gate/up
+// items), each item is split along K into ksplit slices so that every SM
+// streams weights: a slice stores its fp32 accumulators, and the last slice
+// to finish (per-item arrival counter) adds all slices in slice order and runs
+// the epilogue, so the result does not depend on which slice finishes last.
+// The counters are zeroed by the router kernel at the start of each forward
+// and reset by their last arriver.  Persistent, warp-specialised CTA (one per
+// SM, 192 threads):
 //   warp 0     TMA producer: two 128x64 weight tiles and ceil(rows/16) 16x64
 //              token boxes per k-block into a 5-stage ring (128-byte swizzle)
 //   warp 1     owns TMEM (two buffers x two accumulators x 64 columns) and
@@ -63,12 +70,32 @@ struct WtParams {
     const int32_t* n_tiles;
     int n_blk;              // weight-row blocks per row tile
     int num_kb;             // k-blocks of 64
+    int ksplit;             // K slices per item (1: no split)
+    int kb_per;             // k-blocks per slice
+    float* partial;         // [items][ksplit][2][part_rows][128] slice accumulators
+    int part_rows;
+    int32_t* counters;      // [items][4]: slices finished, per epilogue warp
     int w_rows_per_expert;  // I (gate/up) or H (down)
     __nv_bfloat16* out;     // h [P, I] or Y [P, H]
     int out_ld;
     const float* w_perm;    // routing weight per row (down)
     int32_t* status;
 };
+
+// Epilogue of one output row and weight row i of the block: gate/up writes
+// h = silu(D0)·D1; down writes Y = w·D0 and Y = w·D1 for the two 128-row halves.
+template <int MODE>
+__device__ __forceinline__ void store_out(const WtParams& p, size_t row, int blk, int i, float d0,
+                                          float d1) {
+    if (MODE == kGateUp) {
+        p.out[row * p.out_ld + (size_t)blk * kWM + i] = __float2bfloat16_rn(silu_f(d0) * d1);
+    } else {
+        const float wr = p.w_perm[row];
+        __nv_bfloat16* o = p.out + row * p.out_ld + (size_t)blk * (2 * kWM);
+        o[i] = __float2bfloat16_rn(wr * d0);
+        o[kWM + i] = __float2bfloat16_rn(wr * d1);
+    }
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -114,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     pdl_wait();  // the prologue above overlaps the previous kernel's tail
-    const int total = (*p.n_tiles) * p.n_blk;
+    const int total = (*p.n_tiles) * p.n_blk * p.ksplit;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -124,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long issued = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                const RowTile tl = p.tiles[item / p.n_blk];
-                const int blk = item % p.n_blk;
+                const int pitem = item / p.ksplit, ks = item % p.ksplit;
+                const RowTile tl = p.tiles[pitem / p.n_blk];
+                const int blk = pitem % p.n_blk;
+                const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
                 const int nbox = (tl.nrows + kBox - 1) / kBox;
                 int a0, a1;
                 if (MODE == kGateUp) {
@@ -135,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a1 = a0 + kWM;
                 }
                 const uint32_t bytes = 2 * kABytes + nbox * kBoxBytes;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_s,
                                                 kTimeoutNs)) {
                         ok = false;
@@ -175,7 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                const int nrows = p.tiles[item / p.n_blk].nrows;
+                const int pitem = item / p.ksplit, ks = item % p.ksplit;
+                const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
+                const int nrows = p.tiles[pitem / p.n_blk].nrows;
                 const int n = ((nrows + kBox - 1) / kBox) * kBox;
                 const uint32_t idesc = ptx::idesc_bf16_f32(kWM, n);
                 if (!ptx::mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_s,
@@ -186,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t d0 = tmem_base + (uint32_t)acc * (2 * kAccCols);
                 const uint32_t d1 = d0 + kAccCols;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, &abort_s, kTimeoutNs)) {
                         ok = false;
                         break;
@@ -198,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = ptx::desc_sw128_kmajor(a_addr + 2 * kABytes);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {  // K = 16 per MMA: +32 bytes
-                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+                        const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
                         ptx::mma_bf16(d0, adesc0 + 2u * k, bdesc + 2u * k, idesc, accum);
                         ptx::mma_bf16(d1, adesc1 + 2u * k, bdesc + 2u * k, idesc, accum);
                     }
@@ -228,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
-            const RowTile tl = p.tiles[item / p.n_blk];
-            const int blk = item % p.n_blk;
+            const int pitem = item / p.ksplit, ks = item % p.ksplit;
+            const RowTile tl = p.tiles[pitem / p.n_blk];
+            const int blk = pitem % p.n_blk;
             int ok = 1;
             if (lane == 0)
                 ok = ptx::mbar_wait_bounded(&tfull_bar[acc], acc_phase, &abort_s, kTimeoutNs);
@@ -243,33 +275,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (uint32_t)acc * (2 * kAccCols);
             const uint32_t t1 = t0 + kAccCols;
             const int n = ((tl.nrows + kBox - 1) / kBox) * kBox;
+            if (p.ksplit == 1) {
 #pragma unroll 1
-            for (int c = 0; c < n; c += kBox) {
-                uint32_t v0[kBox], v1[kBox];
-                ptx::tmem_ld16(t0 + c, v0);
-                ptx::tmem_ld16(t1 + c, v1);
-                ptx::tmem_ld_wait();
+                for (int c = 0; c < n; c += kBox) {
+                    uint32_t v0[kBox], v1[kBox];
+                    ptx::tmem_ld16(t0 + c, v0);
+                    ptx::tmem_ld16(t1 + c, v1);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < kBox; ++j) {
-                    if (c + j < tl.nrows) {
-                        const size_t row = (size_t)tl.row0 + c + j;
-                        if (MODE == kGateUp) {
-                            const float hv =
-                                silu_f(__uint_as_float(v0[j])) * __uint_as_float(v1[j]);
-                            p.out[row * p.out_ld + (size_t)blk * kWM + i] =
-                                __float2bfloat16_rn(hv);
-                        } else {
-                            const float wr = p.w_perm[row];
-                            __nv_bfloat16* o = p.out + row * p.out_ld + (size_t)blk * (2 * kWM);
-                            o[i] = __float2bfloat16_rn(wr * __uint_as_float(v0[j]));
-                            o[kWM + i] = __float2bfloat16_rn(wr * __uint_as_float(v1[j]));
+                    for (int j = 0; j < kBox; ++j)
+                        if (c + j < tl.nrows)
+                            store_out<MODE>(p, (size_t)tl.row0 + c + j, blk, i,
+                                            __uint_as_float(v0[j]), __uint_as_float(v1[j]));
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
+            } else {
+                // This slice's accumulators -> partial[pitem][ks] (rows j, column i:
+                // each warp store is 128 contiguous bytes), then free TMEM.
+                const size_t slice = (size_t)2 * p.part_rows * kWM;
+                float* mine = p.partial + ((size_t)pitem * p.ksplit + ks) * slice;
+#pragma unroll 1
+                for (int c = 0; c < n; c += kBox) {
+                    uint32_t v0[kBox], v1[kBox];
+                    ptx::tmem_ld16(t0 + c, v0);
+                    ptx::tmem_ld16(t1 + c, v1);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < kBox; ++j)
+                        if (c + j < tl.nrows) {
+                            __stcg(mine + (size_t)(c + j) * kWM + i, __uint_as_float(v0[j]));
+                            __stcg(mine + ((size_t)p.part_rows + c + j) * kWM + i,
+                                   __uint_as_float(v1[j]));
                         }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
+                // Publish, count; the last slice of this item (per warp
+                // quadrant) adds all slices in slice order.
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&p.counters[pitem * 4 + q], 1) == p.ksplit - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    const float* all = p.partial + (size_t)pitem * p.ksplit * slice;
+#pragma unroll 1
+                    for (int j = 0; j < tl.nrows; ++j) {
+                        float a0 = 0.f, a1 = 0.f;
+                        for (int sl = 0; sl < p.ksplit; ++sl) {
+                            const float* src = all + (size_t)sl * slice;
+                            a0 += __ldcg(src + (size_t)j * kWM + i);
+                            a1 += __ldcg(src + ((size_t)p.part_rows + j) * kWM + i);
+                        }
+                        store_out<MODE>(p, (size_t)tl.row0 + j, blk, i, a0, a1);
                     }
+                    if (lane == 0) p.counters[pitem * 4 + q] = 0;  // ready for the next forward
                 }
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -309,37 +375,105 @@ cudaError_t launch_wt(const void* A0, const void* A1, uint64_t a_rows, uint64_t 
 
 bool experts_wt_supported(const Sizes& s) { return s.I % kWM == 0 && s.H % (2 * kWM) == 0; }
 
+namespace {
+
+// Items below which the K split starts, and the grid the split is fitted to:
+// one CTA per SM of a 148-SM B300.  The plan must depend on the sizes only
+// (the workspace is sized from it before any device is known), so this is a
+// constant rather than the device's count.
+constexpr long long kSplitBelow = 148;
+
+// Fraction of the last round of a persistent grid of kSplitBelow CTAs that
+// n equal work items keep busy, over all rounds (1 = no idle tail).
+double round_fill(long long n) {
+    const long long rounds = (n + kSplitBelow - 1) / kSplitBelow;
+    return (double)n / (double)(rounds * kSplitBelow);
+}
+
+// K slices for `items` items of num_kb k-blocks: the slice count (at most 8,
+// at least 8 k-blocks per slice -- shorter slices measured slower, the
+// per-item epilogue and hand-off then dominate -- and no empty slice) whose
+// items fill the rounds of the persistent grid best; ties go to fewer slices.
+int split_for(long long items, int num_kb) {
+    if (items <= 0 || items >= kSplitBelow) return 1;
+    int best = 1;
+    double best_fill = round_fill(items);
+    for (int ks = 2; ks <= 8 && num_kb / ks >= 8; ++ks) {
+        const int kb_per = (num_kb + ks - 1) / ks;
+        if ((num_kb + kb_per - 1) / kb_per != ks) continue;  // would leave a slice empty
+        const double f = round_fill(items * ks);
+        if (f > best_fill + 0.02) {
+            best = ks;
+            best_fill = f;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+WtPlan wt_plan(const Sizes& s) {
+    WtPlan pl;
+    if (!experts_wt_supported(s) || s.T <= 0) return pl;
+    const long long P = s.P();
+    // Row tiles: sum over experts of ceil(count / kWtRows) <= P / kWtRows + experts touched.
+    long long tiles = (s.E < P ? s.E : P) + P / kWtRows;
+    if (tiles > s.max_tiles(kWtRows)) tiles = s.max_tiles(kWtRows);
+    pl.items_gu = tiles * (s.I / kWM);
+    pl.items_dn = tiles * (s.H / (2 * kWM));
+    pl.ks_gu = split_for(pl.items_gu, s.H / kBK);
+    pl.ks_dn = split_for(pl.items_dn, s.I / kBK);
+    // A tile holds at most one row per token, so at most min(kWtRows, T) rows.
+    pl.part_rows = s.T < kWtRows ? ((s.T + kBox - 1) / kBox) * kBox : kWtRows;
+    const size_t per_slice = (size_t)2 * pl.part_rows * kWM;
+    size_t need = 0;
+    if (pl.ks_gu > 1) need = (size_t)pl.items_gu * pl.ks_gu * per_slice;
+    if (pl.ks_dn > 1 && (size_t)pl.items_dn * pl.ks_dn * per_slice > need)
+        need = (size_t)pl.items_dn * pl.ks_dn * per_slice;
+    pl.partial_floats = need;
+    pl.n_counters = (int)((pl.ks_gu > 1 ? pl.items_gu : 0) + (pl.ks_dn > 1 ? pl.items_dn : 0)) * 4;
+    return pl;
+}
+
 cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                               const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid) {
     if (!experts_wt_supported(s)) return cudaErrorInvalidValue;
     const long long P = s.P();
-    const long long max_tiles = s.max_tiles(kWtRows);
+    const WtPlan pl = wt_plan(s);
     WtParams p{};
     p.tiles = ws.tiles;
     p.n_tiles = ws.n_tiles;
     p.status = ws.status;
     p.w_perm = ws.w_perm;
+    p.partial = ws.wt_partial;
+    p.part_rows = pl.part_rows;
 
     // gate/up: A0 = 128 W_gate rows, A1 = the same 128 W_up rows; B = x_perm rows
     p.n_blk = s.I / kWM;
     p.num_kb = s.H / kBK;
+    p.ksplit = pl.ks_gu;
+    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.counters = ws.status + 4;
     p.w_rows_per_expert = s.I;
     p.out = ws.hbuf;
     p.out_ld = s.I;
     cudaError_t err = launch_wt<kGateUp>(Wg, Wu, (uint64_t)s.E * s.I, s.H, ws.x_perm, P, p,
-                                         max_tiles * p.n_blk, st);
+                                         pl.items_gu * p.ksplit, st);
     if (err != cudaSuccess) return err;
     if (ev_mid) cudaEventRecord(ev_mid, st);
 
     // down: A0/A1 = W_down rows [n0, n0 + 128) and [n0 + 128, n0 + 256); B = h rows
     p.n_blk = s.H / (2 * kWM);
     p.num_kb = s.I / kBK;
+    p.ksplit = pl.ks_dn;
+    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.counters = ws.status + 4 + (pl.ks_gu > 1 ? pl.items_gu * 4 : 0);
     p.w_rows_per_expert = s.H;
     p.out = ws.ybuf;
     p.out_ld = s.H;
     return launch_wt<kDown>(Wd, Wd, (uint64_t)s.E * s.H, s.I, ws.hbuf, P, p,
-                            max_tiles * p.n_blk, st);
+                            pl.items_dn * p.ksplit, st);
 }
 
 }  // namespace moe

@@ -91,7 +91,10 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
     w.offsets = (int32_t*)take(((size_t)s.E + 1) * 4);
     w.tiles = (RowTile*)take((size_t)s.max_tiles(kStreamRows) * sizeof(RowTile));
     w.n_tiles = (int32_t*)take(4);
-    w.status = (int32_t*)take(16);
+    const WtPlan plan = wt_plan(s);
+    w.n_clear = 4 + plan.n_counters;
+    w.status = (int32_t*)take((size_t)w.n_clear * 4);
+    w.wt_partial = (float*)take(plan.partial_floats * 4);
     w.p_partial = (float*)take((size_t)s.nrouter() * s.E * 4);
     w.perm_tok = (int32_t*)take(P * 4);
     w.perm_slot = (int32_t*)take(P * 4);
@@ -201,15 +204,16 @@ enum class ExpertPath { kStreaming, kTokensM, kWeightsM };
 
 static ExpertPath expert_path(const Sizes& s) {
     const bool wt_ok = experts_wt_supported(s);
+    const ExpertPath tokens_m = ExpertPath::kTokensM;
     switch (g_expert_path) {
         case MOE_PATH_STREAMING: return ExpertPath::kStreaming;
-        case MOE_PATH_TCGEN05: return ExpertPath::kTokensM;
+        case MOE_PATH_TCGEN05: return tokens_m;
         case MOE_PATH_TCGEN05_WT: return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
         default: break;
     }
     // Token rows fill 128-row tiles from ~32 rows per expert on average up;
     // below that the weights go on the MMA's M side (every stage is weights).
-    if (s.P() >= 32LL * s.E) return ExpertPath::kTokensM;
+    if (s.P() >= 32LL * s.E) return tokens_m;
     return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
 }
 
@@ -222,30 +226,42 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
     if (!w) w = ws.topk_w;
     begin_marks();
     mark(0, st);
-    // Tensor-core router logits from one full 128-token tile up (E <= 128), else the
-    // CUDA-core logits kernel; then the per-token routing kernel either way.
-    const bool router_tc = s.T >= 128 && router_tc_supported(s);
-    cudaError_t e;
-    if (router_tc) {
-        const int nsplit = router_tc_splits(s);
-        e = launch_router_tc(x, Wr, s, nsplit, ws.logit_parts, ws.status, st);
-        if (e == cudaSuccess)
-            e = launch_route_from_logits(ws.logit_parts, nsplit, logits, s, norm, idx, w,
-                                         ws.p_partial, st);
-    } else {
-        e = launch_router(x, Wr, s, norm, logits, ws.logit_parts, idx, w, ws.p_partial, ws.status,
-                          st);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
-    const int n_partials = s.nrouter();
-    mark(1, st);
     const ExpertPath path = expert_path(s);
     const int tile_rows = path == ExpertPath::kTokensM   ? kTcRows
                           : path == ExpertPath::kWeightsM ? kWtRows
                                                           : kStreamRows;
-    // The tensor-core paths read gathered rows (x_perm); streaming reads x.
-    e = launch_dispatch(idx, w, path == ExpertPath::kStreaming ? nullptr : x, s, ws, tile_rows,
-                        ws.p_partial, n_partials, aux, st);
+    // The tensor-core expert paths read gathered rows (x_perm); streaming reads x.
+    const __nv_bfloat16* gather_x = path == ExpertPath::kStreaming ? nullptr : x;
+    // Router logits: tensor cores from one full 128-token tile up (E <= 128),
+    // else the CUDA-core kernel split over H.  Then routing and dispatch: one
+    // CTA for at most 32 tokens, else the routing kernel and the dispatch
+    // kernels.
+    const bool router_tc = s.T >= 128 && router_tc_supported(s);
+    const int n_partials = s.nrouter();
+    cudaError_t e;
+    if (router_tc) {
+        const int nsplit = router_tc_splits(s);
+        e = launch_router_tc(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
+        if (e == cudaSuccess)
+            e = launch_route_from_logits(ws.logit_parts, nsplit, logits, s, norm, idx, w,
+                                         ws.p_partial, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        mark(1, st);
+        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, st);
+    } else if (s.T <= kRouteDispatchTokens) {
+        const int nsplit = router_simt_splits(s);
+        e = launch_router_logits(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        mark(1, st);
+        e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, idx, w, gather_x, s,
+                                        ws, tile_rows, aux, st);
+    } else {
+        e = launch_router(x, Wr, s, norm, logits, ws.logit_parts, idx, w, ws.p_partial, ws.status,
+                          ws.n_clear, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        mark(1, st);
+        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
     cudaEvent_t mid = t_cur_ev[3];

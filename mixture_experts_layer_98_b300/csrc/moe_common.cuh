@@ -39,7 +39,10 @@ struct Workspace {
     int32_t* offsets;       // [E + 1]
     RowTile* tiles;         // [max_tiles]
     int32_t* n_tiles;       // [1]
-    int32_t* status;        // [4] device-side error words
+    int32_t* status;        // [4 + wt counters] device-side error words, then the
+                            // split-K arrival counters; all zeroed by the router
+    int n_clear;            // ints zeroed from status at the start of a forward
+    float* wt_partial;      // slice accumulators of the split weights-as-M kernels
     float* p_partial;       // [n_router_blocks, E]
     int32_t* perm_tok;      // [P]
     int32_t* perm_slot;     // [P]
@@ -68,16 +71,23 @@ struct Sizes {
 size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ------
-// CUDA-core router: expert-split logits kernel + per-token routing kernel;
-// writes s.nrouter() rows of probability sums.  logits_scratch [T,E] is used
-// when logits == null.
+// CUDA-core router: expert- and H-split logits kernel (partial logits in
+// parts [kRouterMaxSplits][T][E]) + per-token routing kernel; writes
+// s.nrouter() rows of probability sums; logits (may be null) gets the sum.
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, float* logits_scratch, int32_t* idx, float* w,
-                          float* p_partial, int32_t* status, cudaStream_t st);
+                          int norm, float* logits, float* parts, int32_t* idx, float* w,
+                          float* p_partial, int32_t* status, int n_clear, cudaStream_t st);
+// The logits kernel of launch_router alone (nsplit slices of H, from
+// router_simt_splits), for the small-batch path that routes in the dispatch.
+int router_simt_splits(const Sizes& s);
+cudaError_t launch_router_logits(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
+                                 int nsplit, float* parts, int32_t* status, int n_clear,
+                                 cudaStream_t st);
 // tcgen05 router logits: nsplit slices of H, partial logits [nsplit][T][E]
 // into parts (then launch_route_from_logits with those parts).
 cudaError_t launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                             int nsplit, float* parts, int32_t* status, cudaStream_t st);
+                             int nsplit, float* parts, int32_t* status, int n_clear,
+                             cudaStream_t st);
 int router_tc_splits(const Sizes& s);
 bool router_tc_supported(const Sizes& s);  // E <= 128
 // Softmax, top-k, renorm and per-32-token probability sums (s.nrouter() rows)
@@ -90,6 +100,16 @@ cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logi
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
                             const float* p_partial, int n_partials, float* aux, cudaStream_t st);
+// Batches of at most kRouteDispatchTokens tokens: routing (softmax, top-k,
+// renorm from nparts partial logits) and the whole dispatch (counts, offsets,
+// tile table, aux, permutation; gather when x != null) in one CTA, then the
+// gather kernel.
+constexpr int kRouteDispatchTokens = 32;
+cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* logits_out,
+                                        int norm, int32_t* idx, float* w,
+                                        const __nv_bfloat16* x, const Sizes& s,
+                                        const Workspace& ws, int rows_per_tile, float* aux,
+                                        cudaStream_t st);
 // ev_mid (may be null) is recorded between the gate/up and the down launch.
 // The streaming kernels stage their input rows from x through ws.perm_tok;
 // the tcgen05 kernels read the gathered rows from ws.x_perm.
@@ -104,6 +124,16 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
 // MMA) and a tile's <= kWtRows token rows its N side; reads ws.x_perm.
 // Needs I % 128 == 0 and H % 256 == 0 (experts_wt_supported).
 bool experts_wt_supported(const Sizes& s);
+// K-split plan of the weights-as-M kernels (a function of the sizes only, so
+// that the workspace size does not depend on the device).
+struct WtPlan {
+    int ks_gu = 1, ks_dn = 1;               // K slices of the gate/up and down items
+    long long items_gu = 0, items_dn = 0;   // upper bounds on the items
+    int part_rows = 0;                      // token rows kept per slice accumulator
+    size_t partial_floats = 0;              // slice-accumulator buffer
+    int n_counters = 0;                     // gate/up counters, then down counters
+};
+WtPlan wt_plan(const Sizes& s);
 cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                               const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);

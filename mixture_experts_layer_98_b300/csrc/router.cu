@@ -12,96 +12,11 @@
 // probabilities of their tokens (in token order) for the load-balance
 // statistic.
 #include "moe_common.cuh"
+#include "routing.cuh"
 
 namespace moe {
 
 namespace {
-
-// Order-preserving map of a float to uint32 (larger float -> larger key);
-// -0 is folded to +0 first, so equal floats give equal keys.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    const uint32_t u = __float_as_uint(v + 0.0f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
-
-// One warp routes one token whose E logits sit in l[] (lane holds experts
-// lane, lane+32, ...).  Writes idx/w for the token and, when probs != null,
-// the full softmax into probs[0..E).
-template <int EPL>
-__device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K, int norm,
-                                            int32_t* idx_row, float* w_row, float* probs) {
-    const int lane = threadIdx.x & 31;
-    float m = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < EPL; ++q)
-        if (lane + 32 * q < E) m = fmaxf(m, l[q]);
-    m = warp_max(m);
-    float ex[EPL];
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-        ex[q] = (lane + 32 * q < E) ? expf(l[q] - m) : 0.f;
-        s += ex[q];
-    }
-    s = warp_sum(s);
-    const float inv_s = 1.0f / s;
-    float p[EPL];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-        p[q] = ex[q] * inv_s;
-        if (probs && lane + 32 * q < E) probs[lane + 32 * q] = p[q];
-    }
-    // K rounds of a warp-wide arg-max: the largest key, then the lowest expert
-    // index among the lanes holding it (two redux.sync per round).  The
-    // winner's probability is recomputed from its value in every lane.
-    uint32_t key[EPL];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) key[q] = (lane + 32 * q < E) ? order_key(l[q]) : 0u;
-    float wsum = 0.f;
-    int my_e = -1;
-    float my_p = 0.f;
-    for (int k = 0; k < K; ++k) {
-        uint32_t bk = 0u;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q)  // experts of a lane come in increasing index
-            if (key[q] > bk) {
-                bk = key[q];
-                be = lane + 32 * q;
-            }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        const int we = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)be : 0x7fffffffu);
-#pragma unroll
-        for (int q = 0; q < EPL; ++q)  // taken
-            if (we == lane + 32 * q) key[q] = 0u;
-        const float pk = expf(key_value(mk) - m) * inv_s;
-        wsum += pk;  // same value and order in every lane
-        if (lane == k) {
-            my_e = we;
-            my_p = pk;
-        }
-    }
-    if (lane < K) {
-        idx_row[lane] = my_e;
-        w_row[lane] = norm ? my_p / wsum : my_p;
-    }
-}
 
 constexpr int kSplitWarps = 8;   // experts per logits CTA (one warp each)
 constexpr int kSplitTokens = 8;  // tokens per logits CTA (staged in shared memory)
@@ -118,43 +33,53 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b, float
     return acc;
 }
 
-// logits[t,e] = x[t]·W_router[e] in fp32.  Grid (ceil(T/8), ceil(E/8)): a CTA
-// stages 8 token rows in shared memory and each of its 8 warps streams one
-// router row with 16-byte loads, so even a single token spreads the router
-// weights over E/8 SMs.  The first CTA also clears the forward's status word.
+// logits[t,e] = x[t]·W_router[e] in fp32.  Grid (ceil(T/8), ceil(E/8), nsplit):
+// a CTA stages 8 token rows of its slice of H (H/nsplit columns) in shared
+// memory and each of its 8 warps streams that slice of one router row with
+// 16-byte loads, writing partial logits to parts + z·T·E (slice z).  A single
+// token thus spreads the router weights over nsplit·E/8 CTAs with a few loads
+// in flight per lane.  The first CTA also zeroes the forward's status words
+// (status[0..n_clear)).
 __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
     const __nv_bfloat16* x, const __nv_bfloat16* Wr, int T, int H,
-    int E, float* logits, int32_t* status) {
-    extern __shared__ uint4 xs[];  // [kSplitTokens][H/8]
+    int E, float* parts, int32_t* status, int n_clear) {
+    extern __shared__ uint4 xs[];  // [kSplitTokens][H/nsplit/8]
     pdl_trigger();
     pdl_wait();
-    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
-    const int vpr = H / 8;
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < n_clear; i += blockDim.x) status[i] = 0;
+    const int vpr = H / 8;                 // 16-byte vectors per row
+    const int vps = vpr / gridDim.z;       // ... per slice
+    const int c0 = blockIdx.z * vps;
     const int t0 = blockIdx.x * kSplitTokens;
     const int nt = min(kSplitTokens, T - t0);
-    const uint4* xg = reinterpret_cast<const uint4*>(x) + (size_t)t0 * vpr;
-    for (int i = threadIdx.x; i < nt * vpr; i += blockDim.x) xs[i] = xg[i];
+    const uint4* xg = reinterpret_cast<const uint4*>(x) + (size_t)t0 * vpr + c0;
+    for (int i = threadIdx.x; i < nt * vps; i += blockDim.x) {
+        const int m = i / vps, c = i - m * vps;
+        xs[i] = xg[(size_t)m * vpr + c];
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = blockIdx.y * kSplitWarps + warp;
     if (e >= E) return;
-    const uint4* wr = reinterpret_cast<const uint4*>(Wr) + (size_t)e * vpr;
+    const uint4* wr = reinterpret_cast<const uint4*>(Wr) + (size_t)e * vpr + c0;
     float acc[kSplitTokens];
 #pragma unroll
     for (int m = 0; m < kSplitTokens; ++m) acc[m] = 0.f;
 #pragma unroll 4
-    for (int c = lane; c < vpr; c += 32) {
+    for (int c = lane; c < vps; c += 32) {
         const uint4 wv = wr[c];
 #pragma unroll
         for (int m = 0; m < kSplitTokens; ++m)
-            if (m < nt) acc[m] = dot8_bf16(wv, xs[m * vpr + c], acc[m]);
+            if (m < nt) acc[m] = dot8_bf16(wv, xs[m * vps + c], acc[m]);
     }
+    float* out = parts + (size_t)blockIdx.z * T * E;
 #pragma unroll
     for (int m = 0; m < kSplitTokens; ++m) {
         float v = acc[m];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == m && m < nt) logits[(size_t)(t0 + m) * E + e] = v;
+        if (lane == m && m < nt) out[(size_t)(t0 + m) * E + e] = v;
     }
 }
 
@@ -213,19 +138,39 @@ cudaError_t launch_route_t(const float* parts, int nparts, float* logits_out, co
 
 }  // namespace
 
-cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, float* logits_scratch, int32_t* idx, float* w,
-                          float* p_partial, int32_t* status, cudaStream_t st) {
-    float* lg = logits ? logits : logits_scratch;
-    const int smem = kSplitTokens * s.H * 2;
-    cudaError_t err = ensure_smem((const void*)router_logits_split_kernel, smem);
+int router_simt_splits(const Sizes& s) {
+    // Slices of H: enough CTAs to cover the SMs about twice (at most
+    // kRouterMaxSplits, and H/nsplit a multiple of 8 columns).
+    const int tiles = ((s.T + kSplitTokens - 1) / kSplitTokens) *
+                      ((s.E + kSplitWarps - 1) / kSplitWarps);
+    int nsplit = 1;
+    while (nsplit < kRouterMaxSplits && tiles * nsplit < 2 * num_sms() &&
+           (s.H / 8) % (2 * nsplit) == 0)
+        nsplit *= 2;
+    return nsplit;
+}
+
+cudaError_t launch_router_logits(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
+                                 int nsplit, float* parts, int32_t* status, int n_clear,
+                                 cudaStream_t st) {
+    const int smem = kSplitTokens * (s.H / nsplit) * 2;
+    cudaError_t err = ensure_smem((const void*)router_logits_split_kernel, kSplitTokens * s.H * 2);
     if (err != cudaSuccess) return err;
-    dim3 grid((s.T + kSplitTokens - 1) / kSplitTokens, (s.E + kSplitWarps - 1) / kSplitWarps);
+    dim3 grid((s.T + kSplitTokens - 1) / kSplitTokens, (s.E + kSplitWarps - 1) / kSplitWarps,
+              nsplit);
     err = launch_pdl(router_logits_split_kernel, grid, dim3(kSplitWarps * 32), smem, st, x, Wr, s.T,
-                     s.H, s.E, lg, status);
+                     s.H, s.E, parts, status, n_clear);
     count_launches(1);
+    return err;
+}
+
+cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
+                          int norm, float* logits, float* parts, int32_t* idx, float* w,
+                          float* p_partial, int32_t* status, int n_clear, cudaStream_t st) {
+    const int nsplit = router_simt_splits(s);
+    cudaError_t err = launch_router_logits(x, Wr, s, nsplit, parts, status, n_clear, st);
     if (err != cudaSuccess) return err;
-    return launch_route_from_logits(lg, 1, nullptr, s, norm, idx, w, p_partial, st);
+    return launch_route_from_logits(parts, nsplit, logits, s, norm, idx, w, p_partial, st);
 }
 
 cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,

@@ -23,7 +23,8 @@
 // chain over all of H drifts by ~1e-5 at H = 4096, which would eat into the
 // margin that separates genuine near-ties in the top-k.
 // Waits are bounded as in the expert GEMMs; a timeout writes MOE_ERR_TIMEOUT to
-// the status word.
+// the status word.  The first CTA zeroes the forward's status words
+// (status[0..n_clear)) after its dependency wait.
 #include "moe_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const __nv_bfloat16* x,
                      const __nv_bfloat16* Wr, int T, int H, int E, int nsplit,
-                     float* parts, int32_t* status) {
+                     float* parts, int32_t* status, int n_clear) {
     constexpr int N = NCH * 32;
     constexpr int kABytes = kRM * kRK * 2;
     constexpr int kStageBytes = kABytes + N * kRK * 2;
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     pdl_wait();  // the prologue above overlaps the previous kernel's tail
-    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+    if (status && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < n_clear; i += blockDim.x) status[i] = 0;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -224,14 +226,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
 template <int NCH>
 cudaError_t launch_router_tc_n(const CUtensorMap& mx, const CUtensorMap& mw,
                                const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                               int nsplit, float* parts, int32_t* status, cudaStream_t st) {
+                               int nsplit, float* parts, int32_t* status, int n_clear,
+                               cudaStream_t st) {
     const int ring = kRStages * (kRM * kRK * 2 + NCH * 32 * kRK * 2);
     const int smem = (ring > kRM * kRowPitch * 4 ? ring : kRM * kRowPitch * 4) + 1024;
     cudaError_t err = ensure_smem((const void*)router_tc_kernel<NCH>, smem);
     if (err != cudaSuccess) return err;
     dim3 grid((s.T + kRM - 1) / kRM, nsplit);
     err = launch_pdl(router_tc_kernel<NCH>, grid, dim3(kRThreads), smem, st, mx, mw, x, Wr, s.T,
-                     s.H, s.E, nsplit, parts, status);
+                     s.H, s.E, nsplit, parts, status, n_clear);
     count_launches(1);
     return err;
 }
@@ -249,7 +252,8 @@ int router_tc_splits(const Sizes& s) {
 }
 
 cudaError_t launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                             int nsplit, float* parts, int32_t* status, cudaStream_t st) {
+                             int nsplit, float* parts, int32_t* status, int n_clear,
+                             cudaStream_t st) {
     const int nch = (s.E + 31) / 32;
     if (nch > 4) return cudaErrorInvalidValue;
     CUtensorMap mx, mw;
@@ -257,10 +261,10 @@ cudaError_t launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr, co
         !make_tma_2d(&mw, Wr, (uint64_t)s.E, (uint64_t)s.H, (uint32_t)(nch * 32)))
         return cudaErrorInvalidValue;
     switch (nch) {
-        case 1: return launch_router_tc_n<1>(mx, mw, x, Wr, s, nsplit, parts, status, st);
-        case 2: return launch_router_tc_n<2>(mx, mw, x, Wr, s, nsplit, parts, status, st);
-        case 3: return launch_router_tc_n<3>(mx, mw, x, Wr, s, nsplit, parts, status, st);
-        default: return launch_router_tc_n<4>(mx, mw, x, Wr, s, nsplit, parts, status, st);
+        case 1: return launch_router_tc_n<1>(mx, mw, x, Wr, s, nsplit, parts, status, n_clear, st);
+        case 2: return launch_router_tc_n<2>(mx, mw, x, Wr, s, nsplit, parts, status, n_clear, st);
+        case 3: return launch_router_tc_n<3>(mx, mw, x, Wr, s, nsplit, parts, status, n_clear, st);
+        default: return launch_router_tc_n<4>(mx, mw, x, Wr, s, nsplit, parts, status, n_clear, st);
     }
 }
 

@@ -121,7 +121,11 @@ def test_tiny(moe, path):
     # shapes the weights-as-M kernels tile (I % 128 == 0, H % 256 == 0): one row,
     # ragged 16-row boxes, several 64-row tiles per expert, an expert with no rows
     (1, 256, 1, 1, 128, False), (17, 256, 8, 3, 256, True), (300, 256, 4, 2, 128, True),
-    (77, 512, 64, 6, 384, False)])
+    (77, 512, 64, 6, 384, False),
+    # few items: gate/up K split into 2 slices; 5 slices of 9,9,9,9,8 k-blocks;
+    # down split into 2 slices
+    (2, 1024, 16, 2, 512, True), (1, 2816, 4, 2, 128, False), (3, 1280, 8, 2, 640, True),
+    (1, 512, 4, 2, 1024, True)])
 def test_shape_fuzz(moe, path, T, H, E, K, I, norm):
     cfg = mi.MoEConfig("fuzz", T, H, E, K, I, norm, seed=T + H + E)
     run_case(cfg)
@@ -181,6 +185,25 @@ def test_deterministic(moe):
     for u, v in zip(a, b):
         assert torch.equal(u, v)
     assert moe.moe_device_status() == 0
+
+
+def test_decode_repeatable_with_dirty_workspace(moe):
+    # One decode token splits the expert GEMMs along K (arrival counters in the
+    # workspace); a caller workspace full of 0xFF bytes and repeated calls must
+    # give the same bits as a fresh forward.
+    cfg = mi.CONFIGS["decode_t1"]
+    inp = mi.make_inputs(cfg, "cuda")
+    ref = [t.clone() for t in moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
+                                              inp["W_up"], inp["W_down"], cfg.K, cfg.norm)]
+    nbytes = moe.moe_workspace_bytes(cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)
+    ws = torch.full((nbytes,), 255, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        got = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"],
+                              inp["W_down"], cfg.K, cfg.norm, workspace=ws)
+        torch.cuda.synchronize()
+        for u, v in zip(ref, got):
+            assert torch.equal(u, v)
+    assert moe.moe_device_status(ws, (cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)) == 0
 
 
 def test_forward_ws_and_host_agree(moe):
