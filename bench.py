@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--quiet-clocks", action="store_true", help="skip nvidia-smi sampling")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the forward captured as a CUDA graph (decode serving)")
+    ap.add_argument("--weights", default="packed", choices=["packed", "row-major"],
+                    help="expert weights packed once into the tile-major layout before timing "
+                         "(moe_pack_experts, a model-load step), or read row-major")
     ap.add_argument("--expert-path", default="auto", choices=["auto", "streaming", "tcgen05", "tcgen05_wt"],
                     help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args()
@@ -316,9 +319,24 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
     moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3}[args.expert_path])
 
+    packed = None
+    if args.weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
+        # one-time weight layout transform (model load), outside every timed region
+        packed = moe.moe_pack_experts(inp["W_gate"], inp["W_up"], inp["W_down"])
+        torch.cuda.synchronize()
+
+    def forward(workspace=None):
+        if packed is not None:
+            moe.moe_forward_packed(inp["x"], inp["W_router"], packed, K, cfg.norm, out=out,
+                                   router_logits=logits, topk_idx=idx, topk_w=w, aux=aux,
+                                   workspace=workspace)
+        else:
+            moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                            K, cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w,
+                            aux=aux, workspace=workspace)
+
     def eager():
-        moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], K,
-                        cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w, aux=aux)
+        forward()
 
     eager()
     torch.cuda.synchronize()
@@ -333,9 +351,7 @@ def run_ours(args, world, rank, local):
         ws = torch.empty(moe.moe_workspace_bytes(T, H, E, K, I), dtype=torch.uint8, device=dev)
 
         def fwd_ws():
-            moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
-                            K, cfg.norm, out=out, router_logits=logits, topk_idx=idx, topk_w=w,
-                            aux=aux, workspace=ws)
+            forward(ws)
 
         fwd_ws()
         torch.cuda.synchronize()
@@ -433,7 +449,7 @@ def run_ours(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev)
+        e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -449,7 +465,10 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(config_block(cfg, world),
-                           launch="CUDA graph replay" if args.graph else "eager launches"),
+                           launch="CUDA graph replay" if args.graph else "eager launches",
+                           expert_weights=("packed once into the tile-major layout before timing "
+                                           "(moe_pack_experts, a model-load step)"
+                                           if packed is not None else "row-major")),
             "roofline": roof, "block_roofline": block,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
@@ -472,7 +491,7 @@ def expert_path_name(flag, cfg):
     return flag
 
 
-def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev):
+def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed):
     T, H, E, K = cfg.T, cfg.H, cfg.E, cfg.K
     x_h = inp["x"].cpu().pin_memory()
     out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
@@ -480,8 +499,12 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev):
     aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
 
     def call():
-        moe.moe_forward_host(x_h, inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], K,
-                             cfg.norm, out_h, router_logits_host=lg_h, aux_host=aux_h)
+        if packed is not None:
+            moe.moe_forward_host_packed(x_h, inp["W_router"], packed, K, cfg.norm, out_h,
+                                        router_logits_host=lg_h, aux_host=aux_h)
+        else:
+            moe.moe_forward_host(x_h, inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                                 K, cfg.norm, out_h, router_logits_host=lg_h, aux_host=aux_h)
 
     for _ in range(max(3, args.warmup)):
         call()
@@ -497,7 +520,8 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev):
     mean = max_over_ranks(mean, world, dev)
     return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
             "d2h_bytes_per_step": T * H * 2 + T * E * 4 + 4, "ms_per_step": mean * 1e3,
-            "api": "moe_forward_host (pinned host x in; out, router_logits, aux out)"}
+            "api": ("moe_forward_host_packed" if packed is not None else "moe_forward_host")
+                   + " (pinned host x in; out, router_logits, aux out)"}
 
 
 def main():

@@ -140,14 +140,61 @@ int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_rou
                      float* router_logits_host, int32_t* topk_idx_host, float* topk_w_host,
                      float* aux_host, void* stream);
 
+/* ---- packed expert weights ------------------------------------------------
+ * No counterpart on the pages: a one-time layout transform of the expert
+ * weights (done when a model is loaded) that lets the expert GEMMs stream them
+ * as contiguous 16 KB blocks instead of 128 row pieces per tile.  Every
+ * 128-row x 64-column block of each expert's W_gate [I,H], W_up [I,H] and
+ * W_down [H,I] becomes one contiguous 16 KB block holding element (r, k) at
+ * byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2; blocks are ordered (expert,
+ * row block, column block); the buffer holds W_gate's blocks, then W_up's,
+ * then W_down's (3*E*I*H*2 bytes).  The forward computes exactly the same
+ * products in the same order as with row-major weights, so its results are
+ * bitwise identical to moe_forward's. */
+
+/* Bytes of the packed weights for (H, E, I), or 0 when the shape cannot be
+ * packed (packing needs I % 128 == 0 and H % 256 == 0, 1 <= E <= 256). */
+size_t moe_packed_experts_bytes(int H, int E, int I);
+
+/* Packs W_gate, W_up [E,I,H] and W_down [E,H,I] (row-major, device) into
+ * `packed` (device, moe_packed_experts_bytes(H,E,I) bytes, 16-byte aligned,
+ * owned by the caller) on `stream`.  MOE_ERR_INVALID_ARG for a shape that
+ * cannot be packed or a NULL pointer; MOE_ERR_ALIGNMENT for a misaligned
+ * pointer.  The row-major weights are not modified and are not needed by
+ * moe_forward_packed. */
+int moe_pack_experts(const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                     int H, int E, int I, void* packed, void* stream);
+
+/* moe_forward with packed expert weights (from moe_pack_experts with the same
+ * H, E, I).  workspace == NULL uses the library-owned workspace of `stream`
+ * (as moe_forward); otherwise it is the caller's scratch of at least
+ * moe_workspace_bytes(T,H,E,K,I) bytes, 256-byte aligned (as moe_forward_ws).
+ * MOE_ERR_INVALID_ARG for a shape that cannot be packed.  With packed
+ * weights the expert MLPs always run on the tensor cores (the
+ * MOE_PATH_STREAMING setting selects the weights-as-M kernels instead). */
+int moe_forward_packed(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                       const void* packed_experts, int E, int K, int I, int norm_topk_prob,
+                       moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
+                       float* aux, void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_forward_host with packed expert weights. */
+int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                            const void* packed_experts, int E, int K, int I,
+                            int norm_topk_prob, moe_bf16* out_host, float* router_logits_host,
+                            int32_t* topk_idx_host, float* topk_w_host, float* aux_host,
+                            void* stream);
+
 /* Per-expert pair counts ("expert utilisation histogram") of the last
- * moe_forward / moe_forward_host on `stream`, copied into counts_host[E]
+ * forward on `stream` that used the library-owned workspace (moe_forward,
+ * moe_forward_host, moe_forward_host_packed, moe_forward_packed without a
+ * workspace), copied into counts_host[E]
  * (waits for the stream).  MOE_ERR_INVALID_ARG if there was no such call. */
 int moe_last_expert_counts(int32_t* counts_host, int E, void* stream);
 
 /* Device-side status of the last forward that used `workspace` (the
- * caller's workspace of moe_forward_ws, with the sizes of that call), or, with
- * workspace == NULL, of the last moe_forward / moe_forward_host on `stream`.
+ * caller's workspace of moe_forward_ws or moe_forward_packed, with the sizes
+ * of that call), or, with workspace == NULL, of the last forward on `stream`
+ * that used the library-owned workspace.
  * Waits for the stream.  Returns MOE_OK, or MOE_ERR_TIMEOUT if a bounded
  * device-side wait of that forward gave up (its outputs are then invalid). */
 int moe_device_status(const void* workspace, int T, int H, int E, int K, int I, void* stream);

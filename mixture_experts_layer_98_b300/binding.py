@@ -24,6 +24,8 @@ MOE_PATH_TCGEN05 = 2
 MOE_PATH_TCGEN05_WT = 3
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
+           "moe_packed_experts_bytes", "moe_pack_experts", "moe_forward_packed",
+           "moe_forward_host_packed",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
            "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
            "moe_stage_times",
@@ -59,6 +61,12 @@ def lib():
         L.moe_forward_ws.argtypes = fwd + [P, sz, P]
         L.moe_forward_host.argtypes = fwd + [P]
         L.moe_forward_noalloc.argtypes = fwd + [P]
+        L.moe_packed_experts_bytes.argtypes = [i, i, i]
+        L.moe_packed_experts_bytes.restype = sz
+        L.moe_pack_experts.argtypes = [P, P, P, i, i, i, P, P]
+        pfwd = [P, i, i, P, P, i, i, i, i, P, P, P, P, P]
+        L.moe_forward_packed.argtypes = pfwd + [P, sz, P]
+        L.moe_forward_host_packed.argtypes = pfwd + [P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
         L.moe_last_expert_counts.argtypes = [P, i, P]
@@ -123,7 +131,21 @@ def moe_forward(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, out=None,
     topk_idx, topk_w and aux always are, unless passed as False to skip them).
     Returns (out, router_logits, topk_idx, topk_w, aux)."""
     T, H, E, I = _shapes(x, W_router, W_gate, W_up, W_down)
-    dev = x.device
+    out, router_logits, topk_idx, topk_w, aux = _outputs(T, H, E, K, x.device, out, router_logits,
+                                                         topk_idx, topk_w, aux)
+    args = [_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up), _ptr(W_down), E, K, I,
+            int(bool(norm_topk_prob)), _ptr(out), _ptr(router_logits), _ptr(topk_idx),
+            _ptr(topk_w), _ptr(aux)]
+    if workspace is None:
+        _call(lib().moe_forward(*args, _stream(stream)), "moe_forward")
+    else:
+        _dev(workspace, torch.uint8, "workspace")
+        _call(lib().moe_forward_ws(*args, _ptr(workspace), workspace.numel(), _stream(stream)),
+              "moe_forward_ws")
+    return out, router_logits, topk_idx, topk_w, aux
+
+
+def _outputs(T, H, E, K, dev, out, router_logits, topk_idx, topk_w, aux):
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     if router_logits is None:
@@ -143,16 +165,77 @@ def moe_forward(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, out=None,
     _dev(topk_idx, torch.int32, "topk_idx", (T, K))
     _dev(topk_w, torch.float32, "topk_w", (T, K))
     _dev(aux, torch.float32, "aux", (1,))
-    args = [_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up), _ptr(W_down), E, K, I,
-            int(bool(norm_topk_prob)), _ptr(out), _ptr(router_logits), _ptr(topk_idx),
-            _ptr(topk_w), _ptr(aux)]
-    if workspace is None:
-        _call(lib().moe_forward(*args, _stream(stream)), "moe_forward")
-    else:
-        _dev(workspace, torch.uint8, "workspace")
-        _call(lib().moe_forward_ws(*args, _ptr(workspace), workspace.numel(), _stream(stream)),
-              "moe_forward_ws")
     return out, router_logits, topk_idx, topk_w, aux
+
+
+class PackedExperts:
+    """Expert weights in the packed tile-major layout of moe_pack_experts:
+    `data` is the uint8 CUDA buffer, E, H, I the layer's sizes."""
+
+    def __init__(self, data, E, H, I):
+        self.data, self.E, self.H, self.I = data, E, H, I
+
+
+def moe_packed_experts_bytes(H, E, I):
+    return int(lib().moe_packed_experts_bytes(H, E, I))
+
+
+def moe_pack_experts(W_gate, W_up, W_down, stream=None):
+    """Packs the row-major expert weights once (a model-load step); returns a
+    PackedExperts for moe_forward_packed / moe_forward_host_packed."""
+    E, I, H = W_gate.shape
+    _dev(W_gate, torch.bfloat16, "W_gate", (E, I, H))
+    _dev(W_up, torch.bfloat16, "W_up", (E, I, H))
+    _dev(W_down, torch.bfloat16, "W_down", (E, H, I))
+    n = moe_packed_experts_bytes(H, E, I)
+    if n == 0:
+        raise ValueError(f"expert weights with H={H}, I={I} cannot be packed "
+                         "(needs I % 128 == 0 and H % 256 == 0)")
+    data = torch.empty(n, dtype=torch.uint8, device=W_gate.device)
+    _call(lib().moe_pack_experts(_ptr(W_gate), _ptr(W_up), _ptr(W_down), H, E, I, _ptr(data),
+                                 _stream(stream)), "moe_pack_experts")
+    return PackedExperts(data, E, H, I)
+
+
+def moe_forward_packed(x, W_router, packed, K, norm_topk_prob, out=None, router_logits=None,
+                       topk_idx=None, topk_w=None, aux=None, stream=None, workspace=None):
+    """moe_forward with PackedExperts weights; `workspace` as for moe_forward."""
+    T, H = x.shape
+    E, I = packed.E, packed.I
+    if packed.H != H:
+        raise ValueError("x and the packed weights disagree on H")
+    _dev(x, torch.bfloat16, "x")
+    _dev(W_router, torch.bfloat16, "W_router", (E, H))
+    out, router_logits, topk_idx, topk_w, aux = _outputs(T, H, E, K, x.device, out, router_logits,
+                                                         topk_idx, topk_w, aux)
+    if workspace is not None:
+        _dev(workspace, torch.uint8, "workspace")
+    _call(lib().moe_forward_packed(_ptr(x), T, H, _ptr(W_router), _ptr(packed.data), E, K, I,
+                                   int(bool(norm_topk_prob)), _ptr(out), _ptr(router_logits),
+                                   _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(workspace),
+                                   0 if workspace is None else workspace.numel(),
+                                   _stream(stream)), "moe_forward_packed")
+    return out, router_logits, topk_idx, topk_w, aux
+
+
+def moe_forward_host_packed(x_host, W_router, packed, K, norm_topk_prob, out_host,
+                            router_logits_host=None, topk_idx_host=None, topk_w_host=None,
+                            aux_host=None, stream=None):
+    """moe_forward_host with PackedExperts weights."""
+    T, H = x_host.shape
+    _dev(W_router, torch.bfloat16, "W_router", (packed.E, H))
+    for n, t in (("x_host", x_host), ("out_host", out_host), ("router_logits_host",
+                                                            router_logits_host),
+                 ("topk_idx_host", topk_idx_host), ("topk_w_host", topk_w_host),
+                 ("aux_host", aux_host)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    _call(lib().moe_forward_host_packed(_ptr(x_host), T, H, _ptr(W_router), _ptr(packed.data),
+                                        packed.E, K, packed.I, int(bool(norm_topk_prob)),
+                                        _ptr(out_host), _ptr(router_logits_host),
+                                        _ptr(topk_idx_host), _ptr(topk_w_host), _ptr(aux_host),
+                                        _stream(stream)), "moe_forward_host_packed")
+    return out_host
 
 
 def moe_workspace_bytes(T, H, E, K, I):

@@ -180,10 +180,13 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
 
 }  // namespace
 
-cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16* Wg,
-                                     const __nv_bfloat16* Wu, const __nv_bfloat16* Wd,
+cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const ExpertWeights& W,
                                      const Sizes& s, const Workspace& ws, cudaStream_t st,
                                      cudaEvent_t ev_mid) {
+    if (W.packed) return cudaErrorInvalidValue;  // reads row-major weight rows
+    const __nv_bfloat16* Wg = W.gate;
+    const __nv_bfloat16* Wu = W.up;
+    const __nv_bfloat16* Wd = W.down;
     const int sms = num_sms();
     const size_t smem_gu = (size_t)kStreamRows * s.H * 2;
     const size_t smem_dn = (size_t)kStreamRows * s.I * 2;

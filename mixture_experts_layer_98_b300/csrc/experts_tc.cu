@@ -51,6 +51,11 @@ struct TcParams {
     int out_ld;
     const float* w_perm;    // routing weight per row (down)
     int32_t* status;
+    // Packed weights (null: row-major through the B tensor maps): block bases of
+    // the two B halves and 128-row blocks per expert of the B matrix.
+    const char* bpk0;
+    const char* bpk1;
+    int b_blocks_per_expert;
 };
 
 template <int MODE, int BN>
@@ -120,12 +125,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
                 const RowTile tl = p.tiles[item / p.n_nt];
                 const int nt = item % p.n_nt;
-                int b0, b1;
+                int b0, b1;    // B rows in the row-major matrices
+                int b0h, b1h;  // the halves' 128-row blocks within the expert (packed)
                 if (MODE == kGateUp) {
                     b0 = b1 = tl.expert * p.b_rows_per_expert + nt * (BN / 2);
+                    b0h = b1h = nt;
                 } else {
                     b0 = tl.expert * p.b_rows_per_expert + nt * BN;
                     b1 = b0 + BN / 2;
+                    b0h = 2 * nt;
+                    b1h = 2 * nt + 1;
                 }
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_s,
@@ -137,8 +146,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sB = sA + C::kABytes;
                     ptx::mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
                     ptx::tma_load_2d(sA, &tmA, &full_bar[stage], kb * kBK, tl.row0);
-                    ptx::tma_load_2d(sB, &tmB0, &full_bar[stage], kb * kBK, b0);
-                    ptx::tma_load_2d(sB + C::kBHalfBytes, &tmB1, &full_bar[stage], kb * kBK, b1);
+                    if (BN == 2 * kPackRows && p.bpk0) {
+                        // packed: each B half is one contiguous 16 KB block
+                        const size_t blk0 =
+                            ((size_t)tl.expert * p.b_blocks_per_expert + (size_t)b0h) * p.num_kb + kb;
+                        const size_t blk1 =
+                            ((size_t)tl.expert * p.b_blocks_per_expert + (size_t)b1h) * p.num_kb + kb;
+                        ptx::bulk_load(sB, p.bpk0 + blk0 * kPackBlockBytes, C::kBHalfBytes,
+                                       &full_bar[stage]);
+                        ptx::bulk_load(sB + C::kBHalfBytes, p.bpk1 + blk1 * kPackBlockBytes,
+                                       C::kBHalfBytes, &full_bar[stage]);
+                    } else {
+                        ptx::tma_load_2d(sB, &tmB0, &full_bar[stage], kb * kBK, b0);
+                        ptx::tma_load_2d(sB + C::kBHalfBytes, &tmB1, &full_bar[stage], kb * kBK,
+                                         b1);
+                    }
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -302,10 +324,14 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
                       cudaStream_t st) {
     using C = TcCfg<MODE, BN>;
     CUtensorMap ma, mb0, mb1;
-    if (!make_tma_2d(&ma, A, a_rows, a_cols, kBM) ||
-        !make_tma_2d(&mb0, B0, b_rows, a_cols, BN / 2) ||
-        !make_tma_2d(&mb1, B1, b_rows, a_cols, BN / 2))
+    if (!make_tma_2d(&ma, A, a_rows, a_cols, kBM)) return cudaErrorInvalidValue;
+    if (p.bpk0) {  // packed weights: the B maps are not used
+        mb0 = ma;
+        mb1 = ma;
+    } else if (!make_tma_2d(&mb0, B0, b_rows, a_cols, BN / 2) ||
+               !make_tma_2d(&mb1, B1, b_rows, a_cols, BN / 2)) {
         return cudaErrorInvalidValue;
+    }
     cudaError_t err = ensure_smem((const void*)grouped_gemm_tc_kernel<MODE, BN>, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     long long grid = num_sms();
@@ -319,11 +345,12 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
 
 }  // namespace
 
-cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                   const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
+cudaError_t launch_experts_tcgen05(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                                    cudaStream_t st, cudaEvent_t ev_mid) {
     const long long P = s.P();
     const long long max_tiles = s.max_tiles(kBM);
+    const bool packed = W.packed != nullptr;
+    if (packed && !packed_supported(s.H, s.E, s.I)) return cudaErrorInvalidValue;
     TcParams p{};
     p.tiles = ws.tiles;
     p.n_tiles = ws.n_tiles;
@@ -335,14 +362,17 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
     p.b_rows_per_expert = s.I;
     p.out = ws.hbuf;
     p.out_ld = s.I;
+    p.bpk0 = packed ? W.packed_gate(s) : nullptr;
+    p.bpk1 = packed ? W.packed_up(s) : nullptr;
+    p.b_blocks_per_expert = s.I / kPackRows;
     cudaError_t err;
     if (s.I % 128 == 0) {
         p.n_nt = s.I / 128;
-        err = launch_tc<kGateUp, 256>(ws.x_perm, P, s.H, Wg, Wu, (uint64_t)s.E * s.I, p,
+        err = launch_tc<kGateUp, 256>(ws.x_perm, P, s.H, W.gate, W.up, (uint64_t)s.E * s.I, p,
                                       max_tiles * p.n_nt, st);
     } else {
         p.n_nt = s.I / 64;
-        err = launch_tc<kGateUp, 128>(ws.x_perm, P, s.H, Wg, Wu, (uint64_t)s.E * s.I, p,
+        err = launch_tc<kGateUp, 128>(ws.x_perm, P, s.H, W.gate, W.up, (uint64_t)s.E * s.I, p,
                                       max_tiles * p.n_nt, st);
     }
     if (err != cudaSuccess) return err;
@@ -353,17 +383,20 @@ cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16*
     p.b_rows_per_expert = s.H;
     p.out = ws.ybuf;
     p.out_ld = s.H;
+    p.bpk0 = packed ? W.packed_down(s) : nullptr;
+    p.bpk1 = p.bpk0;
+    p.b_blocks_per_expert = s.H / kPackRows;
     if (s.H % 256 == 0) {
         p.n_nt = s.H / 256;
-        err = launch_tc<kDown, 256>(ws.hbuf, P, s.I, Wd, Wd, (uint64_t)s.E * s.H, p,
+        err = launch_tc<kDown, 256>(ws.hbuf, P, s.I, W.down, W.down, (uint64_t)s.E * s.H, p,
                                     max_tiles * p.n_nt, st);
     } else if (s.H % 128 == 0) {
         p.n_nt = s.H / 128;
-        err = launch_tc<kDown, 128>(ws.hbuf, P, s.I, Wd, Wd, (uint64_t)s.E * s.H, p,
+        err = launch_tc<kDown, 128>(ws.hbuf, P, s.I, W.down, W.down, (uint64_t)s.E * s.H, p,
                                     max_tiles * p.n_nt, st);
     } else {
         p.n_nt = s.H / 64;
-        err = launch_tc<kDown, 64>(ws.hbuf, P, s.I, Wd, Wd, (uint64_t)s.E * s.H, p,
+        err = launch_tc<kDown, 64>(ws.hbuf, P, s.I, W.down, W.down, (uint64_t)s.E * s.H, p,
                                    max_tiles * p.n_nt, st);
     }
     return err;

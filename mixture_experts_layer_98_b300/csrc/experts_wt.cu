@@ -80,6 +80,11 @@ struct WtParams {
     int out_ld;
     const float* w_perm;    // routing weight per row (down)
     int32_t* status;
+    // Packed weights (null: row-major through the A tensor maps): block bases of
+    // A0 and A1 and 128-row blocks per expert of the weight matrix.
+    const char* apk0;
+    const char* apk1;
+    int a_blocks_per_expert;
 };
 
 // Epilogue of one output row and weight row i of the block: gate/up writes
@@ -156,12 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int blk = pitem % p.n_blk;
                 const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
                 const int nbox = (tl.nrows + kBox - 1) / kBox;
-                int a0, a1;
+                int a0, a1;    // weight rows in the row-major matrices
+                int a0b, a1b;  // the same as 128-row blocks within the expert (packed)
                 if (MODE == kGateUp) {
                     a0 = a1 = tl.expert * p.w_rows_per_expert + blk * kWM;
+                    a0b = a1b = blk;
                 } else {
                     a0 = tl.expert * p.w_rows_per_expert + blk * (2 * kWM);
                     a1 = a0 + kWM;
+                    a0b = 2 * blk;
+                    a1b = 2 * blk + 1;
                 }
                 const uint32_t bytes = 2 * kABytes + nbox * kBoxBytes;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -173,8 +182,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sA = smem + stage * kStageBytes;
                     uint8_t* sB = sA + 2 * kABytes;
                     ptx::mbar_arrive_expect_tx(&full_bar[stage], bytes);
-                    ptx::tma_load_2d(sA, &tmA0, &full_bar[stage], kb * kBK, a0);
-                    ptx::tma_load_2d(sA + kABytes, &tmA1, &full_bar[stage], kb * kBK, a1);
+                    if (p.apk0) {  // packed: each weight tile is one contiguous 16 KB block
+                        const size_t e0 = (size_t)tl.expert * p.a_blocks_per_expert;
+                        ptx::bulk_load(sA, p.apk0 + ((e0 + a0b) * p.num_kb + kb) * kPackBlockBytes,
+                                       kABytes, &full_bar[stage]);
+                        ptx::bulk_load(sA + kABytes,
+                                       p.apk1 + ((e0 + a1b) * p.num_kb + kb) * kPackBlockBytes,
+                                       kABytes, &full_bar[stage]);
+                    } else {
+                        ptx::tma_load_2d(sA, &tmA0, &full_bar[stage], kb * kBK, a0);
+                        ptx::tma_load_2d(sA + kABytes, &tmA1, &full_bar[stage], kb * kBK, a1);
+                    }
                     for (int b = 0; b < nbox; ++b)
                         ptx::tma_load_2d(sB + b * kBoxBytes, &tmB, &full_bar[stage], kb * kBK,
                                          tl.row0 + b * kBox);
@@ -356,10 +374,14 @@ cudaError_t launch_wt(const void* A0, const void* A1, uint64_t a_rows, uint64_t 
                       const void* B, uint64_t b_rows, const WtParams& p, long long max_items,
                       cudaStream_t st) {
     CUtensorMap ma0, ma1, mb;
-    if (!make_tma_2d(&ma0, A0, a_rows, k_cols, kWM) ||
-        !make_tma_2d(&ma1, A1, a_rows, k_cols, kWM) ||
-        !make_tma_2d(&mb, B, b_rows, k_cols, kBox))
+    if (!make_tma_2d(&mb, B, b_rows, k_cols, kBox)) return cudaErrorInvalidValue;
+    if (p.apk0) {  // packed weights: the A maps are not used
+        ma0 = mb;
+        ma1 = mb;
+    } else if (!make_tma_2d(&ma0, A0, a_rows, k_cols, kWM) ||
+               !make_tma_2d(&ma1, A1, a_rows, k_cols, kWM)) {
         return cudaErrorInvalidValue;
+    }
     cudaError_t err = ensure_smem((const void*)expert_wt_tc_kernel<MODE>, kSmemBytes);
     if (err != cudaSuccess) return err;
     long long grid = num_sms();
@@ -435,10 +457,10 @@ WtPlan wt_plan(const Sizes& s) {
     return pl;
 }
 
-cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                              const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
+cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid) {
     if (!experts_wt_supported(s)) return cudaErrorInvalidValue;
+    const bool packed = W.packed != nullptr;
     const long long P = s.P();
     const WtPlan pl = wt_plan(s);
     WtParams p{};
@@ -458,7 +480,10 @@ cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
     p.w_rows_per_expert = s.I;
     p.out = ws.hbuf;
     p.out_ld = s.I;
-    cudaError_t err = launch_wt<kGateUp>(Wg, Wu, (uint64_t)s.E * s.I, s.H, ws.x_perm, P, p,
+    p.apk0 = packed ? W.packed_gate(s) : nullptr;
+    p.apk1 = packed ? W.packed_up(s) : nullptr;
+    p.a_blocks_per_expert = s.I / kPackRows;
+    cudaError_t err = launch_wt<kGateUp>(W.gate, W.up, (uint64_t)s.E * s.I, s.H, ws.x_perm, P, p,
                                          pl.items_gu * p.ksplit, st);
     if (err != cudaSuccess) return err;
     if (ev_mid) cudaEventRecord(ev_mid, st);
@@ -472,7 +497,10 @@ cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
     p.w_rows_per_expert = s.H;
     p.out = ws.ybuf;
     p.out_ld = s.H;
-    return launch_wt<kDown>(Wd, Wd, (uint64_t)s.E * s.H, s.I, ws.hbuf, P, p,
+    p.apk0 = packed ? W.packed_down(s) : nullptr;
+    p.apk1 = p.apk0;
+    p.a_blocks_per_expert = s.H / kPackRows;
+    return launch_wt<kDown>(W.down, W.down, (uint64_t)s.E * s.H, s.I, ws.hbuf, P, p,
                             pl.items_dn * p.ksplit, st);
 }
 

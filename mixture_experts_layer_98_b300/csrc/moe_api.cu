@@ -202,31 +202,32 @@ static void remember_counts(cudaStream_t st, const Workspace& ws, int E) {
 
 enum class ExpertPath { kStreaming, kTokensM, kWeightsM };
 
-static ExpertPath expert_path(const Sizes& s) {
+static ExpertPath expert_path(const Sizes& s, bool packed) {
     const bool wt_ok = experts_wt_supported(s);
-    const ExpertPath tokens_m = ExpertPath::kTokensM;
+    // Packed weights exist only for shapes both tensor-core paths tile; the
+    // streaming kernels read row-major rows, so packed forwards never use them.
+    const ExpertPath small = (wt_ok || packed) ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
     switch (g_expert_path) {
-        case MOE_PATH_STREAMING: return ExpertPath::kStreaming;
-        case MOE_PATH_TCGEN05: return tokens_m;
-        case MOE_PATH_TCGEN05_WT: return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
+        case MOE_PATH_STREAMING: return packed ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
+        case MOE_PATH_TCGEN05: return ExpertPath::kTokensM;
+        case MOE_PATH_TCGEN05_WT: return small;
         default: break;
     }
     // Token rows fill 128-row tiles from ~32 rows per expert on average up;
     // below that the weights go on the MMA's M side (every stage is weights).
-    if (s.P() >= 32LL * s.E) return tokens_m;
-    return wt_ok ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
+    if (s.P() >= 32LL * s.E) return ExpertPath::kTokensM;
+    return small;
 }
 
 // The kernel sequence.  All pointers checked by the caller.
-int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
-                       const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Sizes& s, int norm,
-                       __nv_bfloat16* out, float* logits, int32_t* idx, float* w, float* aux,
-                       const Workspace& ws, cudaStream_t st) {
+int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
+                const Sizes& s, int norm, __nv_bfloat16* out, float* logits, int32_t* idx,
+                float* w, float* aux, const Workspace& ws, cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
     begin_marks();
     mark(0, st);
-    const ExpertPath path = expert_path(s);
+    const ExpertPath path = expert_path(s, W.packed != nullptr);
     const int tile_rows = path == ExpertPath::kTokensM   ? kTcRows
                           : path == ExpertPath::kWeightsM ? kWtRows
                                                           : kStreamRows;
@@ -266,9 +267,9 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bflo
     mark(2, st);
     cudaEvent_t mid = t_cur_ev[3];
     switch (path) {
-        case ExpertPath::kTokensM: e = launch_experts_tcgen05(Wg, Wu, Wd, s, ws, st, mid); break;
-        case ExpertPath::kWeightsM: e = launch_experts_wt(Wg, Wu, Wd, s, ws, st, mid); break;
-        default: e = launch_experts_streaming(x, Wg, Wu, Wd, s, ws, st, mid); break;
+        case ExpertPath::kTokensM: e = launch_experts_tcgen05(W, s, ws, st, mid); break;
+        case ExpertPath::kWeightsM: e = launch_experts_wt(W, s, ws, st, mid); break;
+        default: e = launch_experts_streaming(x, W, s, ws, st, mid); break;
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
@@ -297,6 +298,99 @@ int check_forward_args(const void* x, int T, int H, const void* Wr, const void* 
 }  // namespace moe
 
 using namespace moe;
+
+// The device-pointer forward behind moe_forward, moe_forward_ws and
+// moe_forward_packed: argument checks, T = 0, workspace (library-owned when
+// workspace == NULL), kernel sequence.  wg/wu/wd are only null-checked.
+static int forward_device(const void* x, int T, int H, const void* W_router,
+                          const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
+                          int E, int K, int I, int norm, void* out, float* logits, int32_t* idx,
+                          float* w, float* aux, void* workspace, size_t workspace_bytes,
+                          cudaStream_t st) {
+    int rc = check_forward_args(x, T, H, W_router, wg, wu, wd, E, K, I, out, logits, idx, w, aux);
+    if (rc) return rc;
+    if (T == 0) {
+        if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
+        return MOE_OK;
+    }
+    Sizes s{T, H, E, K, I};
+    const size_t need = layout_workspace(s, nullptr, nullptr);
+    const bool owned = workspace == nullptr;
+    if (owned) {
+        rc = owned_workspace(st, need, &workspace);
+        if (rc) return rc;
+    } else {
+        if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_ALIGNMENT;
+    }
+    Workspace ws;
+    layout_workspace(s, (char*)workspace, &ws);
+    rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s, norm,
+                     (__nv_bfloat16*)out, logits, idx, w, aux, ws, st);
+    if (rc == MOE_OK && owned) remember_counts(st, ws, E);
+    return rc;
+}
+
+// The host-pointer forward behind moe_forward_host and moe_forward_host_packed:
+// x is copied in, the forward runs on library-owned scratch, the outputs are
+// copied back, and the call returns after the stream has finished them.
+static int forward_host(const void* x_host, int T, int H, const void* W_router,
+                        const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
+                        int E, int K, int I, int norm, void* out_host, float* logits_host,
+                        int32_t* idx_host, float* w_host, float* aux_host, cudaStream_t st) {
+    int rc = check_sizes(T, H, E, K, I);
+    if (rc) return rc;
+    if (!W_router || !wg || !wu || !wd) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x_host || !out_host)) return MOE_ERR_INVALID_ARG;
+    const void* dps[] = {W_router, wg, wu, wd};
+    for (const void* p : dps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    rc = check_device();
+    if (rc) return rc;
+    if (T == 0) {
+        if (aux_host) *aux_host = 0.f;
+        return MOE_OK;
+    }
+    Sizes s{T, H, E, K, I};
+    const size_t need = layout_workspace(s, nullptr, nullptr);
+    const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4, kb = (size_t)T * K * 4;
+    const size_t stage = align_up(xb, 256) * 2 + align_up(lb, 256) + align_up(kb, 256) * 2 + 256;
+    void* base = nullptr;
+    rc = owned_workspace(st, need + stage, &base);
+    if (rc) return rc;
+    Workspace ws;
+    layout_workspace(s, (char*)base, &ws);
+    char* p = (char*)base + need;
+    __nv_bfloat16* x_d = (__nv_bfloat16*)p;
+    p += align_up(xb, 256);
+    __nv_bfloat16* out_d = (__nv_bfloat16*)p;
+    p += align_up(xb, 256);
+    float* logits_d = (float*)p;
+    p += align_up(lb, 256);
+    int32_t* idx_d = (int32_t*)p;
+    p += align_up(kb, 256);
+    float* w_d = (float*)p;
+    p += align_up(kb, 256);
+    float* aux_d = (float*)p;
+    cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, out_d,
+                     logits_host ? logits_d : nullptr, idx_d, w_d, aux_host ? aux_d : nullptr, ws,
+                     st);
+    if (rc) return rc;
+    remember_counts(st, ws, E);
+    e = cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && logits_host)
+        e = cudaMemcpyAsync(logits_host, logits_d, lb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && idx_host)
+        e = cudaMemcpyAsync(idx_host, idx_d, kb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && w_host)
+        e = cudaMemcpyAsync(w_host, w_d, kb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && aux_host)
+        e = cudaMemcpyAsync(aux_host, aux_d, sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
 
 extern "C" {
 
@@ -370,51 +464,56 @@ int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                    int K, int I, int norm_topk_prob, moe_bf16* out, float* router_logits,
                    int32_t* topk_idx, float* topk_w, float* aux, void* workspace,
                    size_t workspace_bytes, void* stream) {
-    int rc = check_forward_args(x, T, H, W_router, W_gate, W_up, W_down, E, K, I, out,
-                                router_logits, topk_idx, topk_w, aux);
-    if (rc) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (T == 0) {
-        if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
-        return MOE_OK;
-    }
-    Sizes s{T, H, E, K, I};
-    const size_t need = layout_workspace(s, nullptr, nullptr);
-    if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_ALIGNMENT;
-    Workspace ws;
-    layout_workspace(s, (char*)workspace, &ws);
-    return run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router,
-                       (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
-                       (const __nv_bfloat16*)W_down, s, norm_topk_prob, (__nv_bfloat16*)out,
-                       router_logits, topk_idx, topk_w, aux, ws, st);
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                          (const __nv_bfloat16*)W_down, nullptr};
+    return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
+                          out, router_logits, topk_idx, topk_w, aux, workspace, workspace_bytes,
+                          (cudaStream_t)stream);
 }
 
 int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router, const moe_bf16* W_gate,
                 const moe_bf16* W_up, const moe_bf16* W_down, int E, int K, int I,
                 int norm_topk_prob, moe_bf16* out, float* router_logits, int32_t* topk_idx,
                 float* topk_w, float* aux, void* stream) {
-    int rc = check_forward_args(x, T, H, W_router, W_gate, W_up, W_down, E, K, I, out,
-                                router_logits, topk_idx, topk_w, aux);
+    const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                          (const __nv_bfloat16*)W_down, nullptr};
+    return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
+                          out, router_logits, topk_idx, topk_w, aux, nullptr, 0,
+                          (cudaStream_t)stream);
+}
+
+size_t moe_packed_experts_bytes(int H, int E, int I) {
+    if (H < 64 || H % 64 || I < 64 || I % 64 || E < 1 || E > kMaxExperts) return 0;
+    if (!packed_supported(H, E, I)) return 0;
+    return 3 * packed_matrix_bytes(H, E, I);
+}
+
+int moe_pack_experts(const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down, int H,
+                     int E, int I, void* packed, void* stream) {
+    if (!moe_packed_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+    if (!W_gate || !W_up || !W_down || !packed) return MOE_ERR_INVALID_ARG;
+    const void* ps[] = {W_gate, W_up, W_down, packed};
+    for (const void* p : ps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
     if (rc) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (T == 0) {
-        if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
-        return MOE_OK;
-    }
-    Sizes s{T, H, E, K, I};
-    const size_t need = layout_workspace(s, nullptr, nullptr);
-    void* base = nullptr;
-    rc = owned_workspace(st, need, &base);
-    if (rc) return rc;
-    Workspace ws;
-    layout_workspace(s, (char*)base, &ws);
-    rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router,
-                     (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
-                     (const __nv_bfloat16*)W_down, s, norm_topk_prob, (__nv_bfloat16*)out,
-                     router_logits, topk_idx, topk_w, aux, ws, st);
-    if (rc == MOE_OK) remember_counts(st, ws, E);
-    return rc;
+    return cuda_status(launch_pack_experts((const __nv_bfloat16*)W_gate,
+                                           (const __nv_bfloat16*)W_up,
+                                           (const __nv_bfloat16*)W_down, H, E, I,
+                                           (char*)packed, (cudaStream_t)stream));
+}
+
+int moe_forward_packed(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                       const void* packed_experts, int E, int K, int I, int norm_topk_prob,
+                       moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
+                       float* aux, void* workspace, size_t workspace_bytes, void* stream) {
+    if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+    if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
+    const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
+    return forward_device(x, T, H, W_router, W, packed_experts, packed_experts, packed_experts,
+                          E, K, I, norm_topk_prob, out, router_logits, topk_idx, topk_w, aux,
+                          workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
@@ -422,60 +521,24 @@ int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_rou
                      int K, int I, int norm_topk_prob, moe_bf16* out_host,
                      float* router_logits_host, int32_t* topk_idx_host, float* topk_w_host,
                      float* aux_host, void* stream) {
-    int rc = check_sizes(T, H, E, K, I);
-    if (rc) return rc;
-    if (!W_router || !W_gate || !W_up || !W_down) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!x_host || !out_host)) return MOE_ERR_INVALID_ARG;
-    const void* dps[] = {W_router, W_gate, W_up, W_down};
-    for (const void* p : dps)
-        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
-    rc = check_device();
-    if (rc) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (T == 0) {
-        if (aux_host) *aux_host = 0.f;
-        return MOE_OK;
-    }
-    Sizes s{T, H, E, K, I};
-    const size_t need = layout_workspace(s, nullptr, nullptr);
-    const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4, kb = (size_t)T * K * 4;
-    const size_t stage = align_up(xb, 256) * 2 + align_up(lb, 256) + align_up(kb, 256) * 2 + 256;
-    void* base = nullptr;
-    rc = owned_workspace(st, need + stage, &base);
-    if (rc) return rc;
-    Workspace ws;
-    layout_workspace(s, (char*)base, &ws);
-    char* p = (char*)base + need;
-    __nv_bfloat16* x_d = (__nv_bfloat16*)p;
-    p += align_up(xb, 256);
-    __nv_bfloat16* out_d = (__nv_bfloat16*)p;
-    p += align_up(xb, 256);
-    float* logits_d = (float*)p;
-    p += align_up(lb, 256);
-    int32_t* idx_d = (int32_t*)p;
-    p += align_up(kb, 256);
-    float* w_d = (float*)p;
-    p += align_up(kb, 256);
-    float* aux_d = (float*)p;
-    cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, (const __nv_bfloat16*)W_gate,
-                     (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, s, norm_topk_prob,
-                     out_d, router_logits_host ? logits_d : nullptr, idx_d, w_d,
-                     aux_host ? aux_d : nullptr, ws, st);
-    if (rc) return rc;
-    remember_counts(st, ws, E);
-    e = cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && router_logits_host)
-        e = cudaMemcpyAsync(router_logits_host, logits_d, lb, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && topk_idx_host)
-        e = cudaMemcpyAsync(topk_idx_host, idx_d, kb, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && topk_w_host)
-        e = cudaMemcpyAsync(topk_w_host, w_d, kb, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && aux_host)
-        e = cudaMemcpyAsync(aux_host, aux_d, sizeof(float), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    return cuda_status(e);
+    const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                          (const __nv_bfloat16*)W_down, nullptr};
+    return forward_host(x_host, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
+                        out_host, router_logits_host, topk_idx_host, topk_w_host, aux_host,
+                        (cudaStream_t)stream);
+}
+
+int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                            const void* packed_experts, int E, int K, int I, int norm_topk_prob,
+                            moe_bf16* out_host, float* router_logits_host,
+                            int32_t* topk_idx_host, float* topk_w_host, float* aux_host,
+                            void* stream) {
+    if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+    if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
+    const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
+    return forward_host(x_host, T, H, W_router, W, packed_experts, packed_experts,
+                        packed_experts, E, K, I, norm_topk_prob, out_host, router_logits_host,
+                        topk_idx_host, topk_w_host, aux_host, (cudaStream_t)stream);
 }
 
 int moe_last_expert_counts(int32_t* counts_host, int E, void* stream) {

@@ -22,6 +22,26 @@ constexpr int kTcRows = 128;         // rows per tile of the tcgen05 grouped GEM
 constexpr int kWtRows = 64;          // rows per tile of the weights-as-M tcgen05 kernels
 constexpr int kRouterMaxSplits = 4;  // slices of H the tensor-core router may split into
 
+// Packed expert weights (pack.cu): 128-row x 64-column blocks of 16 KB, each
+// in the 128-byte swizzled K-major arrangement, ordered (expert, row block,
+// column block); W_gate's blocks, then W_up's, then W_down's.
+constexpr int kPackRows = 128;
+constexpr int kPackCols = 64;
+constexpr int kPackBlockBytes = kPackRows * kPackCols * 2;
+
+struct Sizes;
+
+// The expert weights of a forward: row-major matrices, or the packed blocks.
+struct ExpertWeights {
+    const __nv_bfloat16* gate;  // [E, I, H] row-major (null when packed)
+    const __nv_bfloat16* up;    // [E, I, H]
+    const __nv_bfloat16* down;  // [E, H, I]
+    const char* packed;         // packed blocks (null when row-major)
+    const char* packed_gate(const Sizes& s) const;
+    const char* packed_up(const Sizes& s) const;
+    const char* packed_down(const Sizes& s) const;
+};
+
 // One tile of token-expert rows, all routed to one expert: rows
 // [row0, row0 + nrows) of the dispatch order.
 struct __align__(16) RowTile {
@@ -66,6 +86,21 @@ struct Sizes {
         return (P() + rows_per_tile - 1) / rows_per_tile + E;
     }
 };
+
+inline const char* ExpertWeights::packed_gate(const Sizes&) const { return packed; }
+inline const char* ExpertWeights::packed_up(const Sizes& s) const {
+    return packed + (size_t)s.E * s.I * s.H * 2;
+}
+inline const char* ExpertWeights::packed_down(const Sizes& s) const {
+    return packed + (size_t)2 * s.E * s.I * s.H * 2;
+}
+
+// Packing (pack.cu): shapes with I % 128 == 0 and H % 256 == 0.
+bool packed_supported(int H, int E, int I);
+size_t packed_matrix_bytes(int H, int E, int I);
+cudaError_t launch_pack_experts(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                const __nv_bfloat16* Wd, int H, int E, int I, char* packed,
+                                cudaStream_t st);
 
 // Lays out (and, when base != nullptr, fills) the workspace; returns bytes.
 size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
@@ -113,12 +148,12 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
 // ev_mid (may be null) is recorded between the gate/up and the down launch.
 // The streaming kernels stage their input rows from x through ws.perm_tok;
 // the tcgen05 kernels read the gathered rows from ws.x_perm.
-cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const __nv_bfloat16* Wg,
-                                     const __nv_bfloat16* Wu, const __nv_bfloat16* Wd,
+// The streaming kernels need row-major weights; the tcgen05 kernels take
+// either form.
+cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const ExpertWeights& W,
                                      const Sizes& s, const Workspace& ws, cudaStream_t st,
                                      cudaEvent_t ev_mid);
-cudaError_t launch_experts_tcgen05(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                   const __nv_bfloat16* Wd, const Sizes& s,
+cudaError_t launch_experts_tcgen05(const ExpertWeights& W, const Sizes& s,
                                    const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
 // Small batches: the expert weights are the MMA's M side (128 weight rows per
 // MMA) and a tile's <= kWtRows token rows its N side; reads ws.x_perm.
@@ -134,8 +169,7 @@ struct WtPlan {
     int n_counters = 0;                     // gate/up counters, then down counters
 };
 WtPlan wt_plan(const Sizes& s);
-cudaError_t launch_experts_wt(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                              const __nv_bfloat16* Wd, const Sizes& s, const Workspace& ws,
+cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
                            __nv_bfloat16* out, cudaStream_t st);
@@ -160,10 +194,9 @@ int cuda_status(cudaError_t e);
 int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
                        const void* Wu, const void* Wd, int E, int K, int I, const void* out,
                        const void* logits, const void* idx, const void* w, const void* aux);
-int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const __nv_bfloat16* Wg,
-                const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Sizes& s, int norm,
-                __nv_bfloat16* out, float* logits, int32_t* idx, float* w, float* aux,
-                const Workspace& ws, cudaStream_t st);
+int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
+                const Sizes& s, int norm, __nv_bfloat16* out, float* logits, int32_t* idx,
+                float* w, float* aux, const Workspace& ws, cudaStream_t st);
 
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);

@@ -88,3 +88,18 @@ def test_python_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(b, "LIB_PATH", "/nonexistent/libmoe_b300.so")
     with pytest.raises(RuntimeError, match="not built"):
         b.lib()
+
+
+def test_packed_sizes_and_early_rejects(L):
+    # 3·E·I·H·2 bytes for packable shapes (I % 128 == 0, H % 256 == 0), else 0
+    assert L.moe_packed_experts_bytes(2048, 128, 768) == 3 * 128 * 768 * 2048 * 2
+    assert L.moe_packed_experts_bytes(4096, 128, 1536) == 3 * 128 * 1536 * 4096 * 2
+    assert L.moe_packed_experts_bytes(2048, 128, 320) == 0     # I % 128 != 0
+    assert L.moe_packed_experts_bytes(1152, 8, 256) == 0       # H % 256 != 0
+    assert L.moe_packed_experts_bytes(2048, 0, 768) == 0
+    assert L.moe_packed_experts_bytes(2048, 300, 768) == 0
+    z = ctypes.c_void_p(0)
+    # shape checks come before any pointer or device check
+    assert L.moe_pack_experts(z, z, z, 1152, 8, 256, z, z) == 1
+    assert L.moe_forward_packed(z, 4, 1152, z, z, 8, 2, 256, 1, z, z, z, z, z, z, 0, z) == 1
+    assert L.moe_forward_host_packed(z, 4, 1152, z, z, 8, 2, 256, 1, z, z, z, z, z, z) == 1
