@@ -3,9 +3,12 @@
 // Qwen3MoeSparseMoeBlock.forward (cnblogs page "大模型-qwen3 MoE 详细解读")
 // accumulates each expert's weighted output with index_add_ into a zeroed
 // [tokens, hidden] buffer.  Here each token instead reads its K rows of Y (the
-// weighted expert outputs in dispatch order) through inv and sums them in fp32
-// in k order, then rounds once to bf16: no zero-fill, no atomics, and the
-// result does not depend on scheduling.  16-byte loads and stores.
+// weighted expert outputs) and sums them in fp32 in k order, then rounds once
+// to bf16: no zero-fill, no atomics, and the result does not depend on
+// scheduling.  The down-projection kernels store Y token-major ([T, K, H]: the
+// pair (t, k) at row t*K + k), so a token's K rows are one contiguous read;
+// with inv != null, Y is in dispatch order and row inv[t*K + k] is read
+// instead.  16-byte loads and stores.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -24,19 +27,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* Y,
         float a[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = 0.f;
-        for (int k = 0; k < K; ++k) {
-            // plain (coherent) loads: inv and Y are written by earlier kernels of the
-            // forward, which may still have been running when this grid launched
-            const int row = inv[(size_t)t * K + k];
-            const uint4 v = Y[(size_t)row * vpr + c];
-            a[0] += bf16_lo(v.x);
-            a[1] += bf16_hi(v.x);
-            a[2] += bf16_lo(v.y);
-            a[3] += bf16_hi(v.y);
-            a[4] += bf16_lo(v.z);
-            a[5] += bf16_hi(v.z);
-            a[6] += bf16_lo(v.w);
-            a[7] += bf16_hi(v.w);
+        // plain (coherent) loads: Y (and inv) are written by earlier kernels of
+        // the forward, which may still have been running when this grid
+        // launched.  Four rows are loaded before any is added, so four loads
+        // are in flight; the sum still runs in k order.
+        for (int k0 = 0; k0 < K; k0 += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + j;
+                if (k < K) {
+                    const size_t row = inv ? (size_t)inv[(size_t)t * K + k] : (size_t)t * K + k;
+                    v[j] = Y[row * vpr + c];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (k0 + j < K) {
+                    a[0] += bf16_lo(v[j].x);
+                    a[1] += bf16_hi(v[j].x);
+                    a[2] += bf16_lo(v[j].y);
+                    a[3] += bf16_hi(v[j].y);
+                    a[4] += bf16_lo(v[j].z);
+                    a[5] += bf16_hi(v[j].z);
+                    a[6] += bf16_lo(v[j].w);
+                    a[7] += bf16_hi(v[j].w);
+                }
+            }
         }
         uint4 o;
         o.x = pack_bf16x2(a[0], a[1]);

@@ -350,6 +350,12 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
 }
 
 // x_perm[row, :] = x[perm_tok[row], :]; one warp per row, 16-byte vectors.
+// A lane loads all its vectors of the row before storing any (the stores may
+// alias the loads as far as the compiler knows, so without the batching every
+// load would wait for the previous store), keeping up to kGatherVec loads in
+// flight per lane.
+constexpr int kGatherVec = 8;
+
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
                                                           const int32_t* perm_tok,
                                                           long long P, int vec_per_row,
@@ -362,11 +368,23 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
     for (long long r = warp; r < P; r += nwarps) {
         const uint4* src = x + (size_t)perm_tok[r] * vec_per_row;
         uint4* dst = x_perm + (size_t)r * vec_per_row;
-        // x is the caller's input: whatever wrote it finished before the router
-        // (the forward's first kernel) passed its dependency wait, long before
-        // this grid launched, so it is constant for this grid's whole lifetime
-        // and the read-only path is allowed here.
-        for (int c = lane; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
+        for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kGatherVec) {
+            // x is the caller's input: whatever wrote it finished before the router
+            // (the forward's first kernel) passed its dependency wait, long before
+            // this grid launched, so it is constant for this grid's whole lifetime
+            // and the read-only path is allowed here.
+            uint4 v[kGatherVec];
+#pragma unroll
+            for (int j = 0; j < kGatherVec; ++j) {
+                const int c = c0 + j * 32 + lane;
+                if (c < vec_per_row) v[j] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int j = 0; j < kGatherVec; ++j) {
+                const int c = c0 + j * 32 + lane;
+                if (c < vec_per_row) dst[c] = v[j];
+            }
+        }
     }
 }
 

@@ -14,7 +14,8 @@
 // 16-byte loads and dotted with all the tile's rows in fp32.
 //
 //   gate/up : h[r, i]  = bf16( silu(x_r·Wg[e,i]) · (x_r·Wu[e,i]) )
-//   down    : Y[r, n]  = bf16( w_r · (h_r·Wd[e,n]) )
+//   down    : Y[t*K + k, n] = bf16( w_r · (h_r·Wd[e,n]) ) for the pair (t, k)
+//             of dispatch row r (token-major Y)
 #include "moe_common.cuh"
 
 namespace moe {
@@ -127,7 +128,8 @@ __global__ void __launch_bounds__(256) gateup_stream_kernel(
 __global__ void __launch_bounds__(256) down_stream_kernel(
     const __nv_bfloat16* hbuf, const RowTile* tiles,
     const int32_t* n_tiles_p, const __nv_bfloat16* Wd,
-    const float* w_perm, __nv_bfloat16* Y, int H, int I) {
+    const float* w_perm, const int32_t* perm_tok, const int32_t* perm_slot, int K,
+    __nv_bfloat16* Y, int H, int I) {
     extern __shared__ uint4 hs[];  // [kStreamRows][I/8]
     pdl_trigger();
     pdl_wait();
@@ -165,13 +167,15 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
         for (int m = 0; m < kStreamRows; ++m) {
             if (m < tl.nrows) {
                 const float wr = w_perm[tl.row0 + m];
+                const size_t yrow =
+                    (size_t)perm_tok[tl.row0 + m] * K + (size_t)perm_slot[tl.row0 + m];
 #pragma unroll
                 for (int r = 0; r < kRowsPerWarp; ++r) {
                     float v = acc[r][m];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                     if (lane == r)
-                        Y[(size_t)(tl.row0 + m) * H + n0 + r] = __float2bfloat16_rn(wr * v);
+                        Y[yrow * H + n0 + r] = __float2bfloat16_rn(wr * v);
                 }
             }
         }
@@ -209,7 +213,9 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const ExpertWeights
     if (ev_mid) cudaEventRecord(ev_mid, st);
     err = launch_pdl(down_stream_kernel, dim3(g_dn), dim3(256), smem_dn, st,
                      (const __nv_bfloat16*)ws.hbuf, (const RowTile*)ws.tiles,
-                     (const int32_t*)ws.n_tiles, Wd, (const float*)ws.w_perm, ws.ybuf, s.H, s.I);
+                     (const int32_t*)ws.n_tiles, Wd, (const float*)ws.w_perm,
+                     (const int32_t*)ws.perm_tok, (const int32_t*)ws.perm_slot, s.K, ws.ybuf,
+                     s.H, s.I);
     count_launches(1);
     return err;
 }

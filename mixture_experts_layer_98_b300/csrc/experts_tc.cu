@@ -13,7 +13,8 @@
 //             (the B tile stacks BN/2 gate rows over BN/2 up rows, so one MMA
 //             computes both); epilogue h = bf16(silu(D_gate) · D_up)
 //   down    : D[128, BN] = h[rows, I] · Wd[e, n-block]ᵀ
-//             epilogue Y = bf16(w_row · D)
+//             epilogue Y = bf16(w_row · D), stored token-major (row t*K + k of
+//             the pair in dispatch row r: t = perm_tok[r], k = perm_slot[r])
 //
 // Persistent, warp-specialised CTA (one per SM, 192 threads):
 //   warp 0     TMA producer: A tile 128x64 and two B half-tiles (BN/2)x64 per
@@ -56,6 +57,10 @@ struct TcParams {
     const char* bpk0;
     const char* bpk1;
     int b_blocks_per_expert;
+    // down: Y is stored token-major, row perm_tok[r] * K + perm_slot[r]
+    const int32_t* perm_tok;
+    const int32_t* perm_slot;
+    int K;
 };
 
 template <int MODE, int BN>
@@ -276,13 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const float wr = valid ? p.w_perm[row] : 0.f;
+                const size_t yrow =
+                    valid ? (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row] : 0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c, v);
                     ptx::tmem_ld_wait();
                     if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_ld +
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + yrow * p.out_ld +
                                                               (size_t)nt * BN + c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -386,6 +393,9 @@ cudaError_t launch_experts_tcgen05(const ExpertWeights& W, const Sizes& s, const
     p.bpk0 = packed ? W.packed_down(s) : nullptr;
     p.bpk1 = p.bpk0;
     p.b_blocks_per_expert = s.H / kPackRows;
+    p.perm_tok = ws.perm_tok;
+    p.perm_slot = ws.perm_slot;
+    p.K = s.K;
     if (s.H % 256 == 0) {
         p.n_nt = s.H / 256;
         err = launch_tc<kDown, 256>(ws.hbuf, P, s.I, W.down, W.down, (uint64_t)s.E * s.H, p,

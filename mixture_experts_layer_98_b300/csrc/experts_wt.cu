@@ -19,7 +19,8 @@
 //             Du[i, j] = Wu[e, i0 + i] · x_perm[row0 + j]
 //             h[row0 + j, i0 + i] = bf16(silu(Dg) · Du)
 //   down    : D0[i, j] = Wd[e, n0 + i] · h[row0 + j],  D1 likewise for n0 + 128 + i
-//             Y[row0 + j, n0 + i] = bf16(w[row0 + j] · D)
+//             Y[t*K + k, n0 + i] = bf16(w[row0 + j] · D) for the pair (t, k) of
+//             dispatch row row0 + j (token-major Y)
 //
 // One work item is (row tile, block of weight rows): 128 gate rows with the
 // same 128 up rows, or 256 down rows.  When a batch has fewer items than
@@ -85,6 +86,10 @@ struct WtParams {
     const char* apk0;
     const char* apk1;
     int a_blocks_per_expert;
+    // down: Y is stored token-major, row perm_tok[r] * K + perm_slot[r]
+    const int32_t* perm_tok;
+    const int32_t* perm_slot;
+    int K;
 };
 
 // Epilogue of one output row and weight row i of the block: gate/up writes
@@ -96,7 +101,8 @@ __device__ __forceinline__ void store_out(const WtParams& p, size_t row, int blk
         p.out[row * p.out_ld + (size_t)blk * kWM + i] = __float2bfloat16_rn(silu_f(d0) * d1);
     } else {
         const float wr = p.w_perm[row];
-        __nv_bfloat16* o = p.out + row * p.out_ld + (size_t)blk * (2 * kWM);
+        const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
+        __nv_bfloat16* o = p.out + yrow * p.out_ld + (size_t)blk * (2 * kWM);
         o[i] = __float2bfloat16_rn(wr * d0);
         o[kWM + i] = __float2bfloat16_rn(wr * d1);
     }
@@ -500,6 +506,9 @@ cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Work
     p.apk0 = packed ? W.packed_down(s) : nullptr;
     p.apk1 = p.apk0;
     p.a_blocks_per_expert = s.H / kPackRows;
+    p.perm_tok = ws.perm_tok;
+    p.perm_slot = ws.perm_slot;
+    p.K = s.K;
     return launch_wt<kDown>(W.down, W.down, (uint64_t)s.E * s.H, s.I, ws.hbuf, P, p,
                             pl.items_dn * p.ksplit, st);
 }

@@ -273,7 +273,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
-    e = launch_combine(ws.ybuf, ws.inv, s.T, s.K, s.H, out, st);
+    e = launch_combine(ws.ybuf, nullptr, s.T, s.K, s.H, out, st);  // Y is token-major
     if (e != cudaSuccess) return cuda_status(e);
     mark(5, st);
     if (g_timing) g_timed_once = true;

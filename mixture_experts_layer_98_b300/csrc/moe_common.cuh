@@ -73,7 +73,7 @@ struct Workspace {
     float* topk_w;          // [T, K] when the caller passes NULL
     __nv_bfloat16* x_perm;  // [P, H] (tcgen05 path)
     __nv_bfloat16* hbuf;    // [P, I]
-    __nv_bfloat16* ybuf;    // [P, H]
+    __nv_bfloat16* ybuf;    // [P, H] token-major: the pair (t, k) at row t*K + k
     size_t bytes;
 };
 
@@ -171,6 +171,8 @@ struct WtPlan {
 WtPlan wt_plan(const Sizes& s);
 cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
+// out[t] = sum over k of Y row t*K + k (inv == null: Y token-major, as the
+// expert kernels store it) or of Y row inv[t*K + k] (Y in dispatch order).
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
                            __nv_bfloat16* out, cudaStream_t st);
 
