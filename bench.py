@@ -52,7 +52,7 @@ STAGE_SOURCES = {
 }
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--quiet-clocks", action="store_true", help="skip nvidia-smi sampling")
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: oracle seconds per step (default: ~150 s in total)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the forward captured as a CUDA graph (decode serving)")
     ap.add_argument("--weights", default="packed", choices=["packed", "row-major"],
@@ -71,7 +73,7 @@ def parse():
                          "(moe_pack_experts, a model-load step), or read row-major")
     ap.add_argument("--expert-path", default="auto", choices=["auto", "streaming", "tcgen05", "tcgen05_wt"],
                     help="expert MLP kernels (auto picks by rows per expert)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ---- distributed ------------------------------------------------------------------
@@ -93,6 +95,18 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def aggregate_value(tokens_per_rank, world, max_ms):
+    """Whole-job tokens/s: every rank processes its own batch of tokens_per_rank
+    tokens per step (weak scaling); the slowest rank's step time bounds the job."""
+    return tokens_per_rank * world / (max_ms * 1e-3)
+
+
+def replica_seed(cfg, rank):
+    """Each replica draws its own synthetic batch (and weights) from the
+    workload's seed offset by its rank."""
+    return cfg.seed + rank
 
 
 def max_over_ranks(v, world, device):
@@ -259,7 +273,8 @@ def run_reference(args, world, rank):
     bits = {k: mi.bits(v) for k, v in inp.items()}
     import oracle
     # size one step's token sample so that warmup + steps take about 2-3 minutes
-    per_step_s = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    per_step_s = (args.ref_step_seconds if args.ref_step_seconds
+                  else max(0.5, 150.0 / max(1, args.steps + args.warmup)))
     _, n, _, threads = oracle_sample_rate(cfg, bits, per_step_s)
     for _ in range(args.warmup):
         oracle.moe_forward(bits["x"][:n], bits["W_router"], bits["W_gate"], bits["W_up"],
@@ -308,7 +323,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     cfg = mi.CONFIGS[args.config]
-    inp = mi.make_inputs(cfg, dev, seed=cfg.seed + rank)
+    inp = mi.make_inputs(cfg, dev, seed=replica_seed(cfg, rank))
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     logits = torch.empty((T, E), dtype=torch.float32, device=dev)
@@ -416,7 +431,7 @@ def run_ours(args, world, rank, local):
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     mean_ms = sum(step_ms) / len(step_ms)
     mean_ms_all = max_over_ranks(mean_ms, world, dev)
-    value = T * world / (mean_ms_all * 1e-3)
+    value = aggregate_value(T, world, mean_ms_all)
     assert moe.moe_device_status() == 0, "device-side timeout during the benchmark"
 
     pk = peaks()

@@ -225,15 +225,19 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     uint4* x_perm, int vec_per_row) {
     // ROUTE: probability rows [T][E]; otherwise [4][kMaxExperts] partial sums
     __shared__ float prob_s[kRouteDispatchTokens * kMaxExperts];
-    __shared__ int tok_s[ROUTE ? kRouteDispatchTokens * kMaxTopK : 1];  // token of each row
-    __shared__ uint32_t sel[kMaxExperts * kWords];
+    constexpr int kR = ROUTE ? kRouteDispatchTokens * kMaxTopK : 1;
+    __shared__ int tok_s[kR];    // ROUTE: token of each row
+    __shared__ int idx_s[kR];    // ROUTE: the selections and weights, kept here
+    __shared__ float w_s[kR];    //        for the dispatch (also written out)
+    constexpr int kW = ROUTE ? 1 : kWords;  // bitmap words per expert (T <= 32 * kW)
+    __shared__ uint32_t sel[kMaxExperts * kW];
     __shared__ int cnt[kMaxExperts];
     __shared__ int base_s[kMaxExperts];
     __shared__ float term_s[kMaxExperts];
     __shared__ int warp_tot[kSmallThreads / 32];
     pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < E * kWords; i += blockDim.x) sel[i] = 0u;
+    for (int i = tid; i < E * kW; i += blockDim.x) sel[i] = 0u;
     for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
     pdl_wait();
     if (ROUTE) {
@@ -252,8 +256,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
                     l[q] = -INFINITY;
                 }
             }
-            route_token<EPL>(l, E, K, norm, idx + (size_t)t * K, w + (size_t)t * K,
-                             prob_s + t * E);
+            route_token<EPL>(l, E, K, norm, idx_s + t * K, w_s + t * K, prob_s + t * E);
         }
     } else if (aux) {
         // four threads per expert add up rows j, j+4, ... of p_partial
@@ -269,13 +272,17 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
             prob_s[pj * kMaxExperts + pe] = a0 + a1;
         }
     }
-    __syncthreads();  // routing results (global idx/w written by this CTA) visible
+    __syncthreads();  // routing results visible to the CTA
     const int P = T * K;
     for (int i = tid; i < P; i += blockDim.x) {
         const int t = i / K;
-        const int e = idx[i];
+        const int e = ROUTE ? idx_s[i] : idx[i];
+        if (ROUTE) {
+            idx[i] = e;
+            w[i] = w_s[i];
+        }
         atomicAdd(&cnt[e], 1);
-        atomicOr(&sel[e * kWords + (t >> 5)], 1u << (t & 31));
+        atomicOr(&sel[e * kW + (t >> 5)], 1u << (t & 31));
     }
     __syncthreads();
     const int e = tid;
@@ -325,15 +332,15 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     }
     for (int i = tid; i < P; i += blockDim.x) {
         const int t = i / K, k = i - t * K, word = t >> 5, bit = t & 31;
-        const int ex = idx[i];
-        const uint32_t* sb = sel + ex * kWords;
+        const int ex = ROUTE ? idx_s[i] : idx[i];
+        const uint32_t* sb = sel + ex * kW;
         int rank = __popc(sb[word] & ((1u << bit) - 1u));
         for (int j = 0; j < word; ++j) rank += __popc(sb[j]);
         const int row = base_s[ex] + rank;
         perm_tok[row] = t;
         if (perm_slot) perm_slot[row] = k;
         inv[i] = row;
-        if (w_perm) w_perm[row] = w[i];
+        if (w_perm) w_perm[row] = ROUTE ? w_s[i] : w[i];
         if (ROUTE) tok_s[row] = t;
     }
     if (ROUTE && x) {
@@ -341,10 +348,24 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         // caller's input, finished before the forward's first kernel passed
         // its dependency wait, so the read-only path is allowed.
         __syncthreads();
+        // four vectors loaded before any is stored (the stores may alias the
+        // loads as far as the compiler knows)
         const int n = P * vec_per_row;
-        for (int v = tid; v < n; v += blockDim.x) {
-            const int row = v / vec_per_row, c = v - row * vec_per_row;
-            x_perm[(size_t)row * vec_per_row + c] = __ldg(x + (size_t)tok_s[row] * vec_per_row + c);
+        for (int v0 = tid; v0 < n; v0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = v0 + j * blockDim.x;
+                if (i < n) {
+                    const int row = i / vec_per_row, c = i - row * vec_per_row;
+                    v[j] = __ldg(x + (size_t)tok_s[row] * vec_per_row + c);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = v0 + j * blockDim.x;
+                if (i < n) x_perm[i] = v[j];
+            }
         }
     }
 }

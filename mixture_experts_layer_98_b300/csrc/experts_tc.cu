@@ -20,7 +20,9 @@
 //   warp 0     TMA producer: A tile 128x64 and two B half-tiles (BN/2)x64 per
 //              k-block into a 4-stage ring of 128-byte-swizzled buffers
 //   warp 1     owns TMEM (2 x BN fp32 columns: a double-buffered accumulator)
-//              and issues tcgen05.mma M=128 N=BN K=16 (4 per k-block)
+//              and issues tcgen05.mma M=128 N=BN K=16 (4 per k-block); a tile
+//              of at most 64 rows (an expert's last) loads a 64-row A box and
+//              issues M=64 MMAs, half the tensor work of a padded 128-row tile
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //              32·(w%4)..+31 = tile rows), fused activation / scaling, bf16
 //              stores of the rows that belong to the tile's expert
@@ -71,11 +73,13 @@ struct TcCfg {
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
     static constexpr uint32_t kTmemCols = 2 * BN;
     static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN);
+    static constexpr uint32_t kIdesc64 = ptx::idesc_bf16_f32(kBM / 2, BN);
 };
 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmA64,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
     using C = TcCfg<MODE, BN>;
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_s = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmA64);
         ptx::prefetch_tmap(&tmB0);
         ptx::prefetch_tmap(&tmB1);
     }
@@ -149,8 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* sA = smem + stage * C::kStageBytes;
                     uint8_t* sB = sA + C::kABytes;
-                    ptx::mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
-                    ptx::tma_load_2d(sA, &tmA, &full_bar[stage], kb * kBK, tl.row0);
+                    if (tl.nrows <= kBM / 2) {  // a 64-row tile: M=64 MMA, 64-row A box
+                        ptx::mbar_arrive_expect_tx(&full_bar[stage],
+                                                   C::kStageBytes - C::kABytes / 2);
+                        ptx::tma_load_2d(sA, &tmA64, &full_bar[stage], kb * kBK, tl.row0);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+                        ptx::tma_load_2d(sA, &tmA, &full_bar[stage], kb * kBK, tl.row0);
+                    }
                     if (BN == 2 * kPackRows && p.bpk0) {
                         // packed: each B half is one contiguous 16 KB block
                         const size_t blk0 =
@@ -192,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                const uint32_t idesc =
+                    p.tiles[item / p.n_nt].nrows <= kBM / 2 ? C::kIdesc64 : C::kIdesc;
                 if (!ptx::mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_s,
                                             kTimeoutNs)) {
                     ok = false;
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = ptx::desc_sw128_kmajor(a_addr + C::kABytes);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)  // K = 16 per MMA: +32 bytes
-                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, C::kIdesc,
+                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc,
                                       (kb | k) != 0 ? 1u : 0u);
                     ptx::mma_commit(&empty_bar[stage]);
                     if (++stage == kStages) {
@@ -248,8 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const int r = q * 32 + lane;
-            const bool valid = r < tl.nrows;
+            // M=128: tile row q*32 + lane sits in TMEM lane q*32 + lane.  M=64 (a
+            // tile of <= 64 rows): row q*16 + l sits in lane q*32 + l, l < 16.
+            const bool m64 = tl.nrows <= kBM / 2;
+            const int r = m64 ? q * 16 + lane : q * 32 + lane;
+            const bool valid = (!m64 || lane < 16) && r < tl.nrows;
             const size_t row = (size_t)tl.row0 + r;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if (MODE == kGateUp) {
@@ -330,8 +346,9 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
                       const void* B1, uint64_t b_rows, const TcParams& p, long long max_items,
                       cudaStream_t st) {
     using C = TcCfg<MODE, BN>;
-    CUtensorMap ma, mb0, mb1;
-    if (!make_tma_2d(&ma, A, a_rows, a_cols, kBM)) return cudaErrorInvalidValue;
+    CUtensorMap ma, ma64, mb0, mb1;
+    if (!make_tma_2d(&ma, A, a_rows, a_cols, kBM) || !make_tma_2d(&ma64, A, a_rows, a_cols, kBM / 2))
+        return cudaErrorInvalidValue;
     if (p.bpk0) {  // packed weights: the B maps are not used
         mb0 = ma;
         mb1 = ma;
@@ -345,7 +362,7 @@ cudaError_t launch_tc(const void* A, uint64_t a_rows, uint64_t a_cols, const voi
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     err = launch_pdl(grouped_gemm_tc_kernel<MODE, BN>, dim3((unsigned)grid), dim3(kThreads),
-                     C::kSmemBytes, st, ma, mb0, mb1, p);
+                     C::kSmemBytes, st, ma, ma64, mb0, mb1, p);
     count_launches(1);
     return err;
 }

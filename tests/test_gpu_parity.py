@@ -206,6 +206,23 @@ def test_decode_repeatable_with_dirty_workspace(moe):
     assert moe.moe_device_status(ws, (cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)) == 0
 
 
+def test_prefill_repeatable_over_many_forwards(moe):
+    # The gate/up kernel's gathered A tiles reach the tensor cores through
+    # cp.async and a proxy fence; a missing ordering would show up as rare
+    # differences between otherwise identical forwards.
+    cfg = mi.CONFIGS["prefill_h2048"]
+    inp = mi.make_inputs(cfg, "cuda")
+    ref = [t.clone() for t in moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
+                                              inp["W_up"], inp["W_down"], cfg.K, cfg.norm)]
+    out = torch.empty_like(ref[0])
+    for _ in range(12):
+        moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                        cfg.K, cfg.norm, out=out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0])
+    assert moe.moe_device_status() == 0
+
+
 def test_forward_ws_and_host_agree(moe):
     cfg = mi.MoEConfig("ws", 300, 256, 16, 4, 256, True, seed=5)
     inp = mi.make_inputs(cfg, "cuda")
