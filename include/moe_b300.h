@@ -28,8 +28,12 @@
  *    work is enqueued: a call that returns an error other than MOE_ERR_CUDA
  *    has enqueued nothing.  No C++ exception crosses this interface.
  *  - Sizes: T >= 0 tokens, H hidden size, E experts, K experts per token, I
- *    expert intermediate size.  H and I must be multiples of 64, 1 <= E <= 256,
- *    1 <= K <= min(E, 16).  T = 0 is a no-op that writes aux = 0.
+ *    expert intermediate size.  H and I must be multiples of 64 and at most
+ *    65536, 1 <= E <= 256, 1 <= K <= min(E, 16).  T = 0 is a no-op that writes
+ *    aux = 0.  Shapes the tensor-core kernels cannot tile at decode sizes
+ *    (I % 128 != 0 or H % 256 != 0 with T*K < 32*E) run on the weight-streaming
+ *    kernels, which also need H <= 12800 and I <= 12800 (MOE_ERR_INVALID_ARG
+ *    otherwise, before any work).
  *  - Only NVIDIA Blackwell datacenter GPUs of compute capability 10.3 (B300)
  *    are supported; other devices give MOE_ERR_UNSUPPORTED_DEVICE.
  *  - Results are deterministic: the same inputs give bitwise identical outputs

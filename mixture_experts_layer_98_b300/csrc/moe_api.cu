@@ -115,8 +115,7 @@ static int check_sizes(int T, int H, int E, int K, int I) {
     if (T < 0 || H < 64 || H % 64 || I < 64 || I % 64) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
     if ((long long)T * K > (1LL << 31) - 1) return MOE_ERR_INVALID_ARG;
-    if ((long long)H * 8 * 2 > 200 * 1024 || (long long)I * 8 * 2 > 200 * 1024)
-        return MOE_ERR_INVALID_ARG;  // staged rows of the streaming kernels must fit in smem
+    if (H > 65536 || I > 65536) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -225,9 +224,15 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                 float* w, float* aux, const Workspace& ws, cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
+    const ExpertPath path = expert_path(s, W.packed != nullptr);
+    // The streaming kernels stage kStreamRows rows of H (gate/up) and of I
+    // (down) in shared memory; larger layers go to the tensor-core paths.
+    if (path == ExpertPath::kStreaming &&
+        ((long long)kStreamRows * s.H * 2 > 200 * 1024 ||
+         (long long)kStreamRows * s.I * 2 > 200 * 1024))
+        return MOE_ERR_INVALID_ARG;
     begin_marks();
     mark(0, st);
-    const ExpertPath path = expert_path(s, W.packed != nullptr);
     const int tile_rows = path == ExpertPath::kTokensM   ? kTcRows
                           : path == ExpertPath::kWeightsM ? kWtRows
                                                           : kStreamRows;

@@ -55,6 +55,13 @@ CONFIGS = {
     "decode_t64": MoEConfig("decode_t64", 64, 4096, 128, 8, 1536, True),
     "skew": MoEConfig("skew", 16384, 4096, 128, 8, 1536, True, zipf=1.2,
                       note="T=16384 H=4096 E=128 K=8 I=1536, Zipf(1.2) expert popularity"),
+    # few big experts, top-2 without renormalisation (the Mixtral-style router
+    # the cnblogs page contrasts with norm_topk_prob); H and I of a 4096-wide
+    # model with 3.5x wide experts
+    "mixtral_prefill": MoEConfig("mixtral_prefill", 4096, 4096, 8, 2, 14336, False,
+                                 note="T=4096 H=4096 E=8 K=2 I=14336 norm_topk_prob=false"),
+    "mixtral_decode_t1": MoEConfig("mixtral_decode_t1", 1, 4096, 8, 2, 14336, False,
+                                   note="T=1 H=4096 E=8 K=2 I=14336 norm_topk_prob=false"),
 }
 
 

@@ -142,17 +142,31 @@ static int ranks_before(const float* l, int a, int b) {
 }
 
 /* For each token pick the K experts that come first in the ranking, in
- * ranking order; w_k = p[idx_k], divided by Σ_k p[idx_k] when norm != 0. */
-int oracle_route_from_logits(const float* logits, int T, int E, int K, int norm,
-                             int32_t* topk_idx, float* topk_w) {
+ * ranking order; w_k = p[idx_k], divided by Σ_k p[idx_k] when norm != 0.
+ *
+ * With bias != NULL: a per-expert routing bias for auxiliary-loss-free load
+ * balancing (the DeepSeek scheme named in section "第四阶段：更先进的路由方案：
+ * DeepSeek 的突破" of the sshipanoo.com page "项目 17：稀疏性的调度艺术：实现双专家
+ * MoE 路由（MoE Router）"), read as entering the selection only: the ranking key
+ * of expert e is the fp32 sum l_e + b_e, while the weights stay the
+ * probabilities p of the unbiased logits. */
+int oracle_route_biased(const float* logits, const float* bias, int T, int E, int K, int norm,
+                        int32_t* topk_idx, float* topk_w) {
     if (T < 0 || E < 1 || E > 1024 || K < 1 || K > E) return 1;
     if (T == 0) return 0;
     double* probs = (double*)malloc((size_t)T * E * sizeof(double));
-    if (!probs) return 2;
+    float* keys = (float*)malloc((size_t)T * E * sizeof(float));
+    if (!probs || !keys) {
+        free(probs);
+        free(keys);
+        return 2;
+    }
+    for (size_t i = 0; i < (size_t)T * E; ++i)
+        keys[i] = bias ? (float)(logits[i] + bias[i % (size_t)E]) : logits[i];
     oracle_softmax(logits, T, E, probs);
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
-        const float* l = logits + (size_t)t * E;
+        const float* l = keys + (size_t)t * E;
         const double* p = probs + (size_t)t * E;
         char taken[1024];
         int32_t sel[1024];
@@ -176,7 +190,13 @@ int oracle_route_from_logits(const float* logits, int T, int E, int K, int norm,
         }
     }
     free(probs);
+    free(keys);
     return 0;
+}
+
+int oracle_route_from_logits(const float* logits, int T, int E, int K, int norm,
+                             int32_t* topk_idx, float* topk_w) {
+    return oracle_route_biased(logits, NULL, T, E, K, norm, topk_idx, topk_w);
 }
 
 /* ---- step 5: dispatch (group the token-expert pairs by expert) ---------- */
@@ -302,11 +322,11 @@ double oracle_aux(const double* probs, const int32_t* counts, int T, int E, int 
  * order, when rows == NULL), into out[n_rows, H] (bf16) and, when out_f64 is
  * not NULL, out_f64[n_rows, H] (the same values before the bf16 rounding).
  * Any of logits / idx / w / aux / counts may be NULL.  Returns 0 on success. */
-int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, const uint16_t* Wg,
-                       const uint16_t* Wu, const uint16_t* Wd, int E, int K, int I, int norm,
-                       int flags, const int32_t* rows, int n_rows, uint16_t* out,
-                       double* out_f64, float* logits_out, int32_t* idx_out, float* w_out,
-                       float* aux_out, int32_t* counts_out) {
+int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
+                         const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int K,
+                         int I, int norm, int flags, const int32_t* rows, int n_rows,
+                         uint16_t* out, double* out_f64, float* logits_out, int32_t* idx_out,
+                         float* w_out, float* aux_out, int32_t* counts_out) {
     if (T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || I < 1) return 1;
     if (T == 0) {
         if (aux_out) *aux_out = 0.0f;
@@ -323,7 +343,7 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
     if (!logits || !probs || !idx || !w || !counts) rc = 2;
     if (!rc) rc = oracle_router_logits(x, T, H, Wr, E, flags, logits);
     if (!rc) rc = oracle_softmax(logits, T, E, probs);
-    if (!rc) rc = oracle_route_from_logits(logits, T, E, K, norm, idx, w);
+    if (!rc) rc = oracle_route_biased(logits, bias, T, E, K, norm, idx, w);
     if (!rc) {
         for (size_t i = 0; i < TK; ++i) counts[idx[i]] += 1;
         if (aux_out) *aux_out = (float)oracle_aux(probs, counts, T, E, K);
@@ -355,4 +375,14 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
     free(w);
     free(counts);
     return rc;
+}
+
+/* The block forward without a selection bias. */
+int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, const uint16_t* Wg,
+                       const uint16_t* Wu, const uint16_t* Wd, int E, int K, int I, int norm,
+                       int flags, const int32_t* rows, int n_rows, uint16_t* out,
+                       double* out_f64, float* logits_out, int32_t* idx_out, float* w_out,
+                       float* aux_out, int32_t* counts_out) {
+    return oracle_moe_forward_b(x, T, H, Wr, NULL, Wg, Wu, Wd, E, K, I, norm, flags, rows, n_rows,
+                                out, out_f64, logits_out, idx_out, w_out, aux_out, counts_out);
 }

@@ -33,6 +33,7 @@ class _Lib:
         lib.oracle_router_logits.argtypes = [P, i, i, P, i, i, P]
         lib.oracle_softmax.argtypes = [P, i, i, P]
         lib.oracle_route_from_logits.argtypes = [P, i, i, i, i, P, P]
+        lib.oracle_route_biased.argtypes = [P, P, i, i, i, i, P, P]
         lib.oracle_dispatch.argtypes = [P, i, i, i, P, P, P, P, P]
         lib.oracle_expert_mlp.argtypes = [P, i, P, P, P, i, i, P]
         lib.oracle_token_output.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P]
@@ -41,6 +42,8 @@ class _Lib:
         lib.oracle_aux.restype = ctypes.c_double
         lib.oracle_moe_forward.argtypes = [P, i, i, P, P, P, P, i, i, i, i, i, P, i, P, P, P,
                                            P, P, P, P]
+        lib.oracle_moe_forward_b.argtypes = [P, i, i, P, P, P, P, P, i, i, i, i, i, P, i, P, P,
+                                             P, P, P, P, P]
         self.c = lib
 
 
@@ -132,14 +135,22 @@ def softmax(logits):
     return out
 
 
-def route_from_logits(logits, K, norm):
-    """Top-k (logit desc, index asc) and weights -> (idx int32 [T,K], w float32 [T,K])."""
+def route_from_logits(logits, K, norm, bias=None):
+    """Top-k (logit desc, index asc) and weights -> (idx int32 [T,K], w float32 [T,K]).
+    With bias (float32 [E]): ranked by the fp32 key logit + bias, weighted by the
+    unbiased probabilities."""
     l = _c(logits, np.float32)
     T, E = l.shape
     idx = np.empty((T, K), np.int32)
     w = np.empty((T, K), np.float32)
-    _check(_L().oracle_route_from_logits(_p(l), T, E, K, int(bool(norm)), _p(idx), _p(w)),
-           "route")
+    if bias is None:
+        _check(_L().oracle_route_from_logits(_p(l), T, E, K, int(bool(norm)), _p(idx), _p(w)),
+               "route")
+    else:
+        b = _c(bias, np.float32)
+        assert b.shape == (E,)
+        _check(_L().oracle_route_biased(_p(l), _p(b), T, E, K, int(bool(norm)), _p(idx), _p(w)),
+               "route")
     return idx, w
 
 
@@ -193,8 +204,9 @@ def aux(probs, counts, K):
     return float(_L().oracle_aux(_p(p), _p(c), T, E, K))
 
 
-def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True):
-    """The whole block.  Returns dict(out, out_f64, logits, idx, w, aux, counts).
+def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True, bias=None):
+    """The whole block (with bias: the selection-only expert bias of
+    route_from_logits).  Returns dict(out, out_f64, logits, idx, w, aux, counts).
 
     out is bf16 bits [n_rows, H] for the listed token rows (all tokens when
     rows is None) and out_f64 the same values before the final bf16 rounding;
@@ -217,9 +229,11 @@ def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True):
     w = np.empty((T, K), np.float32)
     counts = np.empty(E, np.int32)
     a = np.zeros(1, np.float32)
-    _check(_L().oracle_moe_forward(_p(x), T, H, _p(Wr), _p(Wg), _p(Wu), _p(Wd), E, K, I,
-                                   int(bool(norm)), flags, _p(rows), n, _p(out), _p(out_f64),
-                                   _p(logits), _p(idx), _p(w), _p(a), _p(counts)), "forward")
+    b = None if bias is None else _c(bias, np.float32)
+    _check(_L().oracle_moe_forward_b(_p(x), T, H, _p(Wr), _p(b), _p(Wg), _p(Wu), _p(Wd), E, K,
+                                     I, int(bool(norm)), flags, _p(rows), n, _p(out),
+                                     _p(out_f64), _p(logits), _p(idx), _p(w), _p(a),
+                                     _p(counts)), "forward")
     return dict(out=out, out_f64=out_f64, logits=logits, idx=idx, w=w, aux=float(a[0]),
                 counts=counts)
 

@@ -58,6 +58,8 @@ def test_workspace_bytes(L):
     assert ws(16, 128, 8, 9, 256) == 0        # K > E
     assert ws(16, 128, 300, 2, 256) == 0      # E > 256
     assert ws(16, 128, 64, 17, 256) == 0      # K > 16
+    assert ws(16, 65600, 8, 2, 256) == 0      # H > 65536
+    assert ws(4096, 4096, 8, 2, 14336) > 0    # few big experts (I = 14336)
     assert ws(1, 128, 8, 2, 256) <= ws(2, 128, 8, 2, 256)
 
 

@@ -133,9 +133,18 @@ def test_shape_fuzz(moe, path, T, H, E, K, I, norm):
 
 @pytest.mark.parametrize("path", [pytest.param(0, id="auto"), pytest.param(1, id="streaming")],
                          indirect=True)
-@pytest.mark.parametrize("name", ["decode_t1", "decode_t4", "decode_t16", "decode_t64"])
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t4", "decode_t16", "decode_t64",
+                                  "mixtral_decode_t1"])
 def test_decode_sweep(moe, path, name):
-    run_case(mi.CONFIGS[name])
+    cfg = mi.CONFIGS[name]
+    if path == 1 and cfg.I * 8 * 2 > 200 * 1024:
+        # the streaming kernels stage 8 rows of I in shared memory: refused up front
+        inp = mi.make_inputs(cfg, "cuda")
+        with pytest.raises(moe.MoEError):
+            moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"],
+                            inp["W_down"], cfg.K, cfg.norm)
+        return
+    run_case(cfg)
 
 
 @pytest.mark.parametrize("path", PATHS[:1], indirect=True)
@@ -144,7 +153,7 @@ def test_prefill_h2048_sampled(moe, path):
     run_case(cfg, rows=mi.sample_rows(cfg.T, 96))
 
 
-@pytest.mark.parametrize("name", ["prefill_h4096", "skew"])
+@pytest.mark.parametrize("name", ["prefill_h4096", "skew", "mixtral_prefill"])
 def test_large_sampled(moe, name):
     cfg = mi.CONFIGS[name]
     rep = run_case(cfg, rows=mi.sample_rows(cfg.T, 48))

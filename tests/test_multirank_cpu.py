@@ -92,3 +92,54 @@ def test_whole_job_value_counts_every_rank():
     # 4096 tokens per rank, 2 ranks, slowest rank 0.5 ms per step
     assert bench.aggregate_value(4096, 2, 0.5) == pytest.approx(4096 * 2 / 0.5e-3)
     assert bench.aggregate_value(4096, 1, 0.5) == pytest.approx(4096 / 0.5e-3)
+
+
+# ---- token-sharded aux: the one exchange a sharded forward would need ----------
+
+def _shard_main(rank, world, port, outdir):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+    import torch.distributed as dist
+    import moe_inputs as mi
+    import oracle
+    dist.init_process_group("gloo")
+    try:
+        cfg = mi.MoEConfig("shard", 96, 256, 16, 4, 128, True, seed=13)
+        b = {k: mi.bits(v) for k, v in mi.make_inputs(cfg, "cpu").items()}
+        lo, hi = rank * cfg.T // world, (rank + 1) * cfg.T // world
+        logits = oracle.router_logits(b["x"][lo:hi], b["W_router"])
+        idx, _ = oracle.route_from_logits(logits, cfg.K, cfg.norm)
+        counts = np.bincount(idx.ravel(), minlength=cfg.E).astype(np.float64)
+        psum = oracle.softmax(logits).sum(axis=0)
+        # all-gather both vectors, then add them in rank order (deterministic)
+        mine = torch.from_numpy(np.concatenate([counts, psum]))
+        parts = [torch.empty_like(mine) for _ in range(world)]
+        dist.all_gather(parts, mine)
+        tot = parts[0].clone()
+        for p in parts[1:]:
+            tot += p
+        c_g, p_g = tot[:cfg.E].numpy(), tot[cfg.E:].numpy()
+        aux = cfg.E * float(np.sum((c_g / (cfg.T * cfg.K)) * (p_g / cfg.T)))
+    finally:
+        dist.destroy_process_group()
+    with open(os.path.join(outdir, f"shard{rank}.json"), "w") as f:
+        json.dump({"aux": aux}, f)
+
+
+def test_token_sharded_aux_equals_unsharded(tmp_path):
+    import numpy as np
+    import moe_inputs as mi
+    import oracle
+    oracle.build()
+    mp.spawn(_shard_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    got = [json.load(open(tmp_path / f"shard{r}.json"))["aux"] for r in range(2)]
+    cfg = mi.MoEConfig("shard", 96, 256, 16, 4, 128, True, seed=13)
+    b = {k: mi.bits(v) for k, v in mi.make_inputs(cfg, "cpu").items()}
+    logits = oracle.router_logits(b["x"], b["W_router"])
+    idx, _ = oracle.route_from_logits(logits, cfg.K, cfg.norm)
+    want = oracle.aux(oracle.softmax(logits), np.bincount(idx.ravel(), minlength=cfg.E)
+                      .astype(np.int32), cfg.K)
+    assert got[0] == got[1]
+    assert abs(got[0] - want) <= 1e-12 * max(1.0, want)

@@ -285,10 +285,70 @@ def pin_param_counts():
     assert (cfg.E, cfg.I, cfg.H) == (E, I, H)
 
 
+# ---- selection-only expert bias (auxiliary-loss-free balancing) --------------
+
+def pin_bias_zero_is_unbiased():
+    # a zero bias leaves every selection and weight unchanged
+    rng = np.random.default_rng(21)
+    l = (rng.standard_normal((50, 16)) * 2).astype(np.float32)
+    for norm in (False, True):
+        i0, w0 = oracle.route_from_logits(l, 4, norm)
+        i1, w1 = oracle.route_from_logits(l, 4, norm, bias=np.zeros(16, np.float32))
+        assert np.array_equal(i0, i1) and np.array_equal(w0, w1)
+
+
+def pin_biased_topk_bruteforce():
+    # ranking by the fp32 key logit + bias, ties to the lower index: a full
+    # stable sort of the keys (multiples of 1/4, so the sums are exact and tie)
+    rng = np.random.default_rng(22)
+    T, E, K = 60, 12, 5
+    l = (rng.integers(-8, 9, (T, E)) / 4).astype(np.float32)
+    b = (rng.integers(-4, 5, E) / 4).astype(np.float32)
+    idx, _ = oracle.route_from_logits(l, K, True, bias=b)
+    key = (l + b[None, :]).astype(np.float32)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-float(key[t, e]), e))
+        assert list(idx[t]) == order[:K], t
+
+
+def pin_biased_weights_are_unbiased_probs():
+    # the bias moves the selection only: weights are the softmax of the
+    # unbiased logits at the selected experts (renormalised over them if norm)
+    rng = np.random.default_rng(23)
+    T, E, K = 40, 16, 4
+    l = (rng.standard_normal((T, E)) * 1.5).astype(np.float32)
+    b = (rng.standard_normal(E) * 3).astype(np.float32)
+    p = scipy.special.softmax(l.astype(np.float64), axis=1)
+    for norm in (False, True):
+        idx, w = oracle.route_from_logits(l, K, norm, bias=b)
+        want = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+        if norm:
+            want = want / want.sum(axis=1, keepdims=True)
+        assert np.abs(w - want).max() <= 1e-7 * max(1.0, np.abs(want).max())
+
+
+def pin_bias_forces_selection_and_aux():
+    # a large bias on two experts makes every token pick them (in key order);
+    # aux then counts only those two, with P from the unbiased softmax
+    cfg, b = rand_case(40, 64, 8, 2, 64, seed=24, norm=False)
+    bias = np.zeros(8, np.float32)
+    bias[5], bias[2] = 1000.0, 999.0
+    r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 2, False,
+                           bias=bias)
+    assert (r["idx"] == np.array([5, 2])).all()
+    p = scipy.special.softmax(r["logits"].astype(np.float64), axis=1)
+    want = 8 * (0.5 * p[:, 5].mean() + 0.5 * p[:, 2].mean())
+    assert abs(r["aux"] - want) <= 1e-6 * max(1.0, want)
+    assert np.allclose(r["w"][:, 0], p[:, 5], rtol=1e-6) and np.allclose(r["w"][:, 1], p[:, 2],
+                                                                           rtol=1e-6)
+
+
 PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equal_logits,
         pin_weights_closed_form, pin_router_logits, pin_dispatch_bruteforce,
         pin_single_expert_is_swiglu, pin_dense_equivalence, pin_soft_router,
-        pin_token_permutation_equivariance, pin_aux, pin_param_counts]
+        pin_token_permutation_equivariance, pin_aux, pin_param_counts,
+        pin_bias_zero_is_unbiased, pin_biased_topk_bruteforce,
+        pin_biased_weights_are_unbiased_probs, pin_bias_forces_selection_and_aux]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -330,6 +390,11 @@ MUTATIONS = {
     "down_uses_unrounded_gate": ("double ai = silu(g) * u;", "double ai = silu(u) * u;"),
     "topk_by_smallest": ("    if (l[a] > l[b]) return 1;\n    if (l[a] < l[b]) return 0;",
                          "    if (l[a] < l[b]) return 1;\n    if (l[a] > l[b]) return 0;"),
+    "bias_ignored": ("keys[i] = bias ? (float)(logits[i] + bias[i % (size_t)E]) : logits[i];",
+                     "keys[i] = logits[i];"),
+    "weights_from_biased_keys": (
+        "logits[i];\n    oracle_softmax(logits, T, E, probs);",
+        "logits[i];\n    oracle_softmax(keys, T, E, probs);"),
 }
 
 
