@@ -188,6 +188,38 @@ int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16
                             int32_t* topk_idx_host, float* topk_w_host, float* aux_host,
                             void* stream);
 
+/* ---- forward with options ------------------------------------------------ */
+
+/* Optional inputs of moe_forward_opts; a zero-initialised struct (or a NULL
+ * pointer) gives moe_forward. */
+typedef struct moe_forward_options {
+    /* [E] fp32 device, or NULL.  Selection-only expert bias for
+     * auxiliary-loss-free load balancing (the DeepSeek scheme named on the
+     * sshipanoo.com page "项目 17：稀疏性的调度艺术：实现双专家 MoE 路由（MoE
+     * Router）", section "第四阶段：更先进的路由方案：DeepSeek 的突破"): experts
+     * are ranked by the fp32 key router_logits + expert_bias (ties to the lower
+     * index) while topk_w are the unbiased softmax probabilities of the kept
+     * experts (renormalised when norm_topk_prob); aux counts the biased
+     * selection.  router_logits stay unbiased.  The bias's update rule (a
+     * training-time controller) is the caller's. */
+    const float* expert_bias;
+    /* Packed expert weights from moe_pack_experts, or NULL for the row-major
+     * W_gate / W_up / W_down (then ignored when packed_experts is set). */
+    const void* packed_experts;
+    /* Caller scratch of at least moe_workspace_bytes(T,H,E,K,I) bytes,
+     * 256-byte aligned, or NULL for the library-owned workspace of `stream`. */
+    void* workspace;
+    size_t workspace_bytes;
+} moe_forward_options;
+
+/* moe_forward with the options above; every other argument as for
+ * moe_forward.  A misaligned expert_bias gives MOE_ERR_ALIGNMENT. */
+int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                     const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                     int E, int K, int I, int norm_topk_prob, moe_bf16* out,
+                     float* router_logits, int32_t* topk_idx, float* topk_w, float* aux,
+                     const moe_forward_options* opts, void* stream);
+
 /* Per-expert pair counts ("expert utilisation histogram") of the last
  * forward on `stream` that used the library-owned workspace (moe_forward,
  * moe_forward_host, moe_forward_host_packed, moe_forward_packed without a
@@ -268,9 +300,11 @@ long long moe_kernel_launch_count(void);
 
 /* Steps softmax -> top-k -> renormalise on given fp32 logits [T,E]:
  * topk_idx [T,K] int32 and topk_w [T,K] fp32, exactly as moe_forward
- * computes them from its own logits. */
+ * computes them from its own logits (expert_bias as in moe_forward_options,
+ * or NULL). */
 int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm_topk_prob,
-                              int32_t* topk_idx, float* topk_w, void* stream);
+                              const float* expert_bias, int32_t* topk_idx, float* topk_w,
+                              void* stream);
 
 /* Dispatch of given selections topk_idx [T,K] (each row holds K distinct
  * experts in [0,E)): counts [E], offsets [E+1] (exclusive prefix sum),

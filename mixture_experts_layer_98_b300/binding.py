@@ -25,7 +25,7 @@ MOE_PATH_TCGEN05_WT = 3
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_packed_experts_bytes", "moe_pack_experts", "moe_forward_packed",
-           "moe_forward_host_packed",
+           "moe_forward_host_packed", "moe_forward_opts",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
            "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
            "moe_stage_times",
@@ -33,6 +33,12 @@ EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_for
            "moe_dbg_combine"]
 MOE_NUM_STAGES = 5
 STAGE_NAMES = ["router", "dispatch", "gate_up", "down", "combine"]
+
+
+class _Options(ctypes.Structure):
+    """struct moe_forward_options."""
+    _fields_ = [("expert_bias", ctypes.c_void_p), ("packed_experts", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class MoEError(RuntimeError):
@@ -67,6 +73,7 @@ def lib():
         pfwd = [P, i, i, P, P, i, i, i, i, P, P, P, P, P]
         L.moe_forward_packed.argtypes = pfwd + [P, sz, P]
         L.moe_forward_host_packed.argtypes = pfwd + [P]
+        L.moe_forward_opts.argtypes = fwd + [ctypes.POINTER(_Options), P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
         L.moe_last_expert_counts.argtypes = [P, i, P]
@@ -80,7 +87,7 @@ def lib():
         L.moe_set_next_stage_events.argtypes = [P]
         L.moe_kernel_launch_count.argtypes = []
         L.moe_kernel_launch_count.restype = ctypes.c_longlong
-        L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P]
+        L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P, P]
         L.moe_dbg_permute.argtypes = [P, i, i, i, P, P, P, P, P, P]
         L.moe_dbg_combine.argtypes = [P, P, i, i, i, P, P]
         _lib = L
@@ -238,6 +245,33 @@ def moe_forward_host_packed(x_host, W_router, packed, K, norm_topk_prob, out_hos
     return out_host
 
 
+def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, expert_bias=None,
+                     packed=None, out=None, router_logits=None, topk_idx=None, topk_w=None,
+                     aux=None, stream=None, workspace=None):
+    """moe_forward_opts: expert_bias (fp32 [E] CUDA tensor) is the selection-only
+    expert bias; packed a PackedExperts (then W_gate / W_up / W_down may be None);
+    workspace as for moe_forward."""
+    T, H = x.shape
+    if packed is not None:
+        E, I = packed.E, packed.I
+        _dev(x, torch.bfloat16, "x")
+        _dev(W_router, torch.bfloat16, "W_router", (E, H))
+    else:
+        T, H, E, I = _shapes(x, W_router, W_gate, W_up, W_down)
+    _dev(expert_bias, torch.float32, "expert_bias", (E,))
+    if workspace is not None:
+        _dev(workspace, torch.uint8, "workspace")
+    out, router_logits, topk_idx, topk_w, aux = _outputs(T, H, E, K, x.device, out, router_logits,
+                                                         topk_idx, topk_w, aux)
+    opts = _Options(_ptr(expert_bias), None if packed is None else packed.data.data_ptr(),
+                    _ptr(workspace), 0 if workspace is None else workspace.numel())
+    _call(lib().moe_forward_opts(_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up),
+                                 _ptr(W_down), E, K, I, int(bool(norm_topk_prob)), _ptr(out),
+                                 _ptr(router_logits), _ptr(topk_idx), _ptr(topk_w), _ptr(aux),
+                                 ctypes.byref(opts), _stream(stream)), "moe_forward_opts")
+    return out, router_logits, topk_idx, topk_w, aux
+
+
 def moe_workspace_bytes(T, H, E, K, I):
     return int(lib().moe_workspace_bytes(T, H, E, K, I))
 
@@ -305,13 +339,14 @@ def moe_kernel_launch_count():
     return int(lib().moe_kernel_launch_count())
 
 
-def moe_dbg_route_from_logits(logits, K, norm_topk_prob, stream=None):
+def moe_dbg_route_from_logits(logits, K, norm_topk_prob, stream=None, expert_bias=None):
     T, E = logits.shape
     _dev(logits, torch.float32, "logits")
+    _dev(expert_bias, torch.float32, "expert_bias", (E,))
     idx = torch.empty((T, K), dtype=torch.int32, device=logits.device)
     w = torch.empty((T, K), dtype=torch.float32, device=logits.device)
     _call(lib().moe_dbg_route_from_logits(_ptr(logits), T, E, K, int(bool(norm_topk_prob)),
-                                          _ptr(idx), _ptr(w), _stream(stream)),
+                                          _ptr(expert_bias), _ptr(idx), _ptr(w), _stream(stream)),
           "moe_dbg_route_from_logits")
     return idx, w
 

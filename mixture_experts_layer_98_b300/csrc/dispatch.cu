@@ -218,8 +218,9 @@ static_assert(kRouteDispatchTokens <= kSmallThreads / 32, "one warp per routed t
 //   scatter: row = offsets[e] + tokens before t that chose e.
 template <int EPL, bool ROUTE>
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
-    const float* parts, int nparts, float* logits_out, int norm, int32_t* idx, float* w,
-    const float* p_partial, int nrouter, int T, int E, int K, int rows_per_tile,
+    const float* parts, int nparts, float* logits_out, int norm, const float* bias,
+    int32_t* idx, float* w, const float* p_partial, int nrouter, int T, int E, int K,
+    int rows_per_tile,
     int32_t* counts, int32_t* offsets, RowTile* tiles, int32_t* n_tiles, int32_t* perm_tok,
     int32_t* perm_slot, int32_t* inv, float* w_perm, float* aux, const uint4* x,
     uint4* x_perm, int vec_per_row) {
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
                     l[q] = -INFINITY;
                 }
             }
-            route_token<EPL>(l, E, K, norm, idx_s + t * K, w_s + t * K, prob_s + t * E);
+            route_token<EPL>(l, E, K, norm, bias, idx_s + t * K, w_s + t * K, prob_s + t * E);
         }
     } else if (aux) {
         // four threads per expert add up rows j, j+4, ... of p_partial
@@ -425,11 +426,12 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const Sizes& s, const Workspac
 
 template <int EPL>
 cudaError_t launch_small(const float* parts, int nparts, float* logits_out, int norm,
-                         int32_t* idx, float* w, const Sizes& s, const Workspace& ws,
-                         int rows_per_tile, float* aux, const __nv_bfloat16* x,
-                         cudaStream_t st) {
+                         const float* bias, int32_t* idx, float* w, const Sizes& s,
+                         const Workspace& ws, int rows_per_tile, float* aux,
+                         const __nv_bfloat16* x, cudaStream_t st) {
     cudaError_t e = launch_pdl(dispatch_small_kernel<EPL, true>, dim3(1), dim3(kSmallThreads), 0,
-                               st, parts, nparts, logits_out, norm, idx, w, (const float*)nullptr,
+                               st, parts, nparts, logits_out, norm, bias, idx, w,
+                               (const float*)nullptr,
                                0, s.T, s.E, s.K, rows_per_tile, ws.counts, ws.offsets, ws.tiles,
                                ws.n_tiles, ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm, aux,
                                reinterpret_cast<const uint4*>(x),
@@ -447,7 +449,8 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
     cudaError_t e;
     if (nch == 1) {
         e = launch_pdl(dispatch_small_kernel<1, false>, dim3(1), dim3(kSmallThreads), 0, st,
-                       (const float*)nullptr, 0, (float*)nullptr, 0, const_cast<int32_t*>(idx),
+                       (const float*)nullptr, 0, (float*)nullptr, 0, (const float*)nullptr,
+                       const_cast<int32_t*>(idx),
                        const_cast<float*>(w), p_partial, n_partials, s.T, s.E, s.K,
                        rows_per_tile, ws.counts, ws.offsets, ws.tiles, ws.n_tiles, ws.perm_tok,
                        ws.perm_slot, ws.inv, ws.w_perm, aux, (const uint4*)nullptr,
@@ -471,7 +474,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
 }
 
 cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* logits_out,
-                                        int norm, int32_t* idx, float* w,
+                                        int norm, const float* bias, int32_t* idx, float* w,
                                         const __nv_bfloat16* x, const Sizes& s,
                                         const Workspace& ws, int rows_per_tile, float* aux,
                                         cudaStream_t st) {
@@ -483,10 +486,10 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
     const __nv_bfloat16* xk = in_cta ? x : nullptr;
     const int epl = (s.E + 31) / 32;
     cudaError_t e;
-    if (epl <= 1) e = launch_small<1>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else if (epl <= 2) e = launch_small<2>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else if (epl <= 4) e = launch_small<4>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else e = launch_small<8>(parts, nparts, logits_out, norm, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    if (epl <= 1) e = launch_small<1>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else if (epl <= 2) e = launch_small<2>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else if (epl <= 4) e = launch_small<4>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    else e = launch_small<8>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
     if (e != cudaSuccess) return e;
     return x && !in_cta ? launch_gather(x, s, ws, st) : cudaSuccess;
 }

@@ -220,8 +220,8 @@ static ExpertPath expert_path(const Sizes& s, bool packed) {
 
 // The kernel sequence.  All pointers checked by the caller.
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
-                const Sizes& s, int norm, __nv_bfloat16* out, float* logits, int32_t* idx,
-                float* w, float* aux, const Workspace& ws, cudaStream_t st) {
+                const Sizes& s, int norm, const float* bias, __nv_bfloat16* out, float* logits,
+                int32_t* idx, float* w, float* aux, const Workspace& ws, cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
     const ExpertPath path = expert_path(s, W.packed != nullptr);
@@ -249,7 +249,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         const int nsplit = router_tc_splits(s);
         e = launch_router_tc(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
         if (e == cudaSuccess)
-            e = launch_route_from_logits(ws.logit_parts, nsplit, logits, s, norm, idx, w,
+            e = launch_route_from_logits(ws.logit_parts, nsplit, logits, s, norm, bias, idx, w,
                                          ws.p_partial, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
@@ -259,10 +259,12 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         e = launch_router_logits(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
-        e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, idx, w, gather_x, s,
+        e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, bias, idx, w,
+                                        gather_x, s,
                                         ws, tile_rows, aux, st);
     } else {
-        e = launch_router(x, Wr, s, norm, logits, ws.logit_parts, idx, w, ws.p_partial, ws.status,
+        e = launch_router(x, Wr, s, norm, bias, logits, ws.logit_parts, idx, w, ws.p_partial,
+                          ws.status,
                           ws.n_clear, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
@@ -309,11 +311,12 @@ using namespace moe;
 // workspace == NULL), kernel sequence.  wg/wu/wd are only null-checked.
 static int forward_device(const void* x, int T, int H, const void* W_router,
                           const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
-                          int E, int K, int I, int norm, void* out, float* logits, int32_t* idx,
-                          float* w, float* aux, void* workspace, size_t workspace_bytes,
-                          cudaStream_t st) {
+                          int E, int K, int I, int norm, const float* bias, void* out,
+                          float* logits, int32_t* idx, float* w, float* aux, void* workspace,
+                          size_t workspace_bytes, cudaStream_t st) {
     int rc = check_forward_args(x, T, H, W_router, wg, wu, wd, E, K, I, out, logits, idx, w, aux);
     if (rc) return rc;
+    if (misaligned(bias)) return MOE_ERR_ALIGNMENT;
     if (T == 0) {
         if (aux) return cuda_status(cudaMemsetAsync(aux, 0, sizeof(float), st));
         return MOE_OK;
@@ -330,7 +333,7 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
     }
     Workspace ws;
     layout_workspace(s, (char*)workspace, &ws);
-    rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s, norm,
+    rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s, norm, bias,
                      (__nv_bfloat16*)out, logits, idx, w, aux, ws, st);
     if (rc == MOE_OK && owned) remember_counts(st, ws, E);
     return rc;
@@ -341,13 +344,14 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
 // copied back, and the call returns after the stream has finished them.
 static int forward_host(const void* x_host, int T, int H, const void* W_router,
                         const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
-                        int E, int K, int I, int norm, void* out_host, float* logits_host,
-                        int32_t* idx_host, float* w_host, float* aux_host, cudaStream_t st) {
+                        int E, int K, int I, int norm, const float* bias, void* out_host,
+                        float* logits_host, int32_t* idx_host, float* w_host, float* aux_host,
+                        cudaStream_t st) {
     int rc = check_sizes(T, H, E, K, I);
     if (rc) return rc;
     if (!W_router || !wg || !wu || !wd) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x_host || !out_host)) return MOE_ERR_INVALID_ARG;
-    const void* dps[] = {W_router, wg, wu, wd};
+    const void* dps[] = {W_router, wg, wu, wd, bias};
     for (const void* p : dps)
         if (misaligned(p)) return MOE_ERR_ALIGNMENT;
     rc = check_device();
@@ -379,7 +383,7 @@ static int forward_host(const void* x_host, int T, int H, const void* W_router,
     float* aux_d = (float*)p;
     cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_status(e);
-    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, out_d,
+    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, bias, out_d,
                      logits_host ? logits_d : nullptr, idx_d, w_d, aux_host ? aux_d : nullptr, ws,
                      st);
     if (rc) return rc;
@@ -473,8 +477,8 @@ int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                          out, router_logits, topk_idx, topk_w, aux, workspace, workspace_bytes,
-                          (cudaStream_t)stream);
+                          nullptr, out, router_logits, topk_idx, topk_w, aux, workspace,
+                          workspace_bytes, (cudaStream_t)stream);
 }
 
 int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router, const moe_bf16* W_gate,
@@ -484,7 +488,7 @@ int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router, const
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                          out, router_logits, topk_idx, topk_w, aux, nullptr, 0,
+                          nullptr, out, router_logits, topk_idx, topk_w, aux, nullptr, 0,
                           (cudaStream_t)stream);
 }
 
@@ -517,8 +521,31 @@ int moe_forward_packed(const moe_bf16* x, int T, int H, const moe_bf16* W_router
     if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
     const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
     return forward_device(x, T, H, W_router, W, packed_experts, packed_experts, packed_experts,
-                          E, K, I, norm_topk_prob, out, router_logits, topk_idx, topk_w, aux,
-                          workspace, workspace_bytes, (cudaStream_t)stream);
+                          E, K, I, norm_topk_prob, nullptr, out, router_logits, topk_idx, topk_w,
+                          aux, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                     const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down, int E,
+                     int K, int I, int norm_topk_prob, moe_bf16* out, float* router_logits,
+                     int32_t* topk_idx, float* topk_w, float* aux, const moe_forward_options* opts,
+                     void* stream) {
+    const moe_forward_options none{};
+    const moe_forward_options& o = opts ? *opts : none;
+    if (o.packed_experts) {
+        if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+        if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
+        const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)o.packed_experts};
+        return forward_device(x, T, H, W_router, W, o.packed_experts, o.packed_experts,
+                              o.packed_experts, E, K, I, norm_topk_prob, o.expert_bias, out,
+                              router_logits, topk_idx, topk_w, aux, o.workspace,
+                              o.workspace_bytes, (cudaStream_t)stream);
+    }
+    const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
+                          (const __nv_bfloat16*)W_down, nullptr};
+    return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
+                          o.expert_bias, out, router_logits, topk_idx, topk_w, aux, o.workspace,
+                          o.workspace_bytes, (cudaStream_t)stream);
 }
 
 int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
@@ -529,8 +556,8 @@ int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_rou
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_host(x_host, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                        out_host, router_logits_host, topk_idx_host, topk_w_host, aux_host,
-                        (cudaStream_t)stream);
+                        nullptr, out_host, router_logits_host, topk_idx_host, topk_w_host,
+                        aux_host, (cudaStream_t)stream);
 }
 
 int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
@@ -542,8 +569,9 @@ int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16
     if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
     const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
     return forward_host(x_host, T, H, W_router, W, packed_experts, packed_experts,
-                        packed_experts, E, K, I, norm_topk_prob, out_host, router_logits_host,
-                        topk_idx_host, topk_w_host, aux_host, (cudaStream_t)stream);
+                        packed_experts, E, K, I, norm_topk_prob, nullptr, out_host,
+                        router_logits_host, topk_idx_host, topk_w_host, aux_host,
+                        (cudaStream_t)stream);
 }
 
 int moe_last_expert_counts(int32_t* counts_host, int E, void* stream) {
@@ -585,17 +613,21 @@ int moe_device_status(const void* workspace, int T, int H, int E, int K, int I, 
 }
 
 int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm_topk_prob,
-                              int32_t* topk_idx, float* topk_w, void* stream) {
+                              const float* expert_bias, int32_t* topk_idx, float* topk_w,
+                              void* stream) {
     if (T < 0 || E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK)
         return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!logits || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
-    if (misaligned(logits) || misaligned(topk_idx) || misaligned(topk_w)) return MOE_ERR_ALIGNMENT;
+    if (misaligned(logits) || misaligned(topk_idx) || misaligned(topk_w) ||
+        misaligned(expert_bias))
+        return MOE_ERR_ALIGNMENT;
     int rc = check_device();
     if (rc) return rc;
     if (T == 0) return MOE_OK;
     Sizes s{T, 64, E, K, 64};
-    return cuda_status(launch_route_from_logits(logits, 1, nullptr, s, norm_topk_prob, topk_idx,
-                                                topk_w, nullptr, (cudaStream_t)stream));
+    return cuda_status(launch_route_from_logits(logits, 1, nullptr, s, norm_topk_prob,
+                                                expert_bias, topk_idx, topk_w, nullptr,
+                                                (cudaStream_t)stream));
 }
 
 int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,

@@ -109,9 +109,11 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
 // CUDA-core router: expert- and H-split logits kernel (partial logits in
 // parts [kRouterMaxSplits][T][E]) + per-token routing kernel; writes
 // s.nrouter() rows of probability sums; logits (may be null) gets the sum.
+// bias (fp32 [E] or null): selection-only expert bias (routing.cuh).
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, float* parts, int32_t* idx, float* w,
-                          float* p_partial, int32_t* status, int n_clear, cudaStream_t st);
+                          int norm, const float* bias, float* logits, float* parts, int32_t* idx,
+                          float* w, float* p_partial, int32_t* status, int n_clear,
+                          cudaStream_t st);
 // The logits kernel of launch_router alone (nsplit slices of H, from
 // router_simt_splits), for the small-batch path that routes in the dispatch.
 int router_simt_splits(const Sizes& s);
@@ -128,8 +130,8 @@ bool router_tc_supported(const Sizes& s);  // E <= 128
 // Softmax, top-k, renorm and per-32-token probability sums (s.nrouter() rows)
 // from the sum of nparts partial-logit arrays; logits_out (may be null) gets the sum.
 cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,
-                                     const Sizes& s, int norm, int32_t* idx, float* w,
-                                     float* p_partial, cudaStream_t st);
+                                     const Sizes& s, int norm, const float* bias, int32_t* idx,
+                                     float* w, float* p_partial, cudaStream_t st);
 // p_partial holds n_partials rows of per-expert probability sums (for aux).
 // x != null: also gather x_perm[row] = x[perm_tok[row]].
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
@@ -141,7 +143,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
 // gather kernel.
 constexpr int kRouteDispatchTokens = 32;
 cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* logits_out,
-                                        int norm, int32_t* idx, float* w,
+                                        int norm, const float* bias, int32_t* idx, float* w,
                                         const __nv_bfloat16* x, const Sizes& s,
                                         const Workspace& ws, int rows_per_tile, float* aux,
                                         cudaStream_t st);
@@ -197,8 +199,8 @@ int check_forward_args(const void* x, int T, int H, const void* Wr, const void* 
                        const void* Wu, const void* Wd, int E, int K, int I, const void* out,
                        const void* logits, const void* idx, const void* w, const void* aux);
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
-                const Sizes& s, int norm, __nv_bfloat16* out, float* logits, int32_t* idx,
-                float* w, float* aux, const Workspace& ws, cudaStream_t st);
+                const Sizes& s, int norm, const float* bias, __nv_bfloat16* out, float* logits,
+                int32_t* idx, float* w, float* aux, const Workspace& ws, cudaStream_t st);
 
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);

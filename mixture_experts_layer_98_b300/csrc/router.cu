@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
 template <int EPL>
 __global__ void __launch_bounds__(kRouterTokens * 32) route_from_logits_kernel(
     const float* parts, int nparts, size_t part_stride, float* logits_out, int T, int E, int K,
-    int norm, int32_t* idx, float* w, float* p_partial) {
+    int norm, const float* bias, int32_t* idx, float* w, float* p_partial) {
     __shared__ float ls[kRouterTokens * kMaxExperts];
     pdl_trigger();
     pdl_wait();
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kRouterTokens * 32) route_from_logits_kernel(
                 l[q] = -INFINITY;
             }
         }
-        route_token<EPL>(l, E, K, norm, idx + (size_t)t * K, w + (size_t)t * K, ls + j * E);
+        route_token<EPL>(l, E, K, norm, bias, idx + (size_t)t * K, w + (size_t)t * K, ls + j * E);
     }
     __syncthreads();
     if (p_partial) {
@@ -128,10 +128,11 @@ __global__ void __launch_bounds__(kRouterTokens * 32) route_from_logits_kernel(
 
 template <int EPL>
 cudaError_t launch_route_t(const float* parts, int nparts, float* logits_out, const Sizes& s,
-                           int norm, int32_t* idx, float* w, float* p_partial, cudaStream_t st) {
+                           int norm, const float* bias, int32_t* idx, float* w, float* p_partial,
+                           cudaStream_t st) {
     cudaError_t e = launch_pdl(route_from_logits_kernel<EPL>, dim3(s.nrouter()),
                                dim3(kRouterTokens * 32), 0, st, parts, nparts, (size_t)s.T * s.E,
-                               logits_out, s.T, s.E, s.K, norm, idx, w, p_partial);
+                               logits_out, s.T, s.E, s.K, norm, bias, idx, w, p_partial);
     count_launches(1);
     return e;
 }
@@ -165,22 +166,26 @@ cudaError_t launch_router_logits(const __nv_bfloat16* x, const __nv_bfloat16* Wr
 }
 
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const Sizes& s,
-                          int norm, float* logits, float* parts, int32_t* idx, float* w,
-                          float* p_partial, int32_t* status, int n_clear, cudaStream_t st) {
+                          int norm, const float* bias, float* logits, float* parts, int32_t* idx,
+                          float* w, float* p_partial, int32_t* status, int n_clear,
+                          cudaStream_t st) {
     const int nsplit = router_simt_splits(s);
     cudaError_t err = launch_router_logits(x, Wr, s, nsplit, parts, status, n_clear, st);
     if (err != cudaSuccess) return err;
-    return launch_route_from_logits(parts, nsplit, logits, s, norm, idx, w, p_partial, st);
+    return launch_route_from_logits(parts, nsplit, logits, s, norm, bias, idx, w, p_partial, st);
 }
 
 cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,
-                                     const Sizes& s, int norm, int32_t* idx, float* w,
-                                     float* p_partial, cudaStream_t st) {
+                                     const Sizes& s, int norm, const float* bias, int32_t* idx,
+                                     float* w, float* p_partial, cudaStream_t st) {
     const int epl = (s.E + 31) / 32;
-    if (epl <= 1) return launch_route_t<1>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
-    if (epl <= 2) return launch_route_t<2>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
-    if (epl <= 4) return launch_route_t<4>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
-    return launch_route_t<8>(parts, nparts, logits_out, s, norm, idx, w, p_partial, st);
+    if (epl <= 1)
+        return launch_route_t<1>(parts, nparts, logits_out, s, norm, bias, idx, w, p_partial, st);
+    if (epl <= 2)
+        return launch_route_t<2>(parts, nparts, logits_out, s, norm, bias, idx, w, p_partial, st);
+    if (epl <= 4)
+        return launch_route_t<4>(parts, nparts, logits_out, s, norm, bias, idx, w, p_partial, st);
+    return launch_route_t<8>(parts, nparts, logits_out, s, norm, bias, idx, w, p_partial, st);
 }
 
 }  // namespace moe

@@ -20,10 +20,6 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -38,10 +34,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // One warp routes one token whose E logits sit in l[] (lane holds experts
 // lane, lane+32, ...).  Writes idx/w for the token and, when probs != null,
-// the full softmax into probs[0..E).
+// the full softmax into probs[0..E).  With bias != null (fp32 [E], a
+// selection-only expert bias for auxiliary-loss-free balancing, the DeepSeek
+// scheme of the sshipanoo.com page "项目 17：稀疏性的调度艺术", section
+// "第四阶段：更先进的路由方案：DeepSeek 的突破") the experts are ranked by the
+// fp32 key l + bias while their weights stay the unbiased probabilities.
 template <int EPL>
 __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K, int norm,
-                                            int32_t* idx_row, float* w_row, float* probs) {
+                                            const float* bias, int32_t* idx_row, float* w_row,
+                                            float* probs) {
     const int lane = threadIdx.x & 31;
     float m = -INFINITY;
 #pragma unroll
@@ -65,10 +66,14 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
     }
     // K rounds of a warp-wide arg-max: the largest key, then the lowest expert
     // index among the lanes holding it (two redux.sync per round).  The
-    // winner's probability is recomputed from its value in every lane.
+    // winner's probability is recomputed in every lane from its unbiased
+    // logit, fetched from the lane that holds it.
     uint32_t key[EPL];
 #pragma unroll
-    for (int q = 0; q < EPL; ++q) key[q] = (lane + 32 * q < E) ? order_key(l[q]) : 0u;
+    for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        key[q] = e < E ? order_key(bias ? l[q] + bias[e] : l[q]) : 0u;
+    }
     float wsum = 0.f;
     int my_e = -1;
     float my_p = 0.f;
@@ -83,10 +88,15 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
             }
         const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
         const int we = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)be : 0x7fffffffu);
+        float lw = 0.f;
 #pragma unroll
-        for (int q = 0; q < EPL; ++q)  // taken
-            if (we == lane + 32 * q) key[q] = 0u;
-        const float pk = expf(key_value(mk) - m) * inv_s;
+        for (int q = 0; q < EPL; ++q)  // taken; the winner's unbiased logit
+            if (we == lane + 32 * q) {
+                key[q] = 0u;
+                lw = l[q];
+            }
+        lw = __shfl_sync(0xffffffffu, lw, we & 31);
+        const float pk = expf(lw - m) * inv_s;
         wsum += pk;  // same value and order in every lane
         if (lane == k) {
             my_e = we;

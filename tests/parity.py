@@ -63,13 +63,24 @@ def gpu_forward(inputs, K, norm):
                 w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=counts)
 
 
-def compare(b, g, K, norm, rows=None):
-    """b: host bits of the inputs; g: GPU results.  Returns a report dict and
-    raises AssertionError on any failed check."""
+def near_tie_keys(keys, K, rel):
+    """Tokens whose ranking keys (logit + selection bias) at the K/K+1 boundary,
+    or between adjacent kept experts, differ by less than rel·(1 + |key|): the
+    logits' own tolerance can reorder them, so more than one selection is
+    correct."""
+    k = -np.sort(-np.asarray(keys, np.float64), axis=1)[:, :min(K + 1, keys.shape[1])]
+    d = k[:, :-1] - k[:, 1:]
+    return np.where((d < rel * (1 + np.abs(k[:, 1:]))).any(axis=1))[0]
+
+
+def compare(b, g, K, norm, rows=None, bias=None):
+    """b: host bits of the inputs; g: GPU results; bias: the selection-only
+    expert bias (float32 [E]) when the forward had one.  Returns a report dict
+    and raises AssertionError on any failed check."""
     T, H = b["x"].shape
     E = b["W_router"].shape[0]
     o = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], K, norm,
-                           rows=rows)
+                           rows=rows, bias=bias)
     rep = {}
     # logits
     dl = np.abs(g["logits"].astype(np.float64) - o["logits"])
@@ -77,7 +88,11 @@ def compare(b, g, K, norm, rows=None):
     assert rep["logit_err"] <= LOGIT_RTOL, rep
     # selection
     probs = oracle.softmax(o["logits"])
-    ties = set(oracle.near_tie_tokens(probs, K, TIE_GAP).tolist())
+    if bias is None:
+        ties = set(oracle.near_tie_tokens(probs, K, TIE_GAP).tolist())
+    else:
+        keys = (o["logits"] + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+        ties = set(near_tie_keys(keys, K, 2 * LOGIT_RTOL).tolist())
     mism = np.where((g["idx"] != o["idx"]).any(axis=1))[0]
     bad = [t for t in mism.tolist() if t not in ties]
     rep["near_ties"] = len(ties)

@@ -117,3 +117,20 @@ def test_packed_host_call_and_caller_workspace(moe):
     for u, v in zip(ref, got2):
         assert torch.equal(u, v)
     assert moe.moe_device_status(ws, (cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)) == 0
+
+
+def test_packed_with_selection_bias_matches_row_major(moe):
+    cfg = mi.CONFIGS["decode_t64"]
+    inp = mi.make_inputs(cfg, "cuda")
+    bias = torch.from_numpy((np.random.default_rng(3).standard_normal(cfg.E) * 0.5)
+                            .astype(np.float32)).cuda()
+    ref = [t.clone() for t in moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"],
+                                                   inp["W_up"], inp["W_down"], cfg.K, cfg.norm,
+                                                   expert_bias=bias)]
+    pk = moe.moe_pack_experts(inp["W_gate"], inp["W_up"], inp["W_down"])
+    got = moe.moe_forward_opts(inp["x"], inp["W_router"], None, None, None, cfg.K, cfg.norm,
+                               expert_bias=bias, packed=pk)
+    torch.cuda.synchronize()
+    for u, v in zip(ref, got):
+        assert torch.equal(u, v)
+

@@ -56,6 +56,22 @@ def test_route_from_logits_bit_exact(moe, E, K, norm):
     assert np.abs(w.cpu().numpy() - rw).max() <= 1e-5
 
 
+@pytest.mark.parametrize("E,K", [(8, 2), (128, 8), (256, 16), (33, 7)])
+@pytest.mark.parametrize("norm", [False, True])
+def test_route_with_selection_bias_bit_exact(moe, E, K, norm):
+    # keys logit + bias on multiples of 1/4: exact ties between keys
+    rng = np.random.default_rng(E * 10 + K)
+    T = 200
+    l = (rng.integers(-12, 13, (T, E)) / 4).astype(np.float32)
+    l[100:] = (rng.standard_normal((T - 100, E)) * 1.5).astype(np.float32)
+    b = (rng.integers(-6, 7, E) / 4).astype(np.float32)
+    idx, w = moe.moe_dbg_route_from_logits(torch.from_numpy(l).cuda(), K, norm,
+                                           expert_bias=torch.from_numpy(b).cuda())
+    ridx, rw = oracle.route_from_logits(l, K, norm, bias=b)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 1e-5
+
+
 @pytest.mark.parametrize("T,E,K", [(1, 8, 2), (255, 8, 2), (256, 16, 4), (257, 128, 8),
                                    (4096, 128, 8), (1000, 256, 16), (37, 1, 1), (0, 8, 2)])
 def test_permute_bit_exact(moe, T, E, K):
@@ -213,6 +229,49 @@ def test_decode_repeatable_with_dirty_workspace(moe):
         for u, v in zip(ref, got):
             assert torch.equal(u, v)
     assert moe.moe_device_status(ws, (cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)) == 0
+
+
+def _bias_for(cfg, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal(cfg.E) * 0.5).astype(np.float32)
+
+
+@pytest.mark.parametrize("name,T", [("decode_t4", None), ("decode_t64", None),
+                                    ("tiny", None), ("prefill_h2048", 512)])
+def test_forward_with_selection_bias(moe, name, T):
+    # T <= 32: routing in the one-CTA dispatch; 64: routing kernel after the
+    # CUDA-core router; 512: after the tensor-core router
+    cfg = mi.CONFIGS[name]
+    if T is not None:
+        cfg = mi.MoEConfig(name + "_t", T, cfg.H, cfg.E, cfg.K, cfg.I, cfg.norm, seed=cfg.seed)
+    inp = mi.make_inputs(cfg, "cuda")
+    bias = _bias_for(cfg, 5)
+    out, lg, idx, w, aux = moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"],
+                                                inp["W_up"], inp["W_down"], cfg.K, cfg.norm,
+                                                expert_bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
+             w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
+    rep = compare(host_bits(inp), g, cfg.K, cfg.norm, bias=bias)
+    # the bias moved selections (it is large next to the logit spread at these sizes)
+    plain = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"],
+                            inp["W_down"], cfg.K, cfg.norm)
+    torch.cuda.synchronize()
+    assert not torch.equal(plain[2], idx), rep
+
+
+def test_zero_selection_bias_is_the_plain_forward(moe):
+    cfg = mi.CONFIGS["decode_t16"]
+    inp = mi.make_inputs(cfg, "cuda")
+    ref = moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                          cfg.K, cfg.norm)
+    ref = [t.clone() for t in ref]
+    got = moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"],
+                               inp["W_down"], cfg.K, cfg.norm,
+                               expert_bias=torch.zeros(cfg.E, device="cuda"))
+    torch.cuda.synchronize()
+    for u, v in zip(ref, got):
+        assert torch.equal(u, v)
 
 
 def test_prefill_repeatable_over_many_forwards(moe):
