@@ -208,28 +208,73 @@ int oracle_route_from_logits(const float* logits, int T, int E, int K, int norm,
  *   perm_tok[r]  = token of the pair in row r;  perm_slot[r] = its k-slot
  *   inv[t*K+k]   = row of pair (t,k)
  * Unique, because a token selects each expert at most once. */
-int oracle_dispatch(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
-                    int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv) {
+/* Expert capacity (section "容量因子设计" of the csdn page "MoE架构深度解析：
+ * 128专家与8激活的智能路由": capacity = batch tokens / experts × capacity
+ * factor), read for K experts per token as C = ceil(cf·T·K/E) pairs: each
+ * expert keeps the first C pairs routed to it, in token order, the way the
+ * lpnh.cn page's capacity-aware inference routing fills each expert token by
+ * token; keep[t*K+k] = 0 for the others (dropped: they add nothing to the
+ * block output).  capacity <= 0 keeps every pair. */
+int oracle_keep_mask(const int32_t* topk_idx, int T, int E, int K, int capacity, uint8_t* keep) {
     if (T < 0 || E < 1 || K < 1) return 1;
-    for (int e = 0; e < E; ++e) counts[e] = 0;
-    for (size_t i = 0; i < (size_t)T * K; ++i) {
-        int e = topk_idx[i];
-        if (e < 0 || e >= E) return 3;
-        counts[e] += 1;
+    int32_t* seen = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    if (!seen) return 2;
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            const int e = topk_idx[(size_t)t * K + k];
+            if (e < 0 || e >= E) {
+                free(seen);
+                return 3;
+            }
+            keep[(size_t)t * K + k] = (uint8_t)(capacity <= 0 || seen[e] < capacity);
+            seen[e] += 1;
+        }
+    free(seen);
+    return 0;
+}
+
+/* With a capacity, the rows hold the kept pairs only (same order), counts[e]
+ * stays the number of pairs routed to e, offsets are prefix sums of the kept
+ * counts (offsets[E] = kept pairs) and inv = -1 for a dropped pair. */
+int oracle_dispatch_cap(const int32_t* topk_idx, int T, int E, int K, int capacity,
+                        int32_t* counts, int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot,
+                        int32_t* inv) {
+    if (T < 0 || E < 1 || K < 1) return 1;
+    uint8_t* keep = (uint8_t*)malloc((size_t)T * K + 1);
+    if (!keep) return 2;
+    int rc = oracle_keep_mask(topk_idx, T, E, K, capacity, keep);
+    if (rc) {
+        free(keep);
+        return rc;
     }
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (size_t i = 0; i < (size_t)T * K; ++i) counts[topk_idx[i]] += 1;
     offsets[0] = 0;
-    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    for (int e = 0; e < E; ++e) {
+        const int kept = capacity > 0 && counts[e] > capacity ? capacity : counts[e];
+        offsets[e + 1] = offsets[e] + kept;
+    }
     int32_t row = 0;
     for (int e = 0; e < E; ++e)
         for (int t = 0; t < T; ++t)
             for (int k = 0; k < K; ++k)
                 if (topk_idx[(size_t)t * K + k] == e) {
+                    if (!keep[(size_t)t * K + k]) {
+                        inv[(size_t)t * K + k] = -1;
+                        continue;
+                    }
                     perm_tok[row] = t;
                     perm_slot[row] = k;
                     inv[(size_t)t * K + k] = row;
                     ++row;
                 }
+    free(keep);
     return 0;
+}
+
+int oracle_dispatch(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv) {
+    return oracle_dispatch_cap(topk_idx, T, E, K, 0, counts, offsets, perm_tok, perm_slot, inv);
 }
 
 /* ---- step 6: one expert's SwiGLU MLP on one token ----------------------- */
@@ -323,8 +368,8 @@ double oracle_aux(const double* probs, const int32_t* counts, int T, int E, int 
  * not NULL, out_f64[n_rows, H] (the same values before the bf16 rounding).
  * Any of logits / idx / w / aux / counts may be NULL.  Returns 0 on success. */
 int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
-                         const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int K,
-                         int I, int norm, int flags, const int32_t* rows, int n_rows,
+                         int capacity, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                         int E, int K, int I, int norm, int flags, const int32_t* rows, int n_rows,
                          uint16_t* out, double* out_f64, float* logits_out, int32_t* idx_out,
                          float* w_out, float* aux_out, int32_t* counts_out) {
     if (T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || I < 1) return 1;
@@ -339,14 +384,16 @@ int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, co
     int32_t* idx = (int32_t*)malloc(TK * sizeof(int32_t));
     float* w = (float*)malloc(TK * sizeof(float));
     int32_t* counts = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    uint8_t* keep = (uint8_t*)malloc(TK);
     int rc = 0;
-    if (!logits || !probs || !idx || !w || !counts) rc = 2;
+    if (!logits || !probs || !idx || !w || !counts || !keep) rc = 2;
     if (!rc) rc = oracle_router_logits(x, T, H, Wr, E, flags, logits);
     if (!rc) rc = oracle_softmax(logits, T, E, probs);
     if (!rc) rc = oracle_route_biased(logits, bias, T, E, K, norm, idx, w);
     if (!rc) {
         for (size_t i = 0; i < TK; ++i) counts[idx[i]] += 1;
         if (aux_out) *aux_out = (float)oracle_aux(probs, counts, T, E, K);
+        rc = oracle_keep_mask(idx, T, E, K, capacity, keep);
     }
     if (!rc && (out || out_f64)) {
         int n = rows ? n_rows : T;
@@ -355,8 +402,16 @@ int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, co
         for (int j = 0; j < n; ++j) {
             int t = rows ? rows[j] : j;
             if (t < 0 || t >= T) { fail |= 1; continue; }
-            if (oracle_token_output_ex(x + (size_t)t * H, H, idx + (size_t)t * K,
-                                       w + (size_t)t * K, K, Wg, Wu, Wd, E, I, flags,
+            int32_t ik[1024];  /* the token's kept pairs, in k order */
+            float wk[1024];
+            int nk = 0;
+            for (int k = 0; k < K; ++k)
+                if (keep[(size_t)t * K + k]) {
+                    ik[nk] = idx[(size_t)t * K + k];
+                    wk[nk] = w[(size_t)t * K + k];
+                    ++nk;
+                }
+            if (oracle_token_output_ex(x + (size_t)t * H, H, ik, wk, nk, Wg, Wu, Wd, E, I, flags,
                                        out ? out + (size_t)j * H : NULL,
                                        out_f64 ? out_f64 + (size_t)j * H : NULL))
                 fail |= 1;
@@ -374,15 +429,16 @@ int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, co
     free(idx);
     free(w);
     free(counts);
+    free(keep);
     return rc;
 }
 
-/* The block forward without a selection bias. */
+/* The block forward without a selection bias or a capacity. */
 int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, const uint16_t* Wg,
                        const uint16_t* Wu, const uint16_t* Wd, int E, int K, int I, int norm,
                        int flags, const int32_t* rows, int n_rows, uint16_t* out,
                        double* out_f64, float* logits_out, int32_t* idx_out, float* w_out,
                        float* aux_out, int32_t* counts_out) {
-    return oracle_moe_forward_b(x, T, H, Wr, NULL, Wg, Wu, Wd, E, K, I, norm, flags, rows, n_rows,
+    return oracle_moe_forward_b(x, T, H, Wr, NULL, 0, Wg, Wu, Wd, E, K, I, norm, flags, rows, n_rows,
                                 out, out_f64, logits_out, idx_out, w_out, aux_out, counts_out);
 }

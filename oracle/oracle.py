@@ -35,6 +35,8 @@ class _Lib:
         lib.oracle_route_from_logits.argtypes = [P, i, i, i, i, P, P]
         lib.oracle_route_biased.argtypes = [P, P, i, i, i, i, P, P]
         lib.oracle_dispatch.argtypes = [P, i, i, i, P, P, P, P, P]
+        lib.oracle_dispatch_cap.argtypes = [P, i, i, i, i, P, P, P, P, P]
+        lib.oracle_keep_mask.argtypes = [P, i, i, i, i, P]
         lib.oracle_expert_mlp.argtypes = [P, i, P, P, P, i, i, P]
         lib.oracle_token_output.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P]
         lib.oracle_token_output_ex.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P, P]
@@ -42,8 +44,8 @@ class _Lib:
         lib.oracle_aux.restype = ctypes.c_double
         lib.oracle_moe_forward.argtypes = [P, i, i, P, P, P, P, i, i, i, i, i, P, i, P, P, P,
                                            P, P, P, P]
-        lib.oracle_moe_forward_b.argtypes = [P, i, i, P, P, P, P, P, i, i, i, i, i, P, i, P, P,
-                                             P, P, P, P, P]
+        lib.oracle_moe_forward_b.argtypes = [P, i, i, P, P, i, P, P, P, i, i, i, i, i, P, i, P,
+                                             P, P, P, P, P, P]
         self.c = lib
 
 
@@ -154,8 +156,11 @@ def route_from_logits(logits, K, norm, bias=None):
     return idx, w
 
 
-def dispatch(idx, E):
-    """Group pairs by (expert, token) -> dict(counts, offsets, perm_tok, perm_slot, inv)."""
+def dispatch(idx, E, capacity=0):
+    """Group pairs by (expert, token) -> dict(counts, offsets, perm_tok, perm_slot, inv).
+    With capacity > 0 each expert keeps its first `capacity` pairs in token order:
+    rows hold the kept pairs, offsets count them, inv = -1 for the dropped ones and
+    counts stay the routed pairs; perm_tok / perm_slot have offsets[E] entries."""
     idx = _c(idx, np.int32)
     T, K = idx.shape
     counts = np.empty(E, np.int32)
@@ -163,10 +168,20 @@ def dispatch(idx, E):
     perm_tok = np.empty(T * K, np.int32)
     perm_slot = np.empty(T * K, np.int32)
     inv = np.empty(T * K, np.int32)
-    _check(_L().oracle_dispatch(_p(idx), T, E, K, _p(counts), _p(offsets), _p(perm_tok),
-                                _p(perm_slot), _p(inv)), "dispatch")
-    return dict(counts=counts, offsets=offsets, perm_tok=perm_tok, perm_slot=perm_slot,
+    _check(_L().oracle_dispatch_cap(_p(idx), T, E, K, int(capacity), _p(counts), _p(offsets),
+                                    _p(perm_tok), _p(perm_slot), _p(inv)), "dispatch")
+    n = int(offsets[E])
+    return dict(counts=counts, offsets=offsets, perm_tok=perm_tok[:n], perm_slot=perm_slot[:n],
                 inv=inv.reshape(T, K))
+
+
+def keep_mask(idx, E, capacity):
+    """bool [T,K]: the pairs each expert keeps under the capacity (first in token order)."""
+    idx = _c(idx, np.int32)
+    T, K = idx.shape
+    keep = np.empty((T, K), np.uint8)
+    _check(_L().oracle_keep_mask(_p(idx), T, E, K, int(capacity), _p(keep)), "keep_mask")
+    return keep.astype(bool)
 
 
 def expert_mlp(x_row, Wg_e, Wu_e, Wd_e, flags=0):
@@ -204,9 +219,12 @@ def aux(probs, counts, K):
     return float(_L().oracle_aux(_p(p), _p(c), T, E, K))
 
 
-def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True, bias=None):
+def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True, bias=None,
+                capacity=0):
     """The whole block (with bias: the selection-only expert bias of
-    route_from_logits).  Returns dict(out, out_f64, logits, idx, w, aux, counts).
+    route_from_logits; with capacity > 0: each expert keeps its first `capacity`
+    pairs in token order and the dropped pairs add nothing to out).  Returns
+    dict(out, out_f64, logits, idx, w, aux, counts); counts are the routed pairs.
 
     out is bf16 bits [n_rows, H] for the listed token rows (all tokens when
     rows is None) and out_f64 the same values before the final bf16 rounding;
@@ -230,8 +248,9 @@ def moe_forward(x, Wr, Wg, Wu, Wd, K, norm, rows=None, flags=0, want_out=True, b
     counts = np.empty(E, np.int32)
     a = np.zeros(1, np.float32)
     b = None if bias is None else _c(bias, np.float32)
-    _check(_L().oracle_moe_forward_b(_p(x), T, H, _p(Wr), _p(b), _p(Wg), _p(Wu), _p(Wd), E, K,
-                                     I, int(bool(norm)), flags, _p(rows), n, _p(out),
+    _check(_L().oracle_moe_forward_b(_p(x), T, H, _p(Wr), _p(b), int(capacity), _p(Wg), _p(Wu),
+                                     _p(Wd), E, K, I, int(bool(norm)), flags, _p(rows), n,
+                                     _p(out),
                                      _p(out_f64), _p(logits), _p(idx), _p(w), _p(a),
                                      _p(counts)), "forward")
     return dict(out=out, out_f64=out_f64, logits=logits, idx=idx, w=w, aux=float(a[0]),
@@ -251,3 +270,12 @@ def near_tie_tokens(probs, K, gap=1e-6):
     s = -np.sort(-p, axis=1)[:, :K + 1]
     d = s[:, :-1] - s[:, 1:]
     return np.where((d < gap).any(axis=1))[0]
+
+
+def capacity_of(cf, T, K, E):
+    """Pairs each expert keeps for capacity factor cf: ceil(cf·T·K/E) (0: no limit)."""
+    if not cf or cf <= 0:
+        return 0
+    import math
+    return int(math.ceil(cf * T * K / E))
+

@@ -343,12 +343,76 @@ def pin_bias_forces_selection_and_aux():
                                                                            rtol=1e-6)
 
 
+# ---- expert capacity (first C pairs of each expert in token order) -----------
+
+def _kept_by_hand(idx, E, C):
+    """Brute force: walk the tokens in order, count per expert, keep the first C."""
+    seen = [0] * E
+    keep = np.zeros(idx.shape, bool)
+    for t in range(idx.shape[0]):
+        for k in range(idx.shape[1]):
+            e = int(idx[t, k])
+            keep[t, k] = seen[e] < C
+            seen[e] += 1
+    return keep
+
+
+def pin_capacity_bruteforce():
+    # out[t] = Σ over the token's kept pairs of w·SwiGLU, in float64 numpy
+    cfg, b = rand_case(24, 64, 4, 2, 64, seed=31, norm=True)
+    C = 5
+    r = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 2, True,
+                           capacity=C)
+    keep = _kept_by_hand(r["idx"], 4, C)
+    assert keep.sum() < keep.size  # some pairs are dropped at this capacity
+    x = bf16_bits_to_f64(b["x"])
+    Wg, Wu, Wd = (bf16_bits_to_f64(b[k]) for k in ("W_gate", "W_up", "W_down"))
+    for t in range(24):
+        want = np.zeros(64)
+        for k in range(2):
+            if keep[t, k]:
+                e = int(r["idx"][t, k])
+                want += float(r["w"][t, k]) * np_swiglu(x[t:t + 1], Wg[e], Wu[e], Wd[e])[0]
+        assert np.abs(r["out_f64"][t] - want).max() <= 1e-9 * (1 + np.abs(want).max()), t
+    # aux is the router's statistic: unchanged by the capacity
+    r0 = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 2, True)
+    assert r["aux"] == r0["aux"] and np.array_equal(r["counts"], r0["counts"])
+
+
+def pin_capacity_dispatch():
+    # kept rows: the first C tokens of each expert, in order; inv = -1 elsewhere
+    rng = np.random.default_rng(32)
+    T, E, K, C = 50, 6, 3, 7
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)], np.int32)
+    d = oracle.dispatch(idx, E, capacity=C)
+    keep = _kept_by_hand(idx, E, C)
+    assert np.array_equal(d["counts"], np.bincount(idx.ravel(), minlength=E))
+    kept_counts = np.minimum(d["counts"], C)
+    assert np.array_equal(d["offsets"], np.concatenate([[0], np.cumsum(kept_counts)]))
+    for t in range(T):
+        for k in range(K):
+            r = d["inv"][t, k]
+            if keep[t, k]:
+                assert 0 <= r < d["perm_tok"].size
+                assert d["perm_tok"][r] == t and d["perm_slot"][r] == k
+            else:
+                assert r == -1
+    for e in range(E):
+        rows = d["perm_tok"][d["offsets"][e]:d["offsets"][e + 1]]
+        assert list(rows) == sorted(np.where((idx == e).any(axis=1))[0].tolist())[:C]
+    big = oracle.dispatch(idx, E, capacity=T)  # no expert reaches T pairs: nothing dropped
+    plain = oracle.dispatch(idx, E)
+    for key in plain:
+        assert np.array_equal(big[key], plain[key])
+
+
 PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equal_logits,
         pin_weights_closed_form, pin_router_logits, pin_dispatch_bruteforce,
         pin_single_expert_is_swiglu, pin_dense_equivalence, pin_soft_router,
         pin_token_permutation_equivariance, pin_aux, pin_param_counts,
         pin_bias_zero_is_unbiased, pin_biased_topk_bruteforce,
-        pin_biased_weights_are_unbiased_probs, pin_bias_forces_selection_and_aux]
+        pin_biased_weights_are_unbiased_probs, pin_bias_forces_selection_and_aux,
+        pin_capacity_bruteforce, pin_capacity_dispatch]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -392,6 +456,10 @@ MUTATIONS = {
                          "    if (l[a] < l[b]) return 1;\n    if (l[a] > l[b]) return 0;"),
     "bias_ignored": ("keys[i] = bias ? (float)(logits[i] + bias[i % (size_t)E]) : logits[i];",
                      "keys[i] = logits[i];"),
+    "capacity_off_by_one": ("(uint8_t)(capacity <= 0 || seen[e] < capacity)",
+                            "(uint8_t)(capacity <= 0 || seen[e] <= capacity)"),
+    "dropped_pairs_contribute": ("                if (keep[(size_t)t * K + k]) {\n                    ik[nk]",
+                                 "                if (1) {\n                    ik[nk]"),
     "weights_from_biased_keys": (
         "logits[i];\n    oracle_softmax(logits, T, E, probs);",
         "logits[i];\n    oracle_softmax(keys, T, E, probs);"),
