@@ -210,6 +210,14 @@ typedef struct moe_forward_options {
      * 256-byte aligned, or NULL for the library-owned workspace of `stream`. */
     void* workspace;
     size_t workspace_bytes;
+    /* Expert capacity factor cf >= 0 (0: no capacity).  The capacity of the
+     * csdn page "MoE架构深度解析：128专家与8激活的智能路由", section "容量因子设计"
+     * (batch tokens / experts × factor), counted in token-expert pairs: each
+     * expert keeps the first C = ceil(cf·T·K/E) pairs routed to it, in token
+     * order (C >= 1), and the others are dropped: they add nothing to `out`.
+     * topk_idx / topk_w, router_logits, aux and the expert counts stay the
+     * router's.  A negative or non-finite cf gives MOE_ERR_INVALID_ARG. */
+    float capacity_factor;
 } moe_forward_options;
 
 /* moe_forward with the options above; every other argument as for
@@ -309,9 +317,11 @@ int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm
 /* Dispatch of given selections topk_idx [T,K] (each row holds K distinct
  * experts in [0,E)): counts [E], offsets [E+1] (exclusive prefix sum),
  * perm_tok / perm_slot [T·K] (token and k-slot of each row, rows ordered by
- * expert then token) and inv [T,K] (row of each pair).  Out-of-range experts
- * are not checked on the device. */
-int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+ * expert then token) and inv [T,K] (row of each pair).  With capacity > 0,
+ * each expert keeps its first `capacity` pairs in token order: offsets count
+ * the kept pairs, only they get rows, inv = -1 for the others, and counts stay
+ * the routed pairs.  Out-of-range experts are not checked on the device. */
+int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int capacity, int32_t* counts,
                     int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
                     void* stream);
 

@@ -38,7 +38,8 @@ STAGE_NAMES = ["router", "dispatch", "gate_up", "down", "combine"]
 class _Options(ctypes.Structure):
     """struct moe_forward_options."""
     _fields_ = [("expert_bias", ctypes.c_void_p), ("packed_experts", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("capacity_factor", ctypes.c_float)]
 
 
 class MoEError(RuntimeError):
@@ -88,7 +89,7 @@ def lib():
         L.moe_kernel_launch_count.argtypes = []
         L.moe_kernel_launch_count.restype = ctypes.c_longlong
         L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P, P]
-        L.moe_dbg_permute.argtypes = [P, i, i, i, P, P, P, P, P, P]
+        L.moe_dbg_permute.argtypes = [P, i, i, i, i, P, P, P, P, P, P]
         L.moe_dbg_combine.argtypes = [P, P, i, i, i, P, P]
         _lib = L
     return _lib
@@ -247,10 +248,11 @@ def moe_forward_host_packed(x_host, W_router, packed, K, norm_topk_prob, out_hos
 
 def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, expert_bias=None,
                      packed=None, out=None, router_logits=None, topk_idx=None, topk_w=None,
-                     aux=None, stream=None, workspace=None):
+                     aux=None, stream=None, workspace=None, capacity_factor=0.0):
     """moe_forward_opts: expert_bias (fp32 [E] CUDA tensor) is the selection-only
     expert bias; packed a PackedExperts (then W_gate / W_up / W_down may be None);
-    workspace as for moe_forward."""
+    workspace as for moe_forward; capacity_factor > 0 keeps the first
+    ceil(cf·T·K/E) pairs of each expert in token order."""
     T, H = x.shape
     if packed is not None:
         E, I = packed.E, packed.I
@@ -264,7 +266,8 @@ def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, exper
     out, router_logits, topk_idx, topk_w, aux = _outputs(T, H, E, K, x.device, out, router_logits,
                                                          topk_idx, topk_w, aux)
     opts = _Options(_ptr(expert_bias), None if packed is None else packed.data.data_ptr(),
-                    _ptr(workspace), 0 if workspace is None else workspace.numel())
+                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                    float(capacity_factor))
     _call(lib().moe_forward_opts(_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up),
                                  _ptr(W_down), E, K, I, int(bool(norm_topk_prob)), _ptr(out),
                                  _ptr(router_logits), _ptr(topk_idx), _ptr(topk_w), _ptr(aux),
@@ -351,7 +354,7 @@ def moe_dbg_route_from_logits(logits, K, norm_topk_prob, stream=None, expert_bia
     return idx, w
 
 
-def moe_dbg_permute(topk_idx, E, stream=None):
+def moe_dbg_permute(topk_idx, E, stream=None, capacity=0):
     T, K = topk_idx.shape
     _dev(topk_idx, torch.int32, "topk_idx")
     d = topk_idx.device
@@ -360,7 +363,8 @@ def moe_dbg_permute(topk_idx, E, stream=None):
     perm_tok = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
     perm_slot = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
     inv = torch.empty(max(T * K, 1), dtype=torch.int32, device=d)
-    _call(lib().moe_dbg_permute(_ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets),
+    _call(lib().moe_dbg_permute(_ptr(topk_idx), T, E, K, int(capacity), _ptr(counts),
+                                _ptr(offsets),
                                 _ptr(perm_tok), _ptr(perm_slot), _ptr(inv), _stream(stream)),
           "moe_dbg_permute")
     n = T * K

@@ -7,8 +7,10 @@
 // to bf16: no zero-fill, no atomics, and the result does not depend on
 // scheduling.  The down-projection kernels store Y token-major ([T, K, H]: the
 // pair (t, k) at row t*K + k), so a token's K rows are one contiguous read;
-// with inv != null, Y is in dispatch order and row inv[t*K + k] is read
-// instead.  16-byte loads and stores.
+// a pair with inv[t*K + k] < 0 was dropped by an expert capacity and is
+// skipped (the pages' capacity: csdn page section "容量因子设计").  With
+// y_by_inv, Y is in dispatch order and row inv[t*K + k] is read instead.
+// 16-byte loads and stores.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -16,8 +18,8 @@ namespace moe {
 namespace {
 
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* Y,
-                                                      const int32_t* inv, int T,
-                                                      int K, int vpr, uint4* out) {
+                                                      const int32_t* inv, int y_by_inv,
+                                                      int T, int K, int vpr, uint4* out) {
     pdl_trigger();
     pdl_wait();
     const long long total = (long long)T * vpr;
@@ -33,17 +35,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* Y,
         // are in flight; the sum still runs in k order.
         for (int k0 = 0; k0 < K; k0 += 4) {
             uint4 v[4];
+            bool ok[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int k = k0 + j;
-                if (k < K) {
-                    const size_t row = inv ? (size_t)inv[(size_t)t * K + k] : (size_t)t * K + k;
-                    v[j] = Y[row * vpr + c];
+                ok[j] = k < K;
+                if (ok[j]) {
+                    const int r = inv ? inv[(size_t)t * K + k] : 0;
+                    ok[j] = r >= 0;  // a pair dropped by a capacity adds nothing
+                    const size_t row = y_by_inv ? (size_t)r : (size_t)t * K + k;
+                    if (ok[j]) v[j] = Y[row * vpr + c];
                 }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (k0 + j < K) {
+                if (ok[j]) {
                     a[0] += bf16_lo(v[j].x);
                     a[1] += bf16_hi(v[j].x);
                     a[2] += bf16_lo(v[j].y);
@@ -66,8 +72,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* Y,
 
 }  // namespace
 
-cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
-                           __nv_bfloat16* out, cudaStream_t st) {
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, bool y_by_inv, int T,
+                           int K, int H, __nv_bfloat16* out, cudaStream_t st) {
     const int vpr = H / 8;
     const long long total = (long long)T * vpr;
     long long blocks = (total + 255) / 256;
@@ -75,7 +81,7 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, in
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaError_t e = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                               reinterpret_cast<const uint4*>(Y), inv, T, K, vpr,
+                               reinterpret_cast<const uint4*>(Y), inv, (int)y_by_inv, T, K, vpr,
                                reinterpret_cast<uint4*>(out));
     count_launches(1);
     return e;

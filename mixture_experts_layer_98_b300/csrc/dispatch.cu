@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     const int32_t* chunk_counts, int32_t* chunk_base, int nchunks, int T,
     int E, int K, int32_t* counts, int32_t* offsets,
     RowTile* tiles, int32_t* n_tiles, int rows_per_tile,
-    const float* p_partial, int nrouter, float* aux) {
+    const float* p_partial, int nrouter, float* aux, int cap) {
     __shared__ int warp_tot[kScanThreads / 32];
     __shared__ float term_s[kMaxExperts];
     __shared__ float psum_s[4][kMaxExperts];
@@ -124,10 +124,12 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
         }
         counts[e] = run;
     }
-    const int nt = own ? (run + rows_per_tile - 1) / rows_per_tile : 0;
-    const int off_incl = block_inclusive_scan(own ? run : 0, warp_tot);
+    // with a capacity, an expert's rows are its first cap pairs (token order)
+    const int kept = (cap > 0 && run > cap) ? cap : run;
+    const int nt = own ? (kept + rows_per_tile - 1) / rows_per_tile : 0;
+    const int off_incl = block_inclusive_scan(own ? kept : 0, warp_tot);
     const int toff_incl = block_inclusive_scan(nt, warp_tot);
-    const int base = off_incl - (own ? run : 0);
+    const int base = off_incl - (own ? kept : 0);
     const int tbase = toff_incl - nt;
     if (own) {
         offsets[e] = base;
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
             RowTile tl;
             tl.expert = e;
             tl.row0 = base + j * rows_per_tile;
-            tl.nrows = min(rows_per_tile, run - j * rows_per_tile);
+            tl.nrows = min(rows_per_tile, kept - j * rows_per_tile);
             tl.pad = 0;
             tiles[tbase + j] = tl;
         }
@@ -163,22 +165,26 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
 
 constexpr int kScatterThreads = 1024;
 
-// Row of each pair: offsets[e] + chunk_base[c,e] + (tokens of this chunk
-// before t that chose e), the last from per-expert token bitmaps.  One CTA per
-// chunk; its threads walk the chunk's pairs (token-major), so each thread
-// handles about K / 4 pairs.
+// Rank of each pair within its expert: chunk_base[c,e] + (tokens of this
+// chunk before t that chose e), the last from per-expert token bitmaps; its
+// row is offsets[e] + rank, or, with a capacity cap > 0 and rank >= cap, none
+// (inv = -1: the pair is dropped).  One CTA per chunk; its threads walk the
+// chunk's pairs (token-major), so each thread handles about K / 4 pairs.
 __global__ void __launch_bounds__(kScatterThreads) dispatch_scatter_kernel(
     const int32_t* idx, const float* w, int T, int E, int K,
     const int32_t* offsets, const int32_t* chunk_base,
     int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
-    float* w_perm) {
+    float* w_perm, int cap) {
     __shared__ uint32_t sel[kMaxExperts * kWords];
     __shared__ int base_s[kMaxExperts];
+    __shared__ int cb_s[kMaxExperts];
     pdl_trigger();
     for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) sel[i] = 0u;
     pdl_wait();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        base_s[e] = offsets[e] + chunk_base[(size_t)blockIdx.x * E + e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        base_s[e] = offsets[e];
+        cb_s[e] = chunk_base[(size_t)blockIdx.x * E + e];
+    }
     __syncthreads();
     const int t0 = blockIdx.x * kChunkTokens;
     const int npairs = min(kChunkTokens, T - t0) * K;
@@ -192,10 +198,14 @@ __global__ void __launch_bounds__(kScatterThreads) dispatch_scatter_kernel(
         const int tl = i / K, k = i - tl * K, word = tl >> 5, bit = tl & 31;
         const int e = cidx[i];
         const uint32_t* sb = sel + e * kWords;
-        int rank = __popc(sb[word] & ((1u << bit) - 1u));
+        int rank = cb_s[e] + __popc(sb[word] & ((1u << bit) - 1u));
         for (int j = 0; j < word; ++j) rank += __popc(sb[j]);
-        const int row = base_s[e] + rank;
         const int t = t0 + tl;
+        if (cap > 0 && rank >= cap) {
+            inv[(size_t)t * K + k] = -1;
+            continue;
+        }
+        const int row = base_s[e] + rank;
         perm_tok[row] = t;
         if (perm_slot) perm_slot[row] = k;
         inv[(size_t)t * K + k] = row;
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     int rows_per_tile,
     int32_t* counts, int32_t* offsets, RowTile* tiles, int32_t* n_tiles, int32_t* perm_tok,
     int32_t* perm_slot, int32_t* inv, float* w_perm, float* aux, const uint4* x,
-    uint4* x_perm, int vec_per_row) {
+    uint4* x_perm, int vec_per_row, int cap) {
     // ROUTE: probability rows [T][E]; otherwise [4][kMaxExperts] partial sums
     __shared__ float prob_s[kRouteDispatchTokens * kMaxExperts];
     constexpr int kR = ROUTE ? kRouteDispatchTokens * kMaxTopK : 1;
@@ -236,6 +246,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     __shared__ int base_s[kMaxExperts];
     __shared__ float term_s[kMaxExperts];
     __shared__ int warp_tot[kSmallThreads / 32];
+    __shared__ int kept_total_s;
     pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < E * kW; i += blockDim.x) sel[i] = 0u;
@@ -289,10 +300,11 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     const int e = tid;
     const bool own = e < E;
     const int run = own ? cnt[e] : 0;
-    const int nt = own ? (run + rows_per_tile - 1) / rows_per_tile : 0;
-    const int off_incl = block_inclusive_scan(run, warp_tot);
+    const int kept = (cap > 0 && run > cap) ? cap : run;  // first cap pairs in token order
+    const int nt = own ? (kept + rows_per_tile - 1) / rows_per_tile : 0;
+    const int off_incl = block_inclusive_scan(kept, warp_tot);
     const int toff_incl = block_inclusive_scan(nt, warp_tot);
-    const int base = off_incl - run;
+    const int base = off_incl - kept;
     const int tbase = toff_incl - nt;
     if (own) {
         counts[e] = run;
@@ -301,12 +313,13 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         if (e == E - 1) {
             offsets[E] = off_incl;
             *n_tiles = toff_incl;
+            kept_total_s = off_incl;
         }
         for (int j = 0; j < nt; ++j) {
             RowTile tl;
             tl.expert = e;
             tl.row0 = base + j * rows_per_tile;
-            tl.nrows = min(rows_per_tile, run - j * rows_per_tile);
+            tl.nrows = min(rows_per_tile, kept - j * rows_per_tile);
             tl.pad = 0;
             tiles[tbase + j] = tl;
         }
@@ -337,6 +350,10 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         const uint32_t* sb = sel + ex * kW;
         int rank = __popc(sb[word] & ((1u << bit) - 1u));
         for (int j = 0; j < word; ++j) rank += __popc(sb[j]);
+        if (cap > 0 && rank >= cap) {  // dropped
+            inv[i] = -1;
+            continue;
+        }
         const int row = base_s[ex] + rank;
         perm_tok[row] = t;
         if (perm_slot) perm_slot[row] = k;
@@ -351,7 +368,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         __syncthreads();
         // four vectors loaded before any is stored (the stores may alias the
         // loads as far as the compiler knows)
-        const int n = P * vec_per_row;
+        const int n = kept_total_s * vec_per_row;
         for (int v0 = tid; v0 < n; v0 += 4 * blockDim.x) {
             uint4 v[4];
 #pragma unroll
@@ -380,10 +397,12 @@ constexpr int kGatherVec = 8;
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
                                                           const int32_t* perm_tok,
-                                                          long long P, int vec_per_row,
-                                                          uint4* x_perm) {
+                                                          const int32_t* n_rows_p, long long P,
+                                                          int vec_per_row, uint4* x_perm) {
     pdl_trigger();
     pdl_wait();
+    // the dispatch's row count (below P when a capacity dropped pairs)
+    if (*n_rows_p < P) P = *n_rows_p;
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -418,8 +437,9 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const Sizes& s, const Workspac
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                               reinterpret_cast<const uint4*>(x), (const int32_t*)ws.perm_tok, P,
-                               s.H / 8, reinterpret_cast<uint4*>(ws.x_perm));
+                               reinterpret_cast<const uint4*>(x), (const int32_t*)ws.perm_tok,
+                               (const int32_t*)(ws.offsets + s.E), P, s.H / 8,
+                               reinterpret_cast<uint4*>(ws.x_perm));
     count_launches(1);
     return e;
 }
@@ -428,14 +448,14 @@ template <int EPL>
 cudaError_t launch_small(const float* parts, int nparts, float* logits_out, int norm,
                          const float* bias, int32_t* idx, float* w, const Sizes& s,
                          const Workspace& ws, int rows_per_tile, float* aux,
-                         const __nv_bfloat16* x, cudaStream_t st) {
+                         const __nv_bfloat16* x, int cap, cudaStream_t st) {
     cudaError_t e = launch_pdl(dispatch_small_kernel<EPL, true>, dim3(1), dim3(kSmallThreads), 0,
                                st, parts, nparts, logits_out, norm, bias, idx, w,
                                (const float*)nullptr,
                                0, s.T, s.E, s.K, rows_per_tile, ws.counts, ws.offsets, ws.tiles,
                                ws.n_tiles, ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm, aux,
                                reinterpret_cast<const uint4*>(x),
-                               reinterpret_cast<uint4*>(ws.x_perm), s.H / 8);
+                               reinterpret_cast<uint4*>(ws.x_perm), s.H / 8, cap);
     count_launches(1);
     return e;
 }
@@ -444,7 +464,8 @@ cudaError_t launch_small(const float* parts, int nparts, float* logits_out, int 
 
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
-                            const float* p_partial, int n_partials, float* aux, cudaStream_t st) {
+                            const float* p_partial, int n_partials, float* aux, int cap,
+                            cudaStream_t st) {
     const int nch = s.nchunks();
     cudaError_t e;
     if (nch == 1) {
@@ -454,7 +475,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
                        const_cast<float*>(w), p_partial, n_partials, s.T, s.E, s.K,
                        rows_per_tile, ws.counts, ws.offsets, ws.tiles, ws.n_tiles, ws.perm_tok,
                        ws.perm_slot, ws.inv, ws.w_perm, aux, (const uint4*)nullptr,
-                       (uint4*)nullptr, 0);
+                       (uint4*)nullptr, 0, cap);
         count_launches(1);
     } else {
         e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kChunkTokens), 0, st, idx, s.T, s.E,
@@ -462,11 +483,11 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloa
         if (e != cudaSuccess) return e;
         e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, st,
             ws.chunk_counts, ws.chunk_base, nch, s.T, s.E, s.K, ws.counts, ws.offsets, ws.tiles,
-            ws.n_tiles, rows_per_tile, p_partial, n_partials, aux);
+            ws.n_tiles, rows_per_tile, p_partial, n_partials, aux, cap);
         if (e != cudaSuccess) return e;
         e = launch_pdl(dispatch_scatter_kernel, dim3(nch), dim3(kScatterThreads), 0, st, idx, w,
                        s.T, s.E, s.K, (const int32_t*)ws.offsets, (const int32_t*)ws.chunk_base,
-                       ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm);
+                       ws.perm_tok, ws.perm_slot, ws.inv, ws.w_perm, cap);
         count_launches(3);
     }
     if (e != cudaSuccess) return e;
@@ -477,7 +498,7 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
                                         int norm, const float* bias, int32_t* idx, float* w,
                                         const __nv_bfloat16* x, const Sizes& s,
                                         const Workspace& ws, int rows_per_tile, float* aux,
-                                        cudaStream_t st) {
+                                        int cap, cudaStream_t st) {
     if (s.T > kRouteDispatchTokens) return cudaErrorInvalidValue;
     // Up to 128 KB of gathered rows are copied by the routing CTA itself (one
     // or two decode tokens); more go to the gather kernel, which spreads them
@@ -486,10 +507,10 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
     const __nv_bfloat16* xk = in_cta ? x : nullptr;
     const int epl = (s.E + 31) / 32;
     cudaError_t e;
-    if (epl <= 1) e = launch_small<1>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else if (epl <= 2) e = launch_small<2>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else if (epl <= 4) e = launch_small<4>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
-    else e = launch_small<8>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, st);
+    if (epl <= 1) e = launch_small<1>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, cap, st);
+    else if (epl <= 2) e = launch_small<2>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, cap, st);
+    else if (epl <= 4) e = launch_small<4>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, cap, st);
+    else e = launch_small<8>(parts, nparts, logits_out, norm, bias, idx, w, s, ws, rows_per_tile, aux, xk, cap, st);
     if (e != cudaSuccess) return e;
     return x && !in_cta ? launch_gather(x, s, ws, st) : cudaSuccess;
 }

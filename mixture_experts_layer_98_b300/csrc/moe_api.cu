@@ -8,6 +8,7 @@
 //
 // No host synchronisation: the expert kernels read the tile count on the device.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <unordered_map>
 
@@ -220,8 +221,9 @@ static ExpertPath expert_path(const Sizes& s, bool packed) {
 
 // The kernel sequence.  All pointers checked by the caller.
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
-                const Sizes& s, int norm, const float* bias, __nv_bfloat16* out, float* logits,
-                int32_t* idx, float* w, float* aux, const Workspace& ws, cudaStream_t st) {
+                const Sizes& s, int norm, const float* bias, int cap, __nv_bfloat16* out,
+                float* logits, int32_t* idx, float* w, float* aux, const Workspace& ws,
+                cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
     const ExpertPath path = expert_path(s, W.packed != nullptr);
@@ -253,22 +255,23 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                                          ws.p_partial, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
-        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, st);
+        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, cap,
+                            st);
     } else if (s.T <= kRouteDispatchTokens) {
         const int nsplit = router_simt_splits(s);
         e = launch_router_logits(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
         e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, bias, idx, w,
-                                        gather_x, s,
-                                        ws, tile_rows, aux, st);
+                                        gather_x, s, ws, tile_rows, aux, cap, st);
     } else {
         e = launch_router(x, Wr, s, norm, bias, logits, ws.logit_parts, idx, w, ws.p_partial,
                           ws.status,
                           ws.n_clear, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
-        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, st);
+        e = launch_dispatch(idx, w, gather_x, s, ws, tile_rows, ws.p_partial, n_partials, aux, cap,
+                            st);
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
@@ -280,7 +283,8 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
-    e = launch_combine(ws.ybuf, nullptr, s.T, s.K, s.H, out, st);  // Y is token-major
+    // Y is token-major; with a capacity, inv marks the dropped pairs
+    e = launch_combine(ws.ybuf, cap > 0 ? ws.inv : nullptr, false, s.T, s.K, s.H, out, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(5, st);
     if (g_timing) g_timed_once = true;
@@ -311,7 +315,7 @@ using namespace moe;
 // workspace == NULL), kernel sequence.  wg/wu/wd are only null-checked.
 static int forward_device(const void* x, int T, int H, const void* W_router,
                           const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
-                          int E, int K, int I, int norm, const float* bias, void* out,
+                          int E, int K, int I, int norm, const float* bias, int cap, void* out,
                           float* logits, int32_t* idx, float* w, float* aux, void* workspace,
                           size_t workspace_bytes, cudaStream_t st) {
     int rc = check_forward_args(x, T, H, W_router, wg, wu, wd, E, K, I, out, logits, idx, w, aux);
@@ -334,7 +338,7 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
     Workspace ws;
     layout_workspace(s, (char*)workspace, &ws);
     rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s, norm, bias,
-                     (__nv_bfloat16*)out, logits, idx, w, aux, ws, st);
+                     cap, (__nv_bfloat16*)out, logits, idx, w, aux, ws, st);
     if (rc == MOE_OK && owned) remember_counts(st, ws, E);
     return rc;
 }
@@ -344,9 +348,9 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
 // copied back, and the call returns after the stream has finished them.
 static int forward_host(const void* x_host, int T, int H, const void* W_router,
                         const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
-                        int E, int K, int I, int norm, const float* bias, void* out_host,
-                        float* logits_host, int32_t* idx_host, float* w_host, float* aux_host,
-                        cudaStream_t st) {
+                        int E, int K, int I, int norm, const float* bias, int cap,
+                        void* out_host, float* logits_host, int32_t* idx_host, float* w_host,
+                        float* aux_host, cudaStream_t st) {
     int rc = check_sizes(T, H, E, K, I);
     if (rc) return rc;
     if (!W_router || !wg || !wu || !wd) return MOE_ERR_INVALID_ARG;
@@ -383,7 +387,7 @@ static int forward_host(const void* x_host, int T, int H, const void* W_router,
     float* aux_d = (float*)p;
     cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_status(e);
-    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, bias, out_d,
+    rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, bias, cap, out_d,
                      logits_host ? logits_d : nullptr, idx_d, w_d, aux_host ? aux_d : nullptr, ws,
                      st);
     if (rc) return rc;
@@ -477,7 +481,7 @@ int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                          nullptr, out, router_logits, topk_idx, topk_w, aux, workspace,
+                          nullptr, 0, out, router_logits, topk_idx, topk_w, aux, workspace,
                           workspace_bytes, (cudaStream_t)stream);
 }
 
@@ -488,7 +492,7 @@ int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router, const
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                          nullptr, out, router_logits, topk_idx, topk_w, aux, nullptr, 0,
+                          nullptr, 0, out, router_logits, topk_idx, topk_w, aux, nullptr, 0,
                           (cudaStream_t)stream);
 }
 
@@ -521,8 +525,8 @@ int moe_forward_packed(const moe_bf16* x, int T, int H, const moe_bf16* W_router
     if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
     const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
     return forward_device(x, T, H, W_router, W, packed_experts, packed_experts, packed_experts,
-                          E, K, I, norm_topk_prob, nullptr, out, router_logits, topk_idx, topk_w,
-                          aux, workspace, workspace_bytes, (cudaStream_t)stream);
+                          E, K, I, norm_topk_prob, nullptr, 0, out, router_logits, topk_idx,
+                          topk_w, aux, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
@@ -532,20 +536,25 @@ int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                      void* stream) {
     const moe_forward_options none{};
     const moe_forward_options& o = opts ? *opts : none;
+    if (!(o.capacity_factor >= 0.f) || o.capacity_factor > 1e6f) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || T < 0 || K < 1) return MOE_ERR_INVALID_ARG;
+    // capacity in pairs: ceil(cf * T * K / E); 0 = none
+    const double cf_pairs = (double)o.capacity_factor * T * K / E;
+    const int cap = o.capacity_factor > 0.f ? (int)(cf_pairs < 1.0 ? 1.0 : std::ceil(cf_pairs)) : 0;
     if (o.packed_experts) {
         if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
         if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
         const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)o.packed_experts};
         return forward_device(x, T, H, W_router, W, o.packed_experts, o.packed_experts,
-                              o.packed_experts, E, K, I, norm_topk_prob, o.expert_bias, out,
+                              o.packed_experts, E, K, I, norm_topk_prob, o.expert_bias, cap, out,
                               router_logits, topk_idx, topk_w, aux, o.workspace,
                               o.workspace_bytes, (cudaStream_t)stream);
     }
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_device(x, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                          o.expert_bias, out, router_logits, topk_idx, topk_w, aux, o.workspace,
-                          o.workspace_bytes, (cudaStream_t)stream);
+                          o.expert_bias, cap, out, router_logits, topk_idx, topk_w, aux,
+                          o.workspace, o.workspace_bytes, (cudaStream_t)stream);
 }
 
 int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
@@ -556,7 +565,7 @@ int moe_forward_host(const moe_bf16* x_host, int T, int H, const moe_bf16* W_rou
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return forward_host(x_host, T, H, W_router, W, W_gate, W_up, W_down, E, K, I, norm_topk_prob,
-                        nullptr, out_host, router_logits_host, topk_idx_host, topk_w_host,
+                        nullptr, 0, out_host, router_logits_host, topk_idx_host, topk_w_host,
                         aux_host, (cudaStream_t)stream);
 }
 
@@ -569,7 +578,7 @@ int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16
     if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;
     const ExpertWeights W{nullptr, nullptr, nullptr, (const char*)packed_experts};
     return forward_host(x_host, T, H, W_router, W, packed_experts, packed_experts,
-                        packed_experts, E, K, I, norm_topk_prob, nullptr, out_host,
+                        packed_experts, E, K, I, norm_topk_prob, nullptr, 0, out_host,
                         router_logits_host, topk_idx_host, topk_w_host, aux_host,
                         (cudaStream_t)stream);
 }
@@ -630,7 +639,7 @@ int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm
                                                 (cudaStream_t)stream));
 }
 
-int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* counts,
+int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int capacity, int32_t* counts,
                     int32_t* offsets, int32_t* perm_tok, int32_t* perm_slot, int32_t* inv,
                     void* stream) {
     if (T < 0 || E < 1 || E > kMaxExperts || K < 1 || K > E || K > kMaxTopK)
@@ -672,7 +681,8 @@ int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int32_t* count
     ws.inv = inv;
     ws.w_perm = nullptr;
     return cuda_status(
-        launch_dispatch(topk_idx, nullptr, nullptr, s, ws, kStreamRows, nullptr, 0, nullptr, st));
+        launch_dispatch(topk_idx, nullptr, nullptr, s, ws, kStreamRows, nullptr, 0, nullptr,
+                        capacity > 0 ? capacity : 0, st));
 }
 
 int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H, moe_bf16* out,
@@ -683,7 +693,8 @@ int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H, 
     int rc = check_device();
     if (rc) return rc;
     if (T == 0) return MOE_OK;
-    return cuda_status(launch_combine((const __nv_bfloat16*)Y, inv, T, K, H, (__nv_bfloat16*)out,
+    return cuda_status(launch_combine((const __nv_bfloat16*)Y, inv, true, T, K, H,
+                                      (__nv_bfloat16*)out,
                                       (cudaStream_t)stream));
 }
 

@@ -134,9 +134,12 @@ cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logi
                                      float* w, float* p_partial, cudaStream_t st);
 // p_partial holds n_partials rows of per-expert probability sums (for aux).
 // x != null: also gather x_perm[row] = x[perm_tok[row]].
+// cap > 0: each expert keeps its first cap pairs (token order); the others
+// get inv = -1 and no row.  counts stay the routed pairs; offsets[E] = rows.
 cudaError_t launch_dispatch(const int32_t* idx, const float* w, const __nv_bfloat16* x,
                             const Sizes& s, const Workspace& ws, int rows_per_tile,
-                            const float* p_partial, int n_partials, float* aux, cudaStream_t st);
+                            const float* p_partial, int n_partials, float* aux, int cap,
+                            cudaStream_t st);
 // Batches of at most kRouteDispatchTokens tokens: routing (softmax, top-k,
 // renorm from nparts partial logits) and the whole dispatch (counts, offsets,
 // tile table, aux, permutation; gather when x != null) in one CTA, then the
@@ -146,7 +149,7 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
                                         int norm, const float* bias, int32_t* idx, float* w,
                                         const __nv_bfloat16* x, const Sizes& s,
                                         const Workspace& ws, int rows_per_tile, float* aux,
-                                        cudaStream_t st);
+                                        int cap, cudaStream_t st);
 // ev_mid (may be null) is recorded between the gate/up and the down launch.
 // The streaming kernels stage their input rows from x through ws.perm_tok;
 // the tcgen05 kernels read the gathered rows from ws.x_perm.
@@ -173,10 +176,12 @@ struct WtPlan {
 WtPlan wt_plan(const Sizes& s);
 cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
-// out[t] = sum over k of Y row t*K + k (inv == null: Y token-major, as the
-// expert kernels store it) or of Y row inv[t*K + k] (Y in dispatch order).
-cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, int T, int K, int H,
-                           __nv_bfloat16* out, cudaStream_t st);
+// out[t] = sum over k of Y row t*K + k (Y token-major, as the expert kernels
+// store it), skipping the pairs with inv[t*K + k] < 0 when inv != null
+// (dropped by a capacity); with y_by_inv, Y is in dispatch order and row
+// inv[t*K + k] is read instead.
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, bool y_by_inv, int T,
+                           int K, int H, __nv_bfloat16* out, cudaStream_t st);
 
 int num_sms();  // of the current device (cached)
 
@@ -198,9 +203,11 @@ int cuda_status(cudaError_t e);
 int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
                        const void* Wu, const void* Wd, int E, int K, int I, const void* out,
                        const void* logits, const void* idx, const void* w, const void* aux);
+// cap: expert capacity in pairs (0: none).
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
-                const Sizes& s, int norm, const float* bias, __nv_bfloat16* out, float* logits,
-                int32_t* idx, float* w, float* aux, const Workspace& ws, cudaStream_t st);
+                const Sizes& s, int norm, const float* bias, int cap, __nv_bfloat16* out,
+                float* logits, int32_t* idx, float* w, float* aux, const Workspace& ws,
+                cudaStream_t st);
 
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);

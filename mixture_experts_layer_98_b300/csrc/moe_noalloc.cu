@@ -83,6 +83,6 @@ extern "C" int moe_forward_noalloc(const moe_bf16* x, int T, int H, const moe_bf
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s,
-                       norm_topk_prob, nullptr, (__nv_bfloat16*)out, router_logits, topk_idx, topk_w, aux,
+                       norm_topk_prob, nullptr, 0, (__nv_bfloat16*)out, router_logits, topk_idx, topk_w, aux,
                        ws, st);
 }

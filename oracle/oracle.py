@@ -273,9 +273,11 @@ def near_tie_tokens(probs, K, gap=1e-6):
 
 
 def capacity_of(cf, T, K, E):
-    """Pairs each expert keeps for capacity factor cf: ceil(cf·T·K/E) (0: no limit)."""
-    if not cf or cf <= 0:
+    """Pairs each expert keeps for capacity factor cf: ceil(cf·T·K/E), at least 1
+    (0: no limit).  cf is taken as the fp32 value a caller passes."""
+    cf = float(np.float32(cf))
+    if cf <= 0:
         return 0
     import math
-    return int(math.ceil(cf * T * K / E))
+    return max(1, int(math.ceil(cf * T * K / E)))
 

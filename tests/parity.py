@@ -73,14 +73,15 @@ def near_tie_keys(keys, K, rel):
     return np.where((d < rel * (1 + np.abs(k[:, 1:]))).any(axis=1))[0]
 
 
-def compare(b, g, K, norm, rows=None, bias=None):
+def compare(b, g, K, norm, rows=None, bias=None, capacity=0):
     """b: host bits of the inputs; g: GPU results; bias: the selection-only
-    expert bias (float32 [E]) when the forward had one.  Returns a report dict
-    and raises AssertionError on any failed check."""
+    expert bias (float32 [E]) when the forward had one; capacity: the pairs
+    each expert kept (0: no capacity).  Returns a report dict and raises
+    AssertionError on any failed check."""
     T, H = b["x"].shape
     E = b["W_router"].shape[0]
     o = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], K, norm,
-                           rows=rows, bias=bias)
+                           rows=rows, bias=bias, capacity=capacity)
     rep = {}
     # logits
     dl = np.abs(g["logits"].astype(np.float64) - o["logits"])
@@ -115,8 +116,16 @@ def compare(b, g, K, norm, rows=None, bias=None):
     rows_arr = np.arange(T) if rows is None else np.asarray(rows)
     if rows_arr.size:
         ref = o["out_f64"].copy()
+        if capacity and mism.size:
+            # a different selection (at a near-tie) shifts which later pairs an
+            # expert keeps: evaluate every checked row on the GPU's own selection
+            keep = oracle.keep_mask(g["idx"], E, capacity)
+            for j, t in enumerate(rows_arr.tolist()):
+                ref[j] = oracle.token_output(b["x"][t], g["idx"][t][keep[t]], g["w"][t][keep[t]],
+                                             b["W_gate"], b["W_up"], b["W_down"],
+                                             unrounded=True)[1]
         for j, t in enumerate(rows_arr.tolist()):
-            if t in mism:
+            if t in mism and not capacity:
                 ref[j] = oracle.token_output(b["x"][t], g["idx"][t], g["w"][t], b["W_gate"],
                                              b["W_up"], b["W_down"], unrounded=True)[1]
         got = bf16_to_f64(g["out"][rows_arr])

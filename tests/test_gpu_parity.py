@@ -87,6 +87,23 @@ def test_permute_bit_exact(moe, T, E, K):
         assert np.array_equal(d["inv"].cpu().numpy(), r["inv"])
 
 
+@pytest.mark.parametrize("T,E,K,C", [(200, 16, 4, 30), (200, 16, 4, 1), (1000, 128, 8, 40),
+                                     (3000, 16, 2, 300), (257, 8, 2, 64)])
+def test_permute_with_capacity_bit_exact(moe, T, E, K, C):
+    # one-CTA dispatch (T <= 256) and chunked dispatch; capacities that drop
+    # most pairs, some pairs, and (C = 300 at ~375 per expert) a few
+    rng = np.random.default_rng(T + C)
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)], np.int32).reshape(T, K)
+    d = moe.moe_dbg_permute(torch.from_numpy(idx).cuda(), E, capacity=C)
+    r = oracle.dispatch(idx, E, capacity=C)
+    n = int(r["offsets"][E])
+    assert np.array_equal(d["counts"].cpu().numpy(), r["counts"])
+    assert np.array_equal(d["offsets"].cpu().numpy(), r["offsets"])
+    assert np.array_equal(d["inv"].cpu().numpy(), r["inv"])
+    assert np.array_equal(d["perm_tok"].cpu().numpy()[:n], r["perm_tok"])
+    assert np.array_equal(d["perm_slot"].cpu().numpy()[:n], r["perm_slot"])
+
+
 def test_permute_skewed_all_to_one_expert(moe):
     T, E, K = 3000, 16, 2
     idx = np.zeros((T, K), np.int32)
@@ -258,6 +275,38 @@ def test_forward_with_selection_bias(moe, name, T):
                             inp["W_down"], cfg.K, cfg.norm)
     torch.cuda.synchronize()
     assert not torch.equal(plain[2], idx), rep
+
+
+@pytest.mark.parametrize("name,cf,sample", [("tiny", 1.0, None), ("decode_t4", 1.0, None),
+                                            ("decode_t64", 1.0, None),
+                                            ("prefill_h2048", 1.0, 64), ("skew", 1.25, 48)])
+def test_forward_with_capacity(moe, name, cf, sample):
+    cfg = mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, "cuda")
+    C = oracle.capacity_of(cf, cfg.T, cfg.K, cfg.E)
+    out, lg, idx, w, aux = moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"],
+                                                inp["W_up"], inp["W_down"], cfg.K, cfg.norm,
+                                                capacity_factor=cf)
+    torch.cuda.synchronize()
+    g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
+             w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
+    keep = oracle.keep_mask(g["idx"], cfg.E, C)
+    assert not keep.all()  # the capacity drops pairs at this size
+    rows = None if sample is None else mi.sample_rows(cfg.T, sample)
+    compare(host_bits(inp), g, cfg.K, cfg.norm, rows=rows, capacity=C)
+
+
+def test_capacity_nobody_reaches_is_the_plain_forward(moe):
+    cfg = mi.CONFIGS["decode_t16"]
+    inp = mi.make_inputs(cfg, "cuda")
+    ref = [t.clone() for t in moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
+                                              inp["W_up"], inp["W_down"], cfg.K, cfg.norm)]
+    got = moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"],
+                               inp["W_down"], cfg.K, cfg.norm,
+                               capacity_factor=float(cfg.E))  # C = T·K >= any expert's load
+    torch.cuda.synchronize()
+    for u, v in zip(ref, got):
+        assert torch.equal(u, v)
 
 
 def test_zero_selection_bias_is_the_plain_forward(moe):
