@@ -314,6 +314,14 @@ int moe_dbg_route_from_logits(const float* logits, int T, int E, int K, int norm
                               const float* expert_bias, int32_t* topk_idx, float* topk_w,
                               void* stream);
 
+/* Self-test of the bounded device-side waits (no counterpart on the pages):
+ * one thread waits, for at most timeout_ns (1 ns .. 1 s), on an mbarrier that
+ * nothing arrives on, then writes MOE_ERR_TIMEOUT to *status (device int32).
+ * The same limit-and-record path ends every wait of the forward's kernels;
+ * the context stays usable afterwards.  MOE_ERR_INVALID_ARG for a limit out
+ * of range or a NULL status. */
+int moe_dbg_wait_timeout(long long timeout_ns, int32_t* status, void* stream);
+
 /* Dispatch of given selections topk_idx [T,K] (each row holds K distinct
  * experts in [0,E)): counts [E], offsets [E+1] (exclusive prefix sum),
  * perm_tok / perm_slot [T·K] (token and k-slot of each row, rows ordered by

@@ -30,7 +30,7 @@ EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_for
            "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
            "moe_stage_times",
            "moe_kernel_launch_count", "moe_dbg_route_from_logits", "moe_dbg_permute",
-           "moe_dbg_combine"]
+           "moe_dbg_combine", "moe_dbg_wait_timeout"]
 MOE_NUM_STAGES = 5
 STAGE_NAMES = ["router", "dispatch", "gate_up", "down", "combine"]
 
@@ -91,6 +91,7 @@ def lib():
         L.moe_dbg_route_from_logits.argtypes = [P, i, i, i, i, P, P, P, P]
         L.moe_dbg_permute.argtypes = [P, i, i, i, i, P, P, P, P, P, P]
         L.moe_dbg_combine.argtypes = [P, P, i, i, i, P, P]
+        L.moe_dbg_wait_timeout.argtypes = [ctypes.c_longlong, P, P]
         _lib = L
     return _lib
 
@@ -381,3 +382,12 @@ def moe_dbg_combine(Y, inv, stream=None):
     _call(lib().moe_dbg_combine(_ptr(Y), _ptr(inv), T, K, H, _ptr(out), _stream(stream)),
           "moe_dbg_combine")
     return out
+
+
+def moe_dbg_wait_timeout(timeout_ns, stream=None):
+    """Runs the bounded-wait self-test; returns the device status word it wrote."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _call(lib().moe_dbg_wait_timeout(int(timeout_ns), _ptr(st), _stream(stream)),
+          "moe_dbg_wait_timeout")
+    return int(st.cpu()[0])
+
