@@ -46,8 +46,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 STAGE_SOURCES = {
     "router": ["router.cu", "moe_common.cuh"],
     "dispatch": ["dispatch.cu", "moe_common.cuh"],
-    "gate_up": ["experts_tc.cu", "experts_wt.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
-    "down": ["experts_tc.cu", "experts_wt.cu", "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
+    "gate_up": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_stream.cu",
+                "sm100_ptx.cuh", "moe_common.cuh"],
+    "down": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_stream.cu",
+             "sm100_ptx.cuh", "moe_common.cuh"],
     "combine": ["combine.cu", "moe_common.cuh"],
 }
 
@@ -71,7 +73,8 @@ def parse(argv=None):
     ap.add_argument("--weights", default="packed", choices=["packed", "row-major"],
                     help="expert weights packed once into the tile-major layout before timing "
                          "(moe_pack_experts, a model-load step), or read row-major")
-    ap.add_argument("--expert-path", default="auto", choices=["auto", "streaming", "tcgen05", "tcgen05_wt"],
+    ap.add_argument("--expert-path", default="auto",
+                    choices=["auto", "streaming", "tcgen05", "tcgen05_wt", "tcgen05_pair"],
                     help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args(argv)
 
@@ -332,7 +335,8 @@ def run_ours(args, world, rank, local):
     aux = torch.empty((1,), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3}[args.expert_path])
+    moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3,
+                             "tcgen05_pair": 4}[args.expert_path])
 
     packed = None
     if args.weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
@@ -496,13 +500,16 @@ def run_ours(args, world, rank, local):
 
 def expert_path_name(flag, cfg):
     """Which expert kernels the library runs for this flag and shape."""
-    wt_ok = cfg.I % 128 == 0 and cfg.H % 256 == 0
+    wt_ok = cfg.I % 128 == 0 and cfg.H % 256 == 0  # also the CTA-pair kernels' condition
     if flag == "auto":
         if cfg.T * cfg.K >= 32 * cfg.E:
-            return "tcgen05"
+            pair = wt_ok and cfg.E <= 32 and cfg.T * cfg.K >= 1024 * cfg.E
+            return "tcgen05_pair" if pair else "tcgen05"
         return "tcgen05_wt" if wt_ok else "streaming"
     if flag == "tcgen05_wt" and not wt_ok:
         return "streaming"
+    if flag == "tcgen05_pair" and not wt_ok:
+        return "tcgen05"
     return flag
 
 

@@ -252,11 +252,17 @@ int moe_last_cuda_error(void);
 /* Kernel-path selection for the expert MLPs (process-wide):
  *   MOE_PATH_AUTO         tcgen05 grouped GEMMs with token rows on the MMA's
  *                         M side when the average expert receives >= 32 rows
- *                         (P >= 32*E); below that the tcgen05 kernels with the
- *                         expert weights on the M side, or, for shapes those
- *                         cannot tile, the weight-streaming kernels;
+ *                         (P >= 32*E) -- on CTA pairs (256-row tiles) when
+ *                         E <= 32 experts average >= 1024 rows and
+ *                         I % 128 == 0, H % 256 == 0, else on single CTAs
+ *                         (128-row tiles); below that the tcgen05 kernels with
+ *                         the expert weights on the M side, or, for shapes
+ *                         those cannot tile, the weight-streaming kernels;
  *   MOE_PATH_STREAMING    always the weight-streaming CUDA-core kernels;
- *   MOE_PATH_TCGEN05      always the token-rows-as-M tcgen05 grouped GEMMs;
+ *   MOE_PATH_TCGEN05      always the single-CTA token-rows-as-M tcgen05
+ *                         grouped GEMMs;
+ *   MOE_PATH_TCGEN05_PAIR always the CTA-pair token-rows-as-M grouped GEMMs
+ *                         where the shape allows, else MOE_PATH_TCGEN05;
  *   MOE_PATH_TCGEN05_WT   always the weights-as-M tcgen05 kernels where the
  *                         shape allows (I % 128 == 0 and H % 256 == 0), else
  *                         the weight-streaming kernels.
@@ -267,7 +273,8 @@ enum moe_path {
     MOE_PATH_AUTO = 0,
     MOE_PATH_STREAMING = 1,
     MOE_PATH_TCGEN05 = 2,
-    MOE_PATH_TCGEN05_WT = 3
+    MOE_PATH_TCGEN05_WT = 3,
+    MOE_PATH_TCGEN05_PAIR = 4
 };
 int moe_set_expert_path(int path);
 

@@ -200,7 +200,7 @@ static void remember_counts(cudaStream_t st, const Workspace& ws, int E) {
     w.E = E;
 }
 
-enum class ExpertPath { kStreaming, kTokensM, kWeightsM };
+enum class ExpertPath { kStreaming, kTokensM, kTokensPair, kWeightsM };
 
 static ExpertPath expert_path(const Sizes& s, bool packed) {
     const bool wt_ok = experts_wt_supported(s);
@@ -211,11 +211,21 @@ static ExpertPath expert_path(const Sizes& s, bool packed) {
         case MOE_PATH_STREAMING: return packed ? ExpertPath::kWeightsM : ExpertPath::kStreaming;
         case MOE_PATH_TCGEN05: return ExpertPath::kTokensM;
         case MOE_PATH_TCGEN05_WT: return small;
+        case MOE_PATH_TCGEN05_PAIR:
+            return experts_pair_supported(s) ? ExpertPath::kTokensPair : ExpertPath::kTokensM;
         default: break;
     }
     // Token rows fill 128-row tiles from ~32 rows per expert on average up;
     // below that the weights go on the MMA's M side (every stage is weights).
-    if (s.P() >= 32LL * s.E) return ExpertPath::kTokensM;
+    // CTA pairs (256-row tiles) where few experts each receive >= 1024 rows:
+    // there an expert's ragged last tile adds little padding (measured faster
+    // at E=8, 1024 rows per expert); with 128 experts of 256-1024 rows the
+    // single-CTA tiles (128 rows, 64-row tails) pad less and measured faster.
+    if (s.P() >= 32LL * s.E) {
+        if (experts_pair_supported(s) && s.E <= 32 && s.P() >= 1024LL * s.E)
+            return ExpertPath::kTokensPair;
+        return ExpertPath::kTokensM;
+    }
     return small;
 }
 
@@ -235,9 +245,10 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         return MOE_ERR_INVALID_ARG;
     begin_marks();
     mark(0, st);
-    const int tile_rows = path == ExpertPath::kTokensM   ? kTcRows
-                          : path == ExpertPath::kWeightsM ? kWtRows
-                                                          : kStreamRows;
+    const int tile_rows = path == ExpertPath::kTokensM      ? kTcRows
+                          : path == ExpertPath::kTokensPair ? kPairRows
+                          : path == ExpertPath::kWeightsM   ? kWtRows
+                                                            : kStreamRows;
     // The tensor-core expert paths read gathered rows (x_perm); streaming reads x.
     const __nv_bfloat16* gather_x = path == ExpertPath::kStreaming ? nullptr : x;
     // Router logits: tensor cores from one full 128-token tile up (E <= 128),
@@ -278,6 +289,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     cudaEvent_t mid = t_cur_ev[3];
     switch (path) {
         case ExpertPath::kTokensM: e = launch_experts_tcgen05(W, s, ws, st, mid); break;
+        case ExpertPath::kTokensPair: e = launch_experts_pair(W, s, ws, st, mid); break;
         case ExpertPath::kWeightsM: e = launch_experts_wt(W, s, ws, st, mid); break;
         default: e = launch_experts_streaming(x, W, s, ws, st, mid); break;
     }
@@ -460,7 +472,7 @@ int moe_stage_times(float* ms, int n) {
 }
 
 int moe_set_expert_path(int path) {
-    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05_WT) return -1;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05_PAIR) return -1;
     const int prev = g_expert_path;
     g_expert_path = path;
     return prev;

@@ -19,6 +19,7 @@ constexpr int kChunkTokens = 256;    // tokens per dispatch chunk (one CTA)
 constexpr int kRouterTokens = 32;    // tokens per router CTA (SIMT router)
 constexpr int kStreamRows = 8;       // rows per tile of the weight-streaming kernels
 constexpr int kTcRows = 128;         // rows per tile of the tcgen05 grouped GEMMs
+constexpr int kPairRows = 256;       // rows per tile of the CTA-pair grouped GEMMs
 constexpr int kWtRows = 64;          // rows per tile of the weights-as-M tcgen05 kernels
 constexpr int kRouterMaxSplits = 4;  // slices of H the tensor-core router may split into
 
@@ -160,6 +161,11 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const ExpertWeights
                                      cudaEvent_t ev_mid);
 cudaError_t launch_experts_tcgen05(const ExpertWeights& W, const Sizes& s,
                                    const Workspace& ws, cudaStream_t st, cudaEvent_t ev_mid);
+// The same GEMMs on CTA pairs (tcgen05 cta_group::2, 256-row tiles from a tile
+// table built at kPairRows); needs I % 128 == 0 and H % 256 == 0.
+bool experts_pair_supported(const Sizes& s);
+cudaError_t launch_experts_pair(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
+                                cudaStream_t st, cudaEvent_t ev_mid);
 // Small batches: the expert weights are the MMA's M side (128 weight rows per
 // MMA) and a tile's <= kWtRows token rows its N side; reads ws.x_perm.
 // Needs I % 128 == 0 and H % 256 == 0 (experts_wt_supported).
@@ -193,6 +199,9 @@ cudaError_t ensure_smem(const void* func, int bytes);
 // columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
 bool make_tma_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// Packed weight blocks (already swizzled in memory) as a [rows, 64] bf16 matrix
+// of 128-byte rows; box of box_rows x 64 copied as-is (no swizzle).
+bool make_tma_packed(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
 
 
 // MOE_OK for cudaSuccess, else records the error for moe_last_cuda_error and

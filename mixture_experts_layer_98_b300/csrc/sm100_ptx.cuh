@@ -46,19 +46,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for barriers that another CTA of
+// the cluster arrives on (remote arrive, multicast commit).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // about timeout_ns of wall time (measured with the SM cycle counter at the
 // maximum 2.032 GHz clock, so a slower clock only lengthens the limit), or as
 // soon as *abort becomes non-zero; returns false in both cases (and sets
 // *abort on a timeout).  The clock is read only every 64 polls: the fast path
 // is a bare try_wait.
+// kCluster: acquire at cluster scope (mbar_try_wait_cluster).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() {
+        return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const long long limit = (long long)(timeout_ns * 2.032);
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 63u) == 0u) {
             if (*abort) return false;
             if (clock64() - t0 > limit) {
@@ -67,6 +86,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             }
         }
     }
+}
+
+// ---- clusters -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster: arrive (release), then wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cluster address of the variable at `p` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive on the mbarrier at a shared::cluster address (possibly another CTA's).
+// Default semantics (release at CTA scope): a cluster-scope release here
+// costs a memory-barrier stall per arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // ---- TMA --------------------------------------------------------------------
@@ -101,6 +148,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         : "memory");
 }
 
+// Pair form of tma_load_2d: the box lands in this CTA's shared memory and its
+// bytes complete on the mbarrier at `bar_cluster_addr`, which may be the
+// peer CTA's (the even CTA's barrier collects both CTAs' stage bytes).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster_addr, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -127,6 +186,52 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
+}
+
+// CTA-pair (cta_group::2) forms: the even and odd CTA of a 2-CTA cluster act
+// as one.  alloc / relinquish / dealloc are executed by one warp of EACH CTA
+// of the pair and give both CTAs the same TMEM columns; an MMA is issued by
+// one thread of the even CTA and reads A rows and B rows from the same
+// shared-memory offsets of both CTAs:
+//   M = 256: CTA c holds A rows 128c..128c+127 and B rows (N/2)c..(N/2)c+N/2-1;
+//            D row 128c + l lands in CTA c's TMEM lane l, columns 0..N-1 = n.
+//   M = 128: CTA c holds A rows 64c..64c+63; D row 64c + i lands in CTA c's
+//            lane i (n < N/2, column n) and lane 64 + i (n >= N/2, column n - N/2).
+// (Placement measured on B300 with a one-cluster probe.)
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of cta_mask once all
+// pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {

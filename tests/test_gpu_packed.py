@@ -86,7 +86,7 @@ def test_packed_forward_is_bitwise_the_row_major_forward(moe, name):
     assert moe.moe_device_status() == 0
 
 
-@pytest.mark.parametrize("path", [2, 3], ids=["tokens_as_m", "weights_as_m"])
+@pytest.mark.parametrize("path", [2, 3, 4], ids=["tokens_as_m", "weights_as_m", "pair"])
 @pytest.mark.parametrize("T,H,E,K,I,norm", [
     (1, 256, 1, 1, 128, False), (77, 512, 64, 6, 384, False), (300, 256, 4, 2, 128, True),
     (2, 1024, 16, 2, 512, True), (513, 512, 32, 2, 256, True)])

@@ -36,7 +36,7 @@ def path(moe, request):
 
 
 PATHS = [pytest.param(2, id="tcgen05"), pytest.param(1, id="streaming"),
-         pytest.param(3, id="tcgen05_wt")]
+         pytest.param(3, id="tcgen05_wt"), pytest.param(4, id="tcgen05_pair")]
 
 
 # ---- stage parity -----------------------------------------------------------------
@@ -158,7 +158,11 @@ def test_tiny(moe, path):
     # few items: gate/up K split into 2 slices; 5 slices of 9,9,9,9,8 k-blocks;
     # down split into 2 slices
     (2, 1024, 16, 2, 512, True), (1, 2816, 4, 2, 128, False), (3, 1280, 8, 2, 640, True),
-    (1, 512, 4, 2, 1024, True)])
+    (1, 512, 4, 2, 1024, True),
+    # CTA-pair tiles: experts of ~750 rows (three 256-row tiles and a ragged
+    # one), of ~233 rows (one M=256 tile with a ragged second half), and an
+    # expert with exactly 256 rows (E = 1)
+    (1500, 512, 4, 2, 256, True), (700, 256, 3, 1, 384, False), (256, 256, 1, 1, 128, True)])
 def test_shape_fuzz(moe, path, T, H, E, K, I, norm):
     cfg = mi.MoEConfig("fuzz", T, H, E, K, I, norm, seed=T + H + E)
     run_case(cfg)
@@ -191,6 +195,30 @@ def test_large_sampled(moe, name):
     cfg = mi.CONFIGS[name]
     rep = run_case(cfg, rows=mi.sample_rows(cfg.T, 48))
     assert rep["out_excess"] <= 0
+
+
+# The CTA-pair grouped GEMMs at full size (AUTO runs them for few, large
+# experts only): 256-row tiles with ragged M=256 and M=128 tails, skewed
+# expert loads, and an expert capacity (dropped pairs leave holes in Y).
+@pytest.mark.parametrize("name,cf", [("prefill_h2048", 0.0), ("skew", 0.0),
+                                     ("prefill_h2048", 1.0)])
+def test_pair_path_large_sampled(moe, name, cf):
+    cfg = mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, "cuda")
+    prev = moe.moe_set_expert_path(moe.MOE_PATH_TCGEN05_PAIR)
+    try:
+        out, lg, idx, w, aux = moe.moe_forward_opts(inp["x"], inp["W_router"], inp["W_gate"],
+                                                    inp["W_up"], inp["W_down"], cfg.K, cfg.norm,
+                                                    capacity_factor=cf)
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_set_expert_path(prev)
+    g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
+             w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
+    C = oracle.capacity_of(cf, cfg.T, cfg.K, cfg.E) if cf > 0 else 0
+    rep = compare(host_bits(inp), g, cfg.K, cfg.norm, rows=mi.sample_rows(cfg.T, 48), capacity=C)
+    assert rep["out_excess"] <= 0
+    assert moe.moe_device_status() == 0
 
 
 def test_zero_tokens(moe):
@@ -377,7 +405,7 @@ def test_paths_agree(moe):
     cfg = mi.MoEConfig("paths", 1000, 512, 32, 4, 384, True, seed=9)
     inp = mi.make_inputs(cfg, "cuda")
     res = {}
-    for p in (1, 2, 3):
+    for p in (1, 2, 3, 4):
         prev = moe.moe_set_expert_path(p)
         try:
             res[p] = [t.clone() for t in moe.moe_forward(inp["x"], inp["W_router"], inp["W_gate"],
@@ -388,7 +416,7 @@ def test_paths_agree(moe):
     torch.cuda.synchronize()
     b = res[2][0].float()
     rms = b.pow(2).mean().sqrt()
-    for p in (1, 3):
+    for p in (1, 3, 4):
         assert torch.equal(res[p][2], res[2][2])  # same routing
         assert (res[p][0].float() - b).abs().max() <= 2e-2 * rms
 
