@@ -46,8 +46,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 STAGE_SOURCES = {
     "router": ["router.cu", "moe_common.cuh"],
     "dispatch": ["dispatch.cu", "moe_common.cuh"],
-    "gate_up": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_stream.cu",
-                "sm100_ptx.cuh", "moe_common.cuh"],
+    "gate_up": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_decode.cu",
+                "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
     "down": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_stream.cu",
              "sm100_ptx.cuh", "moe_common.cuh"],
     "combine": ["combine.cu", "moe_common.cuh"],
@@ -74,7 +74,8 @@ def parse(argv=None):
                     help="expert weights packed once into the tile-major layout before timing "
                          "(moe_pack_experts, a model-load step), or read row-major")
     ap.add_argument("--expert-path", default="auto",
-                    choices=["auto", "streaming", "tcgen05", "tcgen05_wt", "tcgen05_pair"],
+                    choices=["auto", "streaming", "tcgen05", "tcgen05_wt", "tcgen05_pair",
+                             "tcgen05_decode"],
                     help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args(argv)
 
@@ -136,17 +137,22 @@ def peaks():
 
 # ---- algorithmic work per stage: bytes and flops a launch must move or compute -----
 
-def stage_work(cfg, counts):
+def stage_work(cfg, counts, fused=False):
+    """fused: the decode kernel runs gate/up, down and the combine in one launch,
+    timed as the gate_up stage, so that stage carries all three stages' work."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     P = T * K
     touched = int((np.asarray(counts) > 0).sum())
-    return {
+    w = {
         "router": dict(flops=2.0 * T * H * E, bytes=T * H * 2 + E * H * 2 + T * E * 4 + T * K * 8),
         "dispatch": dict(flops=0.0, bytes=T * K * 8 + P * 16 + P * H * 2 * 2),
         "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * 2 + P * H * 2 + P * I * 2),
         "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * 2 + P * I * 2 + P * 4 + P * H * 2),
         "combine": dict(flops=0.0, bytes=P * H * 2 + P * 4 + T * H * 2),
-    }, touched
+    }
+    if fused:
+        w["gate_up"] = {k: w["gate_up"][k] + w["down"][k] + w["combine"][k] for k in ("flops", "bytes")}
+    return w, touched
 
 
 def block_work(cfg, counts):
@@ -336,7 +342,7 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3,
-                             "tcgen05_pair": 4}[args.expert_path])
+                             "tcgen05_pair": 4, "tcgen05_decode": 5}[args.expert_path])
 
     packed = None
     if args.weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
@@ -439,7 +445,8 @@ def run_ours(args, world, rank, local):
     assert moe.moe_device_status() == 0, "device-side timeout during the benchmark"
 
     pk = peaks()
-    work, touched = stage_work(cfg, counts)
+    path_name = expert_path_name(args.expert_path, cfg)
+    work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode")
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     dom = max(stage_mean, key=stage_mean.get)
     wk = work[dom]
@@ -454,7 +461,7 @@ def run_ours(args, world, rank, local):
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic_for(dom, cfg.name)
-    roof["kernel"] = dom
+    roof["kernel"] = "experts_fused" if (dom == "gate_up" and path_name == "tcgen05_decode") else dom
     roof["kernel_ms"] = stage_mean[dom]
     roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
     roof["peak_source"] = pk["source"] + " (burst figures: the kernel is timed alone per step)"
@@ -505,9 +512,13 @@ def expert_path_name(flag, cfg):
         if cfg.T * cfg.K >= 32 * cfg.E:
             pair = wt_ok and cfg.E <= 32 and cfg.T * cfg.K >= 1024 * cfg.E
             return "tcgen05_pair" if pair else "tcgen05"
+        if wt_ok and 1 <= cfg.T <= 16:
+            return "tcgen05_decode"
         return "tcgen05_wt" if wt_ok else "streaming"
-    if flag == "tcgen05_wt" and not wt_ok:
+    if flag in ("tcgen05_wt", "tcgen05_decode") and not wt_ok:
         return "streaming"
+    if flag == "tcgen05_decode" and not 1 <= cfg.T <= 64:
+        return "tcgen05_wt"
     if flag == "tcgen05_pair" and not wt_ok:
         return "tcgen05"
     return flag

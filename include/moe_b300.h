@@ -256,8 +256,10 @@ int moe_last_cuda_error(void);
  *                         E <= 32 experts average >= 1024 rows and
  *                         I % 128 == 0, H % 256 == 0, else on single CTAs
  *                         (128-row tiles); below that the tcgen05 kernels with
- *                         the expert weights on the M side, or, for shapes
- *                         those cannot tile, the weight-streaming kernels;
+ *                         the expert weights on the M side (for 1 <= T <= 16
+ *                         fused with the combine into one kernel), or, for
+ *                         shapes those cannot tile, the weight-streaming
+ *                         kernels;
  *   MOE_PATH_STREAMING    always the weight-streaming CUDA-core kernels;
  *   MOE_PATH_TCGEN05      always the single-CTA token-rows-as-M tcgen05
  *                         grouped GEMMs;
@@ -265,7 +267,11 @@ int moe_last_cuda_error(void);
  *                         where the shape allows, else MOE_PATH_TCGEN05;
  *   MOE_PATH_TCGEN05_WT   always the weights-as-M tcgen05 kernels where the
  *                         shape allows (I % 128 == 0 and H % 256 == 0), else
- *                         the weight-streaming kernels.
+ *                         the weight-streaming kernels; gate/up, down and
+ *                         the combine as three kernels;
+ *   MOE_PATH_TCGEN05_DECODE  as MOE_PATH_TCGEN05_WT, but with 1 <= T <= 64
+ *                         the three run as one cooperative kernel (AUTO's
+ *                         choice for T <= 16; bitwise the same results).
  * Every path computes the same function; results agree within the fp32
  * accumulation-order tolerance (not bitwise across paths).
  * Returns the previous setting, or -1 for an unknown value. */
@@ -274,7 +280,8 @@ enum moe_path {
     MOE_PATH_STREAMING = 1,
     MOE_PATH_TCGEN05 = 2,
     MOE_PATH_TCGEN05_WT = 3,
-    MOE_PATH_TCGEN05_PAIR = 4
+    MOE_PATH_TCGEN05_PAIR = 4,
+    MOE_PATH_TCGEN05_DECODE = 5
 };
 int moe_set_expert_path(int path);
 

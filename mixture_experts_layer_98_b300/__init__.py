@@ -5,7 +5,8 @@ only marshals torch tensors into that ABI.  Build with
 ``python -m mixture_experts_layer_98_b300.build``.
 """
 from .binding import (EXPORTS, LIB_PATH, MOE_PATH_AUTO, MOE_PATH_STREAMING,  # noqa: F401
-                      MOE_PATH_TCGEN05, MOE_PATH_TCGEN05_PAIR, MOE_PATH_TCGEN05_WT, MoEError,
+                      MOE_PATH_TCGEN05, MOE_PATH_TCGEN05_DECODE, MOE_PATH_TCGEN05_PAIR,
+                      MOE_PATH_TCGEN05_WT, MoEError,
                       PackedExperts, lib,
                       moe_dbg_combine, moe_dbg_permute, moe_dbg_wait_timeout, moe_forward_host_packed,
                       moe_forward_opts, moe_forward_packed, moe_pack_experts, moe_packed_experts_bytes,

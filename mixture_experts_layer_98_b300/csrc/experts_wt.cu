@@ -453,13 +453,19 @@ WtPlan wt_plan(const Sizes& s) {
     pl.ks_dn = split_for(pl.items_dn, s.I / kBK);
     // A tile holds at most one row per token, so at most min(kWtRows, T) rows.
     pl.part_rows = s.T < kWtRows ? ((s.T + kBox - 1) / kBox) * kBox : kWtRows;
+    // Separate gate/up and down regions: the fused decode kernel runs units of
+    // both kinds at once.
     const size_t per_slice = (size_t)2 * pl.part_rows * kWM;
-    size_t need = 0;
-    if (pl.ks_gu > 1) need = (size_t)pl.items_gu * pl.ks_gu * per_slice;
-    if (pl.ks_dn > 1 && (size_t)pl.items_dn * pl.ks_dn * per_slice > need)
-        need = (size_t)pl.items_dn * pl.ks_dn * per_slice;
-    pl.partial_floats = need;
-    pl.n_counters = (int)((pl.ks_gu > 1 ? pl.items_gu : 0) + (pl.ks_dn > 1 ? pl.items_dn : 0)) * 4;
+    pl.partial_floats_gu = pl.ks_gu > 1 ? (size_t)pl.items_gu * pl.ks_gu * per_slice : 0;
+    pl.partial_floats = pl.partial_floats_gu +
+                        (pl.ks_dn > 1 ? (size_t)pl.items_dn * pl.ks_dn * per_slice : 0);
+    pl.n_counters_gu = (int)(pl.ks_gu > 1 ? pl.items_gu : 0) * 4;
+    pl.n_counters_dn = (int)(pl.ks_dn > 1 ? pl.items_dn : 0) * 4;
+    if (s.T <= kDecodeFusedTokens) {
+        pl.n_ready = (int)tiles;
+        pl.n_cdone = s.T * (s.H / (2 * kWM) * 4);
+    }
+    pl.n_counters = pl.n_counters_gu + pl.n_counters_dn + pl.n_ready + pl.n_cdone;
     return pl;
 }
 
@@ -499,7 +505,8 @@ cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Work
     p.num_kb = s.I / kBK;
     p.ksplit = pl.ks_dn;
     p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
-    p.counters = ws.status + 4 + (pl.ks_gu > 1 ? pl.items_gu * 4 : 0);
+    p.counters = ws.status + 4 + pl.n_counters_gu;
+    p.partial = ws.wt_partial + pl.partial_floats_gu;
     p.w_rows_per_expert = s.H;
     p.out = ws.ybuf;
     p.out_ld = s.H;

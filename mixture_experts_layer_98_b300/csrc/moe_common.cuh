@@ -176,12 +176,23 @@ struct WtPlan {
     int ks_gu = 1, ks_dn = 1;               // K slices of the gate/up and down items
     long long items_gu = 0, items_dn = 0;   // upper bounds on the items
     int part_rows = 0;                      // token rows kept per slice accumulator
-    size_t partial_floats = 0;              // slice-accumulator buffer
-    int n_counters = 0;                     // gate/up counters, then down counters
+    size_t partial_floats_gu = 0;           // gate/up slice accumulators (first)
+    size_t partial_floats = 0;              // slice-accumulator buffer: gate/up, then down
+    int n_counters_gu = 0, n_counters_dn = 0;  // split-K arrival counters
+    int n_ready = 0, n_cdone = 0;           // fused decode kernel: h_ready, tok_done
+    int n_counters = 0;                     // all of the above, zeroed every forward
 };
 WtPlan wt_plan(const Sizes& s);
 cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
+// Decode batches (1 <= T <= kDecodeFusedTokens, shapes experts_wt_supported):
+// the weights-as-M gate/up and down units and the combine in one cooperative
+// persistent kernel (experts_decode.cu); writes out directly.
+constexpr int kDecodeFusedTokens = 64;
+constexpr int kDecodeAutoTokens = 16;  // MOE_PATH_AUTO uses the fused kernel up to here
+bool experts_decode_supported(const Sizes& s);
+cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
+                                  const int32_t* inv, __nv_bfloat16* out, cudaStream_t st);
 // out[t] = sum over k of Y row t*K + k (Y token-major, as the expert kernels
 // store it), skipping the pairs with inv[t*K + k] < 0 when inv != null
 // (dropped by a capacity); with y_by_inv, Y is in dispatch order and row

@@ -46,7 +46,7 @@ def test_strerror(L):
 
 def test_set_expert_path(L):
     assert L.moe_set_expert_path(7) == -1
-    assert L.moe_set_expert_path(5) == -1
+    assert L.moe_set_expert_path(6) == -1
     prev = L.moe_set_expert_path(1)
     assert L.moe_set_expert_path(4) == 1      # MOE_PATH_TCGEN05_PAIR
     assert L.moe_set_expert_path(prev) == 4

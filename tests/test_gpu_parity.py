@@ -36,7 +36,8 @@ def path(moe, request):
 
 
 PATHS = [pytest.param(2, id="tcgen05"), pytest.param(1, id="streaming"),
-         pytest.param(3, id="tcgen05_wt"), pytest.param(4, id="tcgen05_pair")]
+         pytest.param(3, id="tcgen05_wt"), pytest.param(4, id="tcgen05_pair"),
+         pytest.param(5, id="tcgen05_decode")]
 
 
 # ---- stage parity -----------------------------------------------------------------
@@ -218,6 +219,35 @@ def test_pair_path_large_sampled(moe, name, cf):
     C = oracle.capacity_of(cf, cfg.T, cfg.K, cfg.E) if cf > 0 else 0
     rep = compare(host_bits(inp), g, cfg.K, cfg.norm, rows=mi.sample_rows(cfg.T, 48), capacity=C)
     assert rep["out_excess"] <= 0
+    assert moe.moe_device_status() == 0
+
+
+# The fused decode kernel (gate/up, down and the combine in one launch) runs
+# the same units with the same arithmetic as the three separate kernels: the
+# results must agree bit for bit -- one token with a 3-way K split of gate/up,
+# a few tokens, 64 tokens (one 64-row tile per expert), two experts of 14336
+# rows, split shapes from the fuzz list, and a capacity that drops pairs.
+@pytest.mark.parametrize("name,cf", [("decode_t1", 0.0), ("decode_t4", 0.0), ("decode_t16", 0.0),
+                                     ("decode_t64", 0.0), ("mixtral_decode_t1", 0.0),
+                                     ("decode_t16", 1.0), ("decode_t64", 1.0),
+                                     ("split_a", 0.0), ("split_b", 0.0)])
+def test_decode_fused_is_bitwise_the_three_kernels(moe, name, cf):
+    extra = {"split_a": mi.MoEConfig("split_a", 2, 1024, 16, 2, 512, True, seed=7),
+             "split_b": mi.MoEConfig("split_b", 3, 1280, 8, 2, 640, True, seed=8)}
+    cfg = extra.get(name) or mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, "cuda")
+    res = {}
+    for p in (moe.MOE_PATH_TCGEN05_WT, moe.MOE_PATH_TCGEN05_DECODE):
+        prev = moe.moe_set_expert_path(p)
+        try:
+            res[p] = [t.clone() for t in moe.moe_forward_opts(
+                inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], cfg.K,
+                cfg.norm, capacity_factor=cf)]
+        finally:
+            moe.moe_set_expert_path(prev)
+    torch.cuda.synchronize()
+    for u, v in zip(res[moe.MOE_PATH_TCGEN05_WT], res[moe.MOE_PATH_TCGEN05_DECODE]):
+        assert torch.equal(u, v)
     assert moe.moe_device_status() == 0
 
 
