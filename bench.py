@@ -451,11 +451,17 @@ def run_ours(args, world, rank, local):
     dom = max(stage_mean, key=stage_mean.get)
     wk = work[dom]
     t_s = stage_mean[dom] * 1e-3
-    t_flop = wk["flops"] / (pk["bf16_tflops"] * 1e12)
+    # The kernels run inside >= 1 s of back-to-back forwards (the warm-up alone
+    # lasts >= 1 s), i.e. under the board's sustained power limit: a tensor-bound
+    # kernel is measured against the sustained bf16 figure (cuBLAS looped for
+    # seconds), with the burst fraction beside it.
+    tflops = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+    t_flop = wk["flops"] / (tflops * 1e12)
     t_byte = wk["bytes"] / (pk["hbm_gbs"] * 1e9)
     if t_flop >= t_byte:
-        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": pk["bf16_tflops"],
+        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": tflops,
                 "unit": "TFLOP/s"}
+        roof["frac_burst"] = roof["achieved"] / pk["bf16_tflops"]
     else:
         roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
@@ -464,14 +470,21 @@ def run_ours(args, world, rank, local):
     roof["kernel"] = "experts_fused" if (dom == "gate_up" and path_name == "tcgen05_decode") else dom
     roof["kernel_ms"] = stage_mean[dom]
     roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
-    roof["peak_source"] = pk["source"] + " (burst figures: the kernel is timed alone per step)"
+    roof["peak_source"] = pk["source"] + (
+        " (tensor: sustained bf16 figure -- the step runs inside >= 1 s of back-to-back "
+        "forwards; frac_burst against the burst figure)" if roof["bound"] == "tensor" else
+        " (HBM: measured copy bandwidth)")
     bf, bb = block_work(cfg, counts)
-    t_roof = max(bf / (pk["bf16_tflops"] * 1e12), bb / (pk["hbm_gbs"] * 1e9))
+    t_roof = max(bf / (tflops * 1e12), bb / (pk["hbm_gbs"] * 1e9))
+    t_roof_burst = max(bf / (pk["bf16_tflops"] * 1e12), bb / (pk["hbm_gbs"] * 1e9))
     block = {"flops": bf, "bytes": bb, "t_roof_us": t_roof * 1e6, "t_us": mean_ms * 1e3,
              "frac": t_roof / (mean_ms * 1e-3),
-             "tensor_frac": bf / (mean_ms * 1e-3) / (pk["bf16_tflops"] * 1e12),
+             "frac_burst": t_roof_burst / (mean_ms * 1e-3),
+             "tensor_frac": bf / (mean_ms * 1e-3) / (tflops * 1e12),
+             "tensor_frac_burst": bf / (mean_ms * 1e-3) / (pk["bf16_tflops"] * 1e12),
              "hbm_frac": bb / (mean_ms * 1e-3) / (pk["hbm_gbs"] * 1e9),
-             "touched_experts": touched}
+             "touched_experts": touched,
+             "peaks": "HBM measured copy; tensor sustained (frac) and burst (frac_burst)"}
 
     e2e = None
     if not args.no_e2e:
