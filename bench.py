@@ -60,6 +60,9 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="prefill_h2048", choices=sorted(mi.CONFIGS))
+    ap.add_argument("--shape", default=None,
+                    help="T,H,E,K,I: a custom layer (norm_topk_prob on, seed 0) instead of --config, "
+                         "for small profiling cases")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -78,6 +81,13 @@ def parse(argv=None):
                              "tcgen05_decode"],
                     help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args(argv)
+
+
+def workload(args):
+    if args.shape:
+        T, H, E, K, I = (int(v) for v in args.shape.split(","))
+        return mi.MoEConfig(f"shape_T{T}_H{H}_E{E}_K{K}_I{I}", T, H, E, K, I, True)
+    return mi.CONFIGS[args.config]
 
 
 # ---- distributed ------------------------------------------------------------------
@@ -277,7 +287,7 @@ def oracle_sample_rate(cfg, bits, target_s, max_tokens=None):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    cfg = mi.CONFIGS[args.config]
+    cfg = workload(args)
     inp = mi.make_inputs(cfg, "cpu")
     bits = {k: mi.bits(v) for k, v in inp.items()}
     import oracle
@@ -331,7 +341,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    cfg = mi.CONFIGS[args.config]
+    cfg = workload(args)
     inp = mi.make_inputs(cfg, dev, seed=replica_seed(cfg, rank))
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
