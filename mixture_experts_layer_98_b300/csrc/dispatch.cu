@@ -20,7 +20,8 @@
 //   scatter : rank of each pair inside its chunk from per-expert token
 //             bitmaps -> perm_tok, perm_slot, inv, w_perm
 //   gather  : x_perm[row] = x[perm_tok[row]] for the tensor-core expert GEMMs
-//             (16-byte vectors); the streaming kernels read x through perm_tok
+//             (16-byte vectors; in row order, or token by token through inv once
+//             x exceeds 48 MB); the streaming kernels read x through perm_tok
 //
 // A batch of at most one chunk (256 tokens) runs count, scan and scatter as
 // one CTA (dispatch_small_kernel); at most 32 tokens, that CTA also routes
@@ -429,9 +430,63 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* x,
     }
 }
 
+// The same rows gathered token by token: one warp per token loads x[t] once and
+// stores it to the rows inv[t*K + k] of its kept pairs.  Row order reads each
+// token's row K times in scattered order -- from DRAM once x exceeds the L2
+// (8 GB/s of re-reads per TB/s of writes at K = 8); token order reads x once.
+__global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* x, const int32_t* inv,
+                                                            int T, int K, int vec_per_row,
+                                                            uint4* x_perm) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long t = warp; t < T; t += nwarps) {
+        // lane k holds the row of pair (t, k) (-1: dropped by a capacity)
+        const int my_row = lane < K ? inv[(size_t)t * K + lane] : -1;
+        const uint4* src = x + (size_t)t * vec_per_row;
+        for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kGatherVec) {
+            // x is the caller's input, constant for this grid's lifetime (see
+            // gather_rows_kernel): the read-only path is allowed
+            uint4 v[kGatherVec];
+#pragma unroll
+            for (int j = 0; j < kGatherVec; ++j) {
+                const int c = c0 + j * 32 + lane;
+                if (c < vec_per_row) v[j] = __ldg(src + c);
+            }
+            for (int k = 0; k < K; ++k) {
+                const int row = __shfl_sync(0xffffffffu, my_row, k);
+                if (row < 0) continue;
+                uint4* dst = x_perm + (size_t)row * vec_per_row;
+#pragma unroll
+                for (int j = 0; j < kGatherVec; ++j) {
+                    const int c = c0 + j * 32 + lane;
+                    if (c < vec_per_row) dst[c] = v[j];
+                }
+            }
+        }
+    }
+}
+
+// x above this size gathers in token order (gather_tokens_kernel): beyond
+// about half the L2, the row-order re-reads of x start to come from DRAM.
+constexpr size_t kTokenOrderGatherBytes = 48ull << 20;
+
 cudaError_t launch_gather(const __nv_bfloat16* x, const Sizes& s, const Workspace& ws,
                           cudaStream_t st) {
     const long long P = s.P();
+    if ((size_t)s.T * s.H * 2 > kTokenOrderGatherBytes) {
+        long long blocks = ((long long)s.T + 7) / 8;
+        const long long cap = (long long)num_sms() * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                                   reinterpret_cast<const uint4*>(x), (const int32_t*)ws.inv,
+                                   s.T, s.K, s.H / 8, reinterpret_cast<uint4*>(ws.x_perm));
+        count_launches(1);
+        return e;
+    }
     long long blocks = (P + 7) / 8;
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
