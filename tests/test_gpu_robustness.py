@@ -43,12 +43,25 @@ def test_bounded_wait_rejects_bad_limits(moe):
         moe.moe_dbg_wait_timeout(10 ** 10)
 
 
-CASES = [("tiny", 0.0), ("decode_t1", 0.0), ("decode_t64", 0.0), ("prefill_h2048", 0.0),
-         ("prefill_h2048", 1.0), ("decode_t16", 1.0)]
+# (workload, capacity factor, expert path: 0 AUTO, 4 CTA pairs, 5 fused decode)
+CASES = [("tiny", 0.0, 0), ("decode_t1", 0.0, 0), ("decode_t64", 0.0, 0),
+         ("prefill_h2048", 0.0, 0), ("prefill_h2048", 1.0, 0), ("decode_t16", 1.0, 0),
+         ("prefill_h2048", 0.0, 4), ("prefill_h2048", 1.0, 4), ("decode_t64", 1.0, 5)]
 
 
-@pytest.mark.parametrize("name,cf", CASES)
-def test_nothing_is_written_past_the_workspace(moe, name, cf):
+@pytest.fixture
+def on_path(moe, request):
+    prev = moe.moe_set_expert_path(request.param)
+    yield request.param
+    moe.moe_set_expert_path(prev)
+
+
+def _cases():
+    return [pytest.param(n, cf, p, id=f"{n}-{cf}-path{p}") for n, cf, p in CASES]
+
+
+@pytest.mark.parametrize("name,cf,on_path", _cases(), indirect=["on_path"])
+def test_nothing_is_written_past_the_workspace(moe, name, cf, on_path):
     cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, "cuda")
     need = moe.moe_workspace_bytes(cfg.T, cfg.H, cfg.E, cfg.K, cfg.I)
@@ -70,8 +83,8 @@ def _guarded(shape, dtype, fill):
     return buf, buf[g:g + rows * cols].view(rows, cols), g
 
 
-@pytest.mark.parametrize("name,cf", CASES)
-def test_nothing_is_written_outside_the_outputs(moe, name, cf):
+@pytest.mark.parametrize("name,cf,on_path", _cases(), indirect=["on_path"])
+def test_nothing_is_written_outside_the_outputs(moe, name, cf, on_path):
     cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, "cuda")
     T, H, E, K = cfg.T, cfg.H, cfg.E, cfg.K
