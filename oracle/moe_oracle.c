@@ -442,3 +442,81 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
     return oracle_moe_forward_b(x, T, H, Wr, NULL, 0, Wg, Wu, Wd, E, K, I, norm, flags, rows, n_rows,
                                 out, out_f64, logits_out, idx_out, w_out, aux_out, counts_out);
 }
+
+/* ---- 4-bit group quantisation of the expert weights ----------------------
+ *
+ * The csdn page "MoE架构深度解析：128专家与8激活的智能路由", section
+ * "参数量化与存储优化": the experts' weights are stored as 4-bit values in
+ * groups of 128 parameters, each group with its own scale and bias.  The page
+ * gives no formula; the reading taken here:
+ *   - a group is 128 consecutive entries of one weight row, i.e. along the
+ *     projection's input dimension (H for gate_proj / up_proj, I for
+ *     down_proj);
+ *   - lo, hi = the group's minimum and maximum; the scale s = bf16(fp32(hi - lo)
+ *     / 15) and the bias b = lo (a bf16 value already);
+ *   - the code of w is q = clamp(rint(fp32(w - b) / s), 0, 15), every step in
+ *     fp32 arithmetic (q = 0 when s = 0);
+ *   - the dequantised weight is w' = bf16(q·s + b), rounded once from the
+ *     exact value.
+ * A forward with quantised experts is the forward with the weights W'.
+ */
+
+static float q4_f32(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* W [rows, cols] bf16 (cols % 128 == 0) -> q [rows, cols] codes 0..15,
+ * s, b [rows, cols / 128] bf16. */
+int oracle_quantize_q4(const uint16_t* W, int rows, int cols, uint8_t* q, uint16_t* s,
+                       uint16_t* b) {
+    if (rows < 0 || cols <= 0 || cols % 128) return 1;
+    const int groups = cols / 128;
+    for (long long r = 0; r < rows; ++r) {
+        for (int g = 0; g < groups; ++g) {
+            const uint16_t* w = W + r * cols + (long long)g * 128;
+            float lo = q4_f32(w[0]), hi = lo;
+            for (int j = 1; j < 128; ++j) {
+                const float v = q4_f32(w[j]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            const float span = hi - lo;
+            const uint16_t sb = oracle_f64_to_bf16((double)(span / 15.0f));
+            const uint16_t bb = oracle_f64_to_bf16((double)lo);
+            const float sf = q4_f32(sb), bf = q4_f32(bb);
+            for (int j = 0; j < 128; ++j) {
+                int code = 0;
+                if (sf != 0.0f) {
+                    const float t = rintf((q4_f32(w[j]) - bf) / sf);
+                    code = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
+                }
+                q[r * cols + (long long)g * 128 + j] = (uint8_t)code;
+            }
+            s[r * groups + g] = sb;
+            b[r * groups + g] = bb;
+        }
+    }
+    return 0;
+}
+
+/* q, s, b as above -> W' [rows, cols] bf16: w' = bf16(q·s + b).  q·s is exact
+ * in double (a 4-bit integer times a bf16); the sum is exact there too unless
+ * the two terms lie more than 2^41 apart, and then the sum rounds to b in bf16
+ * either way. */
+int oracle_dequantize_q4(const uint8_t* q, const uint16_t* s, const uint16_t* b, int rows,
+                         int cols, uint16_t* W) {
+    if (rows < 0 || cols <= 0 || cols % 128) return 1;
+    const int groups = cols / 128;
+    for (long long r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const long long gi = r * groups + c / 128;
+            const uint8_t code = q[r * cols + c];
+            if (code > 15) return 2;
+            const double v = (double)code * oracle_bf16_to_f64(s[gi]) + oracle_bf16_to_f64(b[gi]);
+            W[r * cols + c] = oracle_f64_to_bf16(v);
+        }
+    return 0;
+}

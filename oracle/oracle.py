@@ -37,6 +37,8 @@ class _Lib:
         lib.oracle_dispatch.argtypes = [P, i, i, i, P, P, P, P, P]
         lib.oracle_dispatch_cap.argtypes = [P, i, i, i, i, P, P, P, P, P]
         lib.oracle_keep_mask.argtypes = [P, i, i, i, i, P]
+        lib.oracle_quantize_q4.argtypes = [P, i, i, P, P, P]
+        lib.oracle_dequantize_q4.argtypes = [P, P, P, i, i, P]
         lib.oracle_expert_mlp.argtypes = [P, i, P, P, P, i, i, P]
         lib.oracle_token_output.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P]
         lib.oracle_token_output_ex.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P, P]
@@ -281,3 +283,29 @@ def capacity_of(cf, T, K, E):
     import math
     return max(1, int(math.ceil(cf * T * K / E)))
 
+
+
+def quantize_q4(W):
+    """4-bit group quantisation of weight rows (csdn page, section
+    "参数量化与存储优化"; the reading is in moe_oracle.c): W [..., cols] bf16 bits
+    (cols % 128 == 0) -> (q uint8 codes [..., cols], s, b bf16 bits [..., cols/128])."""
+    W = _c(W, np.uint16)
+    cols = W.shape[-1]
+    rows = W.size // cols
+    q = np.empty(W.shape, dtype=np.uint8)
+    s = np.empty(W.shape[:-1] + (cols // 128,), dtype=np.uint16)
+    b = np.empty_like(s)
+    _check(_L().oracle_quantize_q4(_p(W), rows, cols, _p(q), _p(s), _p(b)), "quantize_q4")
+    return q, s, b
+
+
+def dequantize_q4(q, s, b):
+    """W' = bf16(q·s + b) per element (bf16 bits, the shape of q)."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint16)
+    b = _c(b, np.uint16)
+    cols = q.shape[-1]
+    W = np.empty(q.shape, dtype=np.uint16)
+    _check(_L().oracle_dequantize_q4(_p(q), _p(s), _p(b), q.size // cols, cols, _p(W)),
+           "dequantize_q4")
+    return W

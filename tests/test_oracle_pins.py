@@ -406,13 +406,83 @@ def pin_capacity_dispatch():
         assert np.array_equal(big[key], plain[key])
 
 
+# ---- 4-bit group quantisation (csdn page, section "参数量化与存储优化") --------
+
+def _bf16_of(v):
+    """bf16 bits of values that are exactly representable (checked)."""
+    v = np.asarray(v, np.float32)
+    bits = (v.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), v)
+    return bits
+
+
+def pin_q4_exact_grid():
+    # Groups whose entries lie on lo + k·s with s a power of two: the codes are k,
+    # scale and bias are s and lo, and dequantisation gives the weights back.
+    # Every group (128 entries of a row) has its own lo and s, so groups taken
+    # along the wrong axis or indexed wrongly change the codes.
+    rng = np.random.default_rng(40)
+    rows, cols = 3, 384
+    k = rng.integers(0, 16, size=(rows, cols))
+    lo = np.empty((rows, cols // 128))
+    st = np.empty_like(lo)
+    vals = np.empty((rows, cols))
+    for r in range(rows):
+        for g in range(cols // 128):
+            kk = k[r, g * 128:(g + 1) * 128]
+            kk[0], kk[1] = 0, 15  # the group's min and max are on the grid's ends
+            lo[r, g] = -0.25 * (1 + r + 2 * g)
+            st[r, g] = 2.0 ** -(3 + (r + g) % 3)
+            vals[r, g * 128:(g + 1) * 128] = lo[r, g] + kk * st[r, g]
+    W = _bf16_of(vals)
+    q, s, b = oracle.quantize_q4(W)
+    assert np.array_equal(q, k)
+    assert np.array_equal(s, _bf16_of(st)) and np.array_equal(b, _bf16_of(lo))
+    assert np.array_equal(oracle.dequantize_q4(q, s, b), W)
+
+
+def pin_q4_round_half_even_and_constant_group():
+    # lo = 0, hi = 15 -> s = 1: entries at k + 0.5 get the even neighbour
+    g = np.zeros(128, np.float32)
+    g[1] = 15.0
+    g[2:8] = [0.5, 1.5, 2.5, 3.5, 13.5, 14.5]
+    # a second group that is constant: scale 0, every code 0, weights unchanged
+    W = _bf16_of(np.concatenate([g, np.full(128, -0.375, np.float32)])[None, :])
+    q, s, b = oracle.quantize_q4(W)
+    assert q[0, 2:8].tolist() == [0, 2, 2, 4, 14, 14]
+    assert q[0, 1] == 15 and q[0, 0] == 0
+    assert oracle.bf16_to_f64(s)[0].tolist() == [1.0, 0.0]
+    assert (q[0, 128:] == 0).all()
+    assert np.array_equal(oracle.dequantize_q4(q, s, b)[0, 128:], W[0, 128:])
+
+
+def pin_q4_error_bound():
+    # random weights: codes span 0..15 with the min at 0 and the max at 15, and
+    # |w' - w| <= s/2 + half a bf16 ulp of w' (rounding to the grid, then to bf16)
+    rng = np.random.default_rng(41)
+    W = _bf16_of((rng.standard_normal((16, 512)) * 0.02).astype(np.float32).view(np.uint32)
+                 .__and__(np.uint32(0xFFFF0000)).view(np.float32))
+    q, s, b = oracle.quantize_q4(W)
+    w = oracle.bf16_to_f64(W)
+    wd = oracle.bf16_to_f64(oracle.dequantize_q4(q, s, b))
+    sv = np.repeat(oracle.bf16_to_f64(s), 128, axis=1)
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(wd) + 1e-300)) - 7)
+    assert (np.abs(wd - w) <= sv / 2 + ulp / 2 + 1e-12).all()
+    for r in range(16):
+        for gi in range(4):
+            grp = w[r, gi * 128:(gi + 1) * 128]
+            qq = q[r, gi * 128:(gi + 1) * 128]
+            assert qq[np.argmin(grp)] == 0 and qq[np.argmax(grp)] == 15
+
+
 PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equal_logits,
         pin_weights_closed_form, pin_router_logits, pin_dispatch_bruteforce,
         pin_single_expert_is_swiglu, pin_dense_equivalence, pin_soft_router,
         pin_token_permutation_equivariance, pin_aux, pin_param_counts,
         pin_bias_zero_is_unbiased, pin_biased_topk_bruteforce,
         pin_biased_weights_are_unbiased_probs, pin_bias_forces_selection_and_aux,
-        pin_capacity_bruteforce, pin_capacity_dispatch]
+        pin_capacity_bruteforce, pin_capacity_dispatch, pin_q4_exact_grid,
+        pin_q4_round_half_even_and_constant_group, pin_q4_error_bound]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -460,6 +530,12 @@ MUTATIONS = {
                             "(uint8_t)(capacity <= 0 || seen[e] <= capacity)"),
     "dropped_pairs_contribute": ("                if (keep[(size_t)t * K + k]) {\n                    ik[nk]",
                                  "                if (1) {\n                    ik[nk]"),
+    "q4_bias_dropped": ("(double)code * oracle_bf16_to_f64(s[gi]) + oracle_bf16_to_f64(b[gi]);",
+                        "(double)code * oracle_bf16_to_f64(s[gi]);"),
+    "q4_sixteen_levels": ("(double)(span / 15.0f)", "(double)(span / 16.0f)"),
+    "q4_codes_truncate": ("rintf((q4_f32(w[j]) - bf) / sf)", "truncf((q4_f32(w[j]) - bf) / sf)"),
+    "q4_wrong_group": ("const long long gi = r * groups + c / 128;",
+                       "const long long gi = r * groups + c % groups;"),
     "weights_from_biased_keys": (
         "logits[i];\n    oracle_softmax(logits, T, E, probs);",
         "logits[i];\n    oracle_softmax(keys, T, E, probs);"),
