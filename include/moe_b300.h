@@ -102,7 +102,7 @@ int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
  * library holds those 32 MiB until the process exits.  Sizes whose
  * moe_workspace_bytes(T,H,E,K,I) exceeds 32 MiB are rejected with
  * MOE_ERR_WORKSPACE before any work (e.g. the H=4096, E=128, K=8, I=1536
- * layer fits up to T = 214 tokens).
+ * layer fits up to T = 212 tokens).
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any stream
