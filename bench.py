@@ -73,9 +73,10 @@ def parse(argv=None):
                     help="reference arm: oracle seconds per step (default: ~150 s in total)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the forward captured as a CUDA graph (decode serving)")
-    ap.add_argument("--weights", default="packed", choices=["packed", "row-major"],
+    ap.add_argument("--weights", default="packed", choices=["packed", "row-major", "q4"],
                     help="expert weights packed once into the tile-major layout before timing "
-                         "(moe_pack_experts, a model-load step), or read row-major")
+                         "(moe_pack_experts, a model-load step), read row-major, or quantised "
+                         "once to 4 bits in groups of 128 (moe_quantize_experts_q4)")
     ap.add_argument("--expert-path", default="auto",
                     choices=["auto", "streaming", "tcgen05", "tcgen05_wt", "tcgen05_pair",
                              "tcgen05_decode"],
@@ -147,17 +148,22 @@ def peaks():
 
 # ---- algorithmic work per stage: bytes and flops a launch must move or compute -----
 
-def stage_work(cfg, counts, fused=False):
+# bytes per expert weight: bf16, or 4-bit codes plus a bf16 scale and bias per 128
+WEIGHT_BYTES = {"bf16": 2.0, "q4": 0.5 + 4.0 / 128}
+
+
+def stage_work(cfg, counts, fused=False, wb=2.0):
     """fused: the decode kernel runs gate/up, down and the combine in one launch,
-    timed as the gate_up stage, so that stage carries all three stages' work."""
+    timed as the gate_up stage, so that stage carries all three stages' work.
+    wb: bytes per expert weight."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     P = T * K
     touched = int((np.asarray(counts) > 0).sum())
     w = {
         "router": dict(flops=2.0 * T * H * E, bytes=T * H * 2 + E * H * 2 + T * E * 4 + T * K * 8),
         "dispatch": dict(flops=0.0, bytes=T * K * 8 + P * 16 + P * H * 2 * 2),
-        "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * 2 + P * H * 2 + P * I * 2),
-        "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * 2 + P * I * 2 + P * 4 + P * H * 2),
+        "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * wb + P * H * 2 + P * I * 2),
+        "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * wb + P * I * 2 + P * 4 + P * H * 2),
         "combine": dict(flops=0.0, bytes=P * H * 2 + P * 4 + T * H * 2),
     }
     if fused:
@@ -165,13 +171,14 @@ def stage_work(cfg, counts, fused=False):
     return w, touched
 
 
-def block_work(cfg, counts):
+def block_work(cfg, counts, wb=2.0):
     """Whole-block roofline: routed FLOPs and the bytes of the touched experts'
-    weights plus the block's inputs and outputs (intermediates excluded)."""
+    weights (wb bytes each) plus the block's inputs and outputs (intermediates
+    excluded)."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     touched = int((np.asarray(counts) > 0).sum())
     flops = 6.0 * T * K * H * I + 2.0 * T * H * E
-    byts = touched * 3 * H * I * 2 + E * H * 2 + T * H * 2 * 2 + T * E * 4 + T * K * 8 + 4
+    byts = touched * 3 * H * I * wb + E * H * 2 + T * H * 2 * 2 + T * E * 4 + T * K * 8 + 4
     return flops, byts
 
 
@@ -355,13 +362,21 @@ def run_ours(args, world, rank, local):
                              "tcgen05_pair": 4, "tcgen05_decode": 5}[args.expert_path])
 
     packed = None
+    q4 = None
     if args.weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
         # one-time weight layout transform (model load), outside every timed region
         packed = moe.moe_pack_experts(inp["W_gate"], inp["W_up"], inp["W_down"])
         torch.cuda.synchronize()
+    if args.weights == "q4":
+        q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+        torch.cuda.synchronize()
 
     def forward(workspace=None):
-        if packed is not None:
+        if q4 is not None:
+            moe.moe_forward_q4(inp["x"], inp["W_router"], q4, K, cfg.norm, out=out,
+                               router_logits=logits, topk_idx=idx, topk_w=w, aux=aux,
+                               workspace=workspace)
+        elif packed is not None:
             moe.moe_forward_packed(inp["x"], inp["W_router"], packed, K, cfg.norm, out=out,
                                    router_logits=logits, topk_idx=idx, topk_w=w, aux=aux,
                                    workspace=workspace)
@@ -455,8 +470,9 @@ def run_ours(args, world, rank, local):
     assert moe.moe_device_status() == 0, "device-side timeout during the benchmark"
 
     pk = peaks()
-    path_name = expert_path_name(args.expert_path, cfg)
-    work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode")
+    path_name = "tcgen05_wt_q4" if q4 is not None else expert_path_name(args.expert_path, cfg)
+    wb = WEIGHT_BYTES["q4" if q4 is not None else "bf16"]
+    work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode", wb=wb)
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     dom = max(stage_mean, key=stage_mean.get)
     wk = work[dom]
@@ -484,7 +500,7 @@ def run_ours(args, world, rank, local):
         " (tensor: sustained bf16 figure -- the step runs inside >= 1 s of back-to-back "
         "forwards; frac_burst against the burst figure)" if roof["bound"] == "tensor" else
         " (HBM: measured copy bandwidth)")
-    bf, bb = block_work(cfg, counts)
+    bf, bb = block_work(cfg, counts, wb=wb)
     t_roof = max(bf / (tflops * 1e12), bb / (pk["hbm_gbs"] * 1e9))
     t_roof_burst = max(bf / (pk["bf16_tflops"] * 1e12), bb / (pk["hbm_gbs"] * 1e9))
     block = {"flops": bf, "bytes": bb, "t_roof_us": t_roof * 1e6, "t_us": mean_ms * 1e3,
@@ -498,7 +514,7 @@ def run_ours(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed)
+        e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -515,15 +531,18 @@ def run_ours(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(config_block(cfg, world),
                            launch="CUDA graph replay" if args.graph else "eager launches",
-                           expert_weights=("packed once into the tile-major layout before timing "
-                                           "(moe_pack_experts, a model-load step)"
-                                           if packed is not None else "row-major")),
+                           expert_weights=(
+                               "quantised once to 4 bits, groups of 128 with a bf16 scale and "
+                               "bias (moe_quantize_experts_q4, a model-load step)" if q4 is not None
+                               else "packed once into the tile-major layout before timing "
+                               "(moe_pack_experts, a model-load step)" if packed is not None
+                               else "row-major")),
             "roofline": roof, "block_roofline": block,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                        "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
             "stage_ms": {k: round(v, 5) for k, v in stage_mean.items()},
-            "expert_path": expert_path_name(args.expert_path, cfg),
+            "expert_path": path_name,
         }
         print(json.dumps(line), flush=True)
 
@@ -547,15 +566,28 @@ def expert_path_name(flag, cfg):
     return flag
 
 
-def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed):
+def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4=None):
     T, H, E, K = cfg.T, cfg.H, cfg.E, cfg.K
     x_h = inp["x"].cpu().pin_memory()
     out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     lg_h = torch.empty((T, E), dtype=torch.float32).pin_memory()
     aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    if q4 is not None:  # no host-memory 4-bit entry: copies around moe_forward_q4
+        x_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        out_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        lg_d = torch.empty((T, E), dtype=torch.float32, device=dev)
+        aux_d = torch.empty(1, dtype=torch.float32, device=dev)
 
     def call():
-        if packed is not None:
+        if q4 is not None:
+            x_d.copy_(x_h, non_blocking=True)
+            moe.moe_forward_q4(x_d, inp["W_router"], q4, K, cfg.norm, out=out_d,
+                               router_logits=lg_d, aux=aux_d)
+            out_h.copy_(out_d, non_blocking=True)
+            lg_h.copy_(lg_d, non_blocking=True)
+            aux_h.copy_(aux_d, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        elif packed is not None:
             moe.moe_forward_host_packed(x_h, inp["W_router"], packed, K, cfg.norm, out_h,
                                         router_logits_host=lg_h, aux_host=aux_h)
         else:
@@ -576,7 +608,8 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed):
     mean = max_over_ranks(mean, world, dev)
     return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
             "d2h_bytes_per_step": T * H * 2 + T * E * 4 + 4, "ms_per_step": mean * 1e3,
-            "api": ("moe_forward_host_packed" if packed is not None else "moe_forward_host")
+            "api": ("pinned copies around moe_forward_q4" if q4 is not None
+                    else "moe_forward_host_packed" if packed is not None else "moe_forward_host")
                    + " (pinned host x in; out, router_logits, aux out)"}
 
 

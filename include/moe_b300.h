@@ -188,6 +188,60 @@ int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16
                             int32_t* topk_idx_host, float* topk_w_host, float* aux_host,
                             void* stream);
 
+/* ---- 4-bit group-quantised experts ----------------------------------------
+ *
+ * Weight-only quantisation of the expert projections as the csdn page
+ * "MoE架构深度解析：128专家与8激活的智能路由" describes it (section
+ * "参数量化与存储优化": 4-bit values, groups of 128 parameters, a scale and a
+ * bias per group; the page gives no formula).  Reading implemented: a group is
+ * 128 consecutive entries of a weight row (along H for W_gate / W_up, along I
+ * for W_down); with lo / hi its minimum / maximum (a zero minimum as +0),
+ * s = bf16((hi - lo) / 15), b = lo, and each weight's code
+ * q = clamp(rint((w - b) / s), 0, 15) in fp32 (q = 0 when s = 0).  A forward
+ * with 4-bit experts is exactly the bf16 forward with the dequantised weights
+ * w' = bf16(q·s + b) (rounded once); it reads 4.25 bits per weight.
+ *
+ * Buffer layout (device, from moe_quantize_experts_q4), per matrix -- W_gate
+ * [E,I,H], W_up [E,I,H], W_down [E,H,I], R rows per expert, C columns -- a code
+ * section then a scale section, in the order gate, up, down:
+ *   codes  (E·R·C/2 bytes): 4096-byte blocks of 128 rows x 64 columns ordered
+ *          (expert, row block, column block); in a block, row r is 8 32-bit
+ *          words from byte r·32; word c holds columns 8c..8c+7: column 8c+2j
+ *          in bits 4j..4j+3 and column 8c+2j+1 in bits 16+4j..19+4j (j=0..3);
+ *   scales (E·R·(C/128)·4 bytes): 512-byte blocks of 128 rows x one 128-column
+ *          group ordered (expert, row block, group); word r = bf16 s (bits
+ *          0-15) | bf16 b (bits 16-31) of row r.
+ * Shapes: I % 128 == 0 and H % 256 == 0 (else 0 bytes / MOE_ERR_INVALID_ARG).
+ */
+
+/* Bytes of the 4-bit buffer for (H, E, I); 0 for an unsupported shape. */
+size_t moe_q4_experts_bytes(int H, int E, int I);
+
+/* Quantises row-major bf16 expert weights (device) into `q4_experts` (device,
+ * moe_q4_experts_bytes bytes, 16-byte aligned, owned by the caller) on
+ * `stream`: a one-time model-load step.  MOE_ERR_INVALID_ARG for an
+ * unsupported shape or a NULL pointer, MOE_ERR_ALIGNMENT for a misaligned one. */
+int moe_quantize_experts_q4(const moe_bf16* W_gate, const moe_bf16* W_up,
+                            const moe_bf16* W_down, int H, int E, int I, void* q4_experts,
+                            void* stream);
+
+/* The dequantised weights w' = bf16(q·s + b) of a 4-bit buffer, written as
+ * row-major bf16 W_gate [E,I,H], W_up [E,I,H], W_down [E,H,I] (device, caller
+ * owned) on `stream`.  Errors as moe_quantize_experts_q4. */
+int moe_dequantize_experts_q4(const void* q4_experts, int H, int E, int I, moe_bf16* W_gate,
+                              moe_bf16* W_up, moe_bf16* W_down, void* stream);
+
+/* moe_forward with 4-bit expert weights (moe_quantize_experts_q4 with the
+ * same H, E, I); workspace as for moe_forward_packed.  The expert MLPs run on
+ * tensor-core kernels at any T with a row tile's tokens (<= 64) on the MMA's
+ * M side and 256 dequantised weight rows (dequantised in shared memory) on its
+ * N side; results are those of the bf16 forward on the dequantised weights up
+ * to the order of fp32 sums. */
+int moe_forward_q4(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                   const void* q4_experts, int E, int K, int I, int norm_topk_prob,
+                   moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
+                   float* aux, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- forward with options ------------------------------------------------ */
 
 /* Optional inputs of moe_forward_opts; a zero-initialised struct (or a NULL
@@ -218,6 +272,10 @@ typedef struct moe_forward_options {
      * topk_idx / topk_w, router_logits, aux and the expert counts stay the
      * router's.  A negative or non-finite cf gives MOE_ERR_INVALID_ARG. */
     float capacity_factor;
+    /* 4-bit quantised expert weights from moe_quantize_experts_q4 (the row-major
+     * W_gate / W_up / W_down are then ignored), or NULL.  Not together with
+     * packed_experts (MOE_ERR_INVALID_ARG). */
+    const void* q4_experts;
 } moe_forward_options;
 
 /* moe_forward with the options above; every other argument as for

@@ -27,7 +27,8 @@ MOE_PATH_TCGEN05_DECODE = 5
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_packed_experts_bytes", "moe_pack_experts", "moe_forward_packed",
-           "moe_forward_host_packed", "moe_forward_opts",
+           "moe_forward_host_packed", "moe_forward_opts", "moe_q4_experts_bytes",
+           "moe_quantize_experts_q4", "moe_dequantize_experts_q4", "moe_forward_q4",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
            "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
            "moe_stage_times",
@@ -41,7 +42,7 @@ class _Options(ctypes.Structure):
     """struct moe_forward_options."""
     _fields_ = [("expert_bias", ctypes.c_void_p), ("packed_experts", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("capacity_factor", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float), ("q4_experts", ctypes.c_void_p)]
 
 
 class MoEError(RuntimeError):
@@ -77,6 +78,11 @@ def lib():
         L.moe_forward_packed.argtypes = pfwd + [P, sz, P]
         L.moe_forward_host_packed.argtypes = pfwd + [P]
         L.moe_forward_opts.argtypes = fwd + [ctypes.POINTER(_Options), P]
+        L.moe_q4_experts_bytes.argtypes = [i, i, i]
+        L.moe_q4_experts_bytes.restype = sz
+        L.moe_quantize_experts_q4.argtypes = [P, P, P, i, i, i, P, P]
+        L.moe_dequantize_experts_q4.argtypes = [P, i, i, i, P, P, P, P]
+        L.moe_forward_q4.argtypes = pfwd + [P, sz, P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
         L.moe_last_expert_counts.argtypes = [P, i, P]
@@ -249,16 +255,82 @@ def moe_forward_host_packed(x_host, W_router, packed, K, norm_topk_prob, out_hos
     return out_host
 
 
+class Q4Experts:
+    """4-bit group-quantised expert weights (moe_quantize_experts_q4): `data` is
+    the uint8 CUDA buffer, E, H, I the layer's sizes."""
+
+    def __init__(self, data, E, H, I):
+        self.data, self.E, self.H, self.I = data, E, H, I
+
+
+def moe_q4_experts_bytes(H, E, I):
+    return int(lib().moe_q4_experts_bytes(H, E, I))
+
+
+def moe_quantize_experts_q4(W_gate, W_up, W_down, stream=None):
+    """Quantises the row-major expert weights once (a model-load step); returns a
+    Q4Experts for moe_forward_q4 / moe_forward_opts(q4=...)."""
+    E, I, H = W_gate.shape
+    _dev(W_gate, torch.bfloat16, "W_gate", (E, I, H))
+    _dev(W_up, torch.bfloat16, "W_up", (E, I, H))
+    _dev(W_down, torch.bfloat16, "W_down", (E, H, I))
+    n = moe_q4_experts_bytes(H, E, I)
+    if n == 0:
+        raise ValueError(f"expert weights with H={H}, I={I} cannot be quantised here "
+                         "(needs I % 128 == 0 and H % 256 == 0)")
+    data = torch.empty(n, dtype=torch.uint8, device=W_gate.device)
+    _call(lib().moe_quantize_experts_q4(_ptr(W_gate), _ptr(W_up), _ptr(W_down), H, E, I,
+                                        _ptr(data), _stream(stream)), "moe_quantize_experts_q4")
+    return Q4Experts(data, E, H, I)
+
+
+def moe_dequantize_experts_q4(q4, stream=None):
+    """The dequantised bf16 weights (W_gate, W_up, W_down) of a Q4Experts."""
+    E, H, I = q4.E, q4.H, q4.I
+    dev = q4.data.device
+    Wg = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
+    Wu = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
+    Wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+    _call(lib().moe_dequantize_experts_q4(_ptr(q4.data), H, E, I, _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                          _stream(stream)), "moe_dequantize_experts_q4")
+    return Wg, Wu, Wd
+
+
+def moe_forward_q4(x, W_router, q4, K, norm_topk_prob, out=None, router_logits=None,
+                   topk_idx=None, topk_w=None, aux=None, stream=None, workspace=None):
+    """moe_forward with Q4Experts weights; `workspace` as for moe_forward."""
+    T, H = x.shape
+    E, I = q4.E, q4.I
+    if q4.H != H:
+        raise ValueError("x and the 4-bit weights disagree on H")
+    _dev(x, torch.bfloat16, "x")
+    _dev(W_router, torch.bfloat16, "W_router", (E, H))
+    out, router_logits, topk_idx, topk_w, aux = _outputs(T, H, E, K, x.device, out, router_logits,
+                                                         topk_idx, topk_w, aux)
+    if workspace is not None:
+        _dev(workspace, torch.uint8, "workspace")
+    _call(lib().moe_forward_q4(_ptr(x), T, H, _ptr(W_router), _ptr(q4.data), E, K, I,
+                               int(bool(norm_topk_prob)), _ptr(out), _ptr(router_logits),
+                               _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(workspace),
+                               0 if workspace is None else workspace.numel(),
+                               _stream(stream)), "moe_forward_q4")
+    return out, router_logits, topk_idx, topk_w, aux
+
+
 def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, expert_bias=None,
                      packed=None, out=None, router_logits=None, topk_idx=None, topk_w=None,
-                     aux=None, stream=None, workspace=None, capacity_factor=0.0):
+                     aux=None, stream=None, workspace=None, capacity_factor=0.0, q4=None):
     """moe_forward_opts: expert_bias (fp32 [E] CUDA tensor) is the selection-only
-    expert bias; packed a PackedExperts (then W_gate / W_up / W_down may be None);
-    workspace as for moe_forward; capacity_factor > 0 keeps the first
-    ceil(cf·T·K/E) pairs of each expert in token order."""
+    expert bias; packed a PackedExperts or q4 a Q4Experts (then W_gate / W_up /
+    W_down may be None); workspace as for moe_forward; capacity_factor > 0 keeps
+    the first ceil(cf·T·K/E) pairs of each expert in token order."""
     T, H = x.shape
-    if packed is not None:
-        E, I = packed.E, packed.I
+    if packed is None and q4 is not None:
+        packed_like = q4
+    else:
+        packed_like = packed
+    if packed_like is not None:
+        E, I = packed_like.E, packed_like.I
         _dev(x, torch.bfloat16, "x")
         _dev(W_router, torch.bfloat16, "W_router", (E, H))
     else:
@@ -270,7 +342,7 @@ def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, exper
                                                          topk_idx, topk_w, aux)
     opts = _Options(_ptr(expert_bias), None if packed is None else packed.data.data_ptr(),
                     _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                    float(capacity_factor))
+                    float(capacity_factor), None if q4 is None else q4.data.data_ptr())
     _call(lib().moe_forward_opts(_ptr(x), T, H, _ptr(W_router), _ptr(W_gate), _ptr(W_up),
                                  _ptr(W_down), E, K, I, int(bool(norm_topk_prob)), _ptr(out),
                                  _ptr(router_logits), _ptr(topk_idx), _ptr(topk_w), _ptr(aux),

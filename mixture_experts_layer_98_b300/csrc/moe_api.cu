@@ -200,7 +200,7 @@ static void remember_counts(cudaStream_t st, const Workspace& ws, int E) {
     w.E = E;
 }
 
-enum class ExpertPath { kStreaming, kTokensM, kTokensPair, kWeightsM, kDecodeFused };
+enum class ExpertPath { kStreaming, kTokensM, kTokensPair, kWeightsM, kDecodeFused, kWeightsQ4 };
 
 static ExpertPath expert_path(const Sizes& s, bool packed) {
     const bool wt_ok = experts_wt_supported(s);
@@ -244,7 +244,9 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                 cudaStream_t st) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
-    const ExpertPath path = expert_path(s, W.packed != nullptr);
+    // 4-bit experts always run their own kernels (tokens as M, weights
+    // dequantised in shared memory); otherwise the path by batch size and setting
+    const ExpertPath path = W.q4 ? ExpertPath::kWeightsQ4 : expert_path(s, W.packed != nullptr);
     // The streaming kernels stage kStreamRows rows of H (gate/up) and of I
     // (down) in shared memory; larger layers go to the tensor-core paths.
     if (path == ExpertPath::kStreaming &&
@@ -257,6 +259,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                           : path == ExpertPath::kTokensPair ? kPairRows
                           : path == ExpertPath::kWeightsM   ? kWtRows
                           : path == ExpertPath::kDecodeFused ? kWtRows
+                          : path == ExpertPath::kWeightsQ4  ? kWtRows
                                                             : kStreamRows;
     // The tensor-core expert paths read gathered rows (x_perm); streaming reads x.
     const __nv_bfloat16* gather_x = path == ExpertPath::kStreaming ? nullptr : x;
@@ -300,6 +303,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         case ExpertPath::kTokensM: e = launch_experts_tcgen05(W, s, ws, st, mid); break;
         case ExpertPath::kTokensPair: e = launch_experts_pair(W, s, ws, st, mid); break;
         case ExpertPath::kWeightsM: e = launch_experts_wt(W, s, ws, st, mid); break;
+        case ExpertPath::kWeightsQ4: e = launch_experts_q4(W.q4, s, ws, st, mid); break;
         case ExpertPath::kDecodeFused: {
             // experts and combine in one kernel: the whole kernel is timed as the
             // gate/up stage; the down and combine stages read zero
@@ -561,6 +565,55 @@ int moe_forward_packed(const moe_bf16* x, int T, int H, const moe_bf16* W_router
                           topk_w, aux, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+size_t moe_q4_experts_bytes(int H, int E, int I) {
+    if (H < 64 || H % 64 || I < 64 || I % 64 || E < 1 || E > kMaxExperts) return 0;
+    if (!q4_supported(H, E, I)) return 0;
+    return q4_experts_bytes(H, E, I);
+}
+
+int moe_quantize_experts_q4(const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                            int H, int E, int I, void* q4_experts, void* stream) {
+    if (!moe_q4_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+    if (!W_gate || !W_up || !W_down || !q4_experts) return MOE_ERR_INVALID_ARG;
+    const void* ps[] = {W_gate, W_up, W_down, q4_experts};
+    for (const void* p : ps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_status(launch_quantize_q4((const __nv_bfloat16*)W_gate,
+                                          (const __nv_bfloat16*)W_up,
+                                          (const __nv_bfloat16*)W_down, H, E, I,
+                                          (char*)q4_experts, (cudaStream_t)stream));
+}
+
+int moe_dequantize_experts_q4(const void* q4_experts, int H, int E, int I, moe_bf16* W_gate,
+                              moe_bf16* W_up, moe_bf16* W_down, void* stream) {
+    if (!moe_q4_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+    if (!W_gate || !W_up || !W_down || !q4_experts) return MOE_ERR_INVALID_ARG;
+    const void* ps[] = {W_gate, W_up, W_down, q4_experts};
+    for (const void* p : ps)
+        if (misaligned(p)) return MOE_ERR_ALIGNMENT;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_status(launch_dequantize_q4((const char*)q4_experts, H, E, I,
+                                            (__nv_bfloat16*)W_gate, (__nv_bfloat16*)W_up,
+                                            (__nv_bfloat16*)W_down, (cudaStream_t)stream));
+}
+
+int moe_forward_q4(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
+                   const void* q4_experts, int E, int K, int I, int norm_topk_prob,
+                   moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
+                   float* aux, void* workspace, size_t workspace_bytes, void* stream) {
+    if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+    if (!moe_q4_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+    if (misaligned(q4_experts)) return MOE_ERR_ALIGNMENT;
+    ExpertWeights W{nullptr, nullptr, nullptr, nullptr};
+    W.q4 = (const char*)q4_experts;
+    return forward_device(x, T, H, W_router, W, q4_experts, q4_experts, q4_experts, E, K, I,
+                          norm_topk_prob, nullptr, 0, out, router_logits, topk_idx, topk_w, aux,
+                          workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
 int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                      const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down, int E,
                      int K, int I, int norm_topk_prob, moe_bf16* out, float* router_logits,
@@ -573,6 +626,18 @@ int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
     // capacity in pairs: ceil(cf * T * K / E); 0 = none
     const double cf_pairs = (double)o.capacity_factor * T * K / E;
     const int cap = o.capacity_factor > 0.f ? (int)(cf_pairs < 1.0 ? 1.0 : std::ceil(cf_pairs)) : 0;
+    if (o.packed_experts && o.q4_experts) return MOE_ERR_INVALID_ARG;
+    if (o.q4_experts) {
+        if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+        if (!moe_q4_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+        if (misaligned(o.q4_experts)) return MOE_ERR_ALIGNMENT;
+        ExpertWeights W{nullptr, nullptr, nullptr, nullptr};
+        W.q4 = (const char*)o.q4_experts;
+        return forward_device(x, T, H, W_router, W, o.q4_experts, o.q4_experts, o.q4_experts, E,
+                              K, I, norm_topk_prob, o.expert_bias, cap, out, router_logits,
+                              topk_idx, topk_w, aux, o.workspace, o.workspace_bytes,
+                              (cudaStream_t)stream);
+    }
     if (o.packed_experts) {
         if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
         if (!packed_supported(H, E, I)) return MOE_ERR_INVALID_ARG;

@@ -30,6 +30,42 @@ constexpr int kPackRows = 128;
 constexpr int kPackCols = 64;
 constexpr int kPackBlockBytes = kPackRows * kPackCols * 2;
 
+// 4-bit group-quantised experts (quant.cu): 4 KB code blocks of 128 rows x
+// 64 columns and 512-byte scale blocks of 128 rows x one 128-column group.
+constexpr int kQ4CodeBlockBytes = kPackRows * kPackCols / 2;
+constexpr int kQ4ScaleBlockBytes = kPackRows * 4;
+struct Q4Sections {
+    const char* codes[3];   // W_gate, W_up, W_down
+    const char* scales[3];
+};
+bool q4_supported(int H, int E, int I);  // I % 128 == 0, H % 256 == 0
+size_t q4_experts_bytes(int H, int E, int I);
+Q4Sections q4_sections(const char* base, int H, int E, int I);
+cudaError_t launch_quantize_q4(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                               const __nv_bfloat16* Wd, int H, int E, int I, char* q4,
+                               cudaStream_t st);
+cudaError_t launch_dequantize_q4(const char* q4, int H, int E, int I, __nv_bfloat16* Wg,
+                                 __nv_bfloat16* Wu, __nv_bfloat16* Wd, cudaStream_t st);
+
+// Eight dequantised weights (one code word, columns 8c..8c+7) as four bf16
+// pairs: w' = bf16(q·s + b) with one rounding.  (word >> 4j) & 0x000F000F puts
+// the codes of columns 2j, 2j+1 in the two halves; OR-ing 0x4300 makes each
+// half the bf16 value 128 + q, and subtracting 128 leaves q exactly.
+__device__ __forceinline__ uint4 q4_dequant8(uint32_t w, uint32_t sbw) {
+    const __nv_bfloat162 s2 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw & 0xFFFFu)));
+    const __nv_bfloat162 b2 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw >> 16)));
+    const __nv_bfloat162 k128 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0x4300u));
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&t);
+        v = __hfma2(__hsub2(v, k128), s2, b2);
+        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 struct Sizes;
 
 // The expert weights of a forward: row-major matrices, or the packed blocks.
@@ -38,6 +74,7 @@ struct ExpertWeights {
     const __nv_bfloat16* up;    // [E, I, H]
     const __nv_bfloat16* down;  // [E, H, I]
     const char* packed;         // packed blocks (null when row-major)
+    const char* q4 = nullptr;   // 4-bit quantised experts (quant.cu), or null
     const char* packed_gate(const Sizes& s) const;
     const char* packed_up(const Sizes& s) const;
     const char* packed_down(const Sizes& s) const;
@@ -184,6 +221,10 @@ struct WtPlan {
 };
 WtPlan wt_plan(const Sizes& s);
 cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
+                              cudaStream_t st, cudaEvent_t ev_mid);
+// The experts on 4-bit quantised weights (experts_q4.cu): the q4 buffer of
+// launch_quantize_q4; shapes q4_supported and experts_wt_supported.
+cudaError_t launch_experts_q4(const char* q4, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
 // Decode batches (1 <= T <= kDecodeFusedTokens, shapes experts_wt_supported):
 // the weights-as-M gate/up and down units and the combine in one cooperative

@@ -452,8 +452,9 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
  *   - a group is 128 consecutive entries of one weight row, i.e. along the
  *     projection's input dimension (H for gate_proj / up_proj, I for
  *     down_proj);
- *   - lo, hi = the group's minimum and maximum; the scale s = bf16(fp32(hi - lo)
- *     / 15) and the bias b = lo (a bf16 value already);
+ *   - lo, hi = the group's minimum and maximum (a zero minimum taken as +0);
+ *     the scale s = bf16(fp32(hi - lo) / 15) and the bias b = lo (a bf16 value
+ *     already);
  *   - the code of w is q = clamp(rint(fp32(w - b) / s), 0, 15), every step in
  *     fp32 arithmetic (q = 0 when s = 0);
  *   - the dequantised weight is w' = bf16(q·s + b), rounded once from the
@@ -483,6 +484,7 @@ int oracle_quantize_q4(const uint16_t* W, int rows, int cols, uint8_t* q, uint16
                 if (v < lo) lo = v;
                 if (v > hi) hi = v;
             }
+            if (lo == 0.0f) lo = 0.0f; /* a zero minimum is stored as +0 */
             const float span = hi - lo;
             const uint16_t sb = oracle_f64_to_bf16((double)(span / 15.0f));
             const uint16_t bb = oracle_f64_to_bf16((double)lo);

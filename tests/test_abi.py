@@ -107,3 +107,17 @@ def test_packed_sizes_and_early_rejects(L):
     assert L.moe_pack_experts(z, z, z, 1152, 8, 256, z, z) == 1
     assert L.moe_forward_packed(z, 4, 1152, z, z, 8, 2, 256, 1, z, z, z, z, z, z, 0, z) == 1
     assert L.moe_forward_host_packed(z, 4, 1152, z, z, 8, 2, 256, 1, z, z, z, z, z, z) == 1
+
+
+def test_q4_experts_bytes(L):
+    # per matrix: codes E*R*C/2 bytes + scales E*R*(C/128)*4 bytes
+    def mat(R, C, E):
+        return E * R * C // 2 + E * R * (C // 128) * 4
+    H, E, I = 2048, 128, 768
+    assert L.moe_q4_experts_bytes(H, E, I) == 2 * mat(I, H, E) + mat(H, I, E)
+    assert L.moe_q4_experts_bytes(128, 8, 256) == 0    # H % 256 != 0
+    assert L.moe_q4_experts_bytes(256, 8, 192) == 0    # I % 128 != 0
+    assert L.moe_q4_experts_bytes(256, 0, 128) == 0
+    assert L.moe_quantize_experts_q4(None, None, None, 256, 8, 128, None, None) != 0
+    assert L.moe_forward_q4(None, 1, 256, None, None, 8, 2, 128, 1, None, None, None, None,
+                            None, None, 0, None) != 0

@@ -1,0 +1,160 @@
+"""4-bit group-quantised experts on the GPU (csdn page, section
+"参数量化与存储优化"; the reading is in moe_b300.h and the oracle).
+
+- The quantiser's codes, scales and biases are bitwise the oracle's, read back
+  from the buffer through the layout the header documents (a numpy
+  transcription of its formula, independent of the CUDA code).
+- The dequantiser gives bitwise the oracle's w' = bf16(q·s + b).
+- The 4-bit forward computes the bf16 forward on the dequantised weights
+  (tokens on the MMA's M side instead of the weights, so only the fp32
+  summation order differs): routing outputs bitwise equal, the block output
+  within two bf16 ulps, at decode sizes, with K splits, at a prefill size,
+  with a capacity and a selection bias; and it is compared with the oracle
+  run on the oracle's dequantised weights.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from parity import compare, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_ok):
+    from mixture_experts_layer_98_b300 import build
+    build.build()
+    import mixture_experts_layer_98_b300 as m
+    m.lib()
+    yield m
+    m.moe_set_expert_path(m.MOE_PATH_AUTO)
+
+
+def read_q4(buf, E, H, I):
+    """(codes, s, b) per matrix from the documented layout: for each of W_gate,
+    W_up, W_down a code section (4 KB blocks of 128 rows x 64 columns ordered
+    (expert, row block, column block); row r = 8 words from byte r*32; word c
+    holds columns 8c+2j in bits 4j.. and 8c+2j+1 in bits 16+4j..) and a scale
+    section (512-byte blocks per (expert, row block, 128-column group); word r
+    = bf16 s | bf16 b << 16)."""
+    data = buf.cpu().numpy()
+    out = []
+    off = 0
+    for R, C in ((I, H), (I, H), (H, I)):
+        n_code = E * R * C // 2
+        words = data[off:off + n_code].view(np.uint32).reshape(E, R // 128, C // 64, 128, 8)
+        off += n_code
+        codes = np.zeros((E, R, C), np.uint8)
+        for j in range(4):
+            lo = (words >> (4 * j)) & 0xF
+            hi = (words >> (16 + 4 * j)) & 0xF
+            # [E, rb, kb, r, c] -> columns kb*64 + 8c + 2j (+1)
+            for half, v in ((0, lo), (1, hi)):
+                col = (np.arange(C // 64)[:, None] * 64 + np.arange(8)[None, :] * 8
+                       + 2 * j + half)  # [kb, c]
+                codes.reshape(E, R // 128, 128, C)[:, :, :, col] = v.transpose(0, 1, 3, 2, 4)
+        n_sc = E * R * (C // 128) * 4
+        sw = data[off:off + n_sc].view(np.uint32).reshape(E, R // 128, C // 128, 128)
+        off += n_sc
+        sw = sw.transpose(0, 1, 3, 2).reshape(E, R, C // 128)
+        out.append((codes, (sw & 0xFFFF).astype(np.uint16), (sw >> 16).astype(np.uint16)))
+    assert off == data.size
+    return out
+
+
+SHAPES = [(8, 1024, 512), (4, 256, 384), (2, 512, 128)]
+
+
+@pytest.mark.parametrize("E,H,I", SHAPES)
+def test_quantiser_and_dequantiser_are_the_oracles(moe, E, H, I):
+    cfg = mi.MoEConfig("q4", 4, H, E, 2, I, True, seed=E + H + I)
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    deq = moe.moe_dequantize_experts_q4(q4)
+    torch.cuda.synchronize()
+    assert q4.data.numel() == moe.moe_q4_experts_bytes(H, E, I)
+    got = read_q4(q4.data, E, H, I)
+    for name, (codes, s, b), dq in zip(("W_gate", "W_up", "W_down"), got, deq):
+        rq, rs, rb = oracle.quantize_q4(mi.bits(inp[name]))
+        assert np.array_equal(codes, rq), name
+        assert np.array_equal(s, rs) and np.array_equal(b, rb), name
+        assert np.array_equal(mi.bits(dq), oracle.dequantize_q4(rq, rs, rb)), name
+
+
+def _bf16_forward_on(moe, cfg, inp, Wd3, **kw):
+    prev = moe.moe_set_expert_path(moe.MOE_PATH_TCGEN05_WT)
+    try:
+        return [t.clone() for t in moe.moe_forward_opts(inp["x"], inp["W_router"], *Wd3, cfg.K,
+                                                        cfg.norm, **kw)]
+    finally:
+        moe.moe_set_expert_path(prev)
+
+
+def _same_forward(ref, got):
+    """Routing outputs bitwise; out within 2 bf16 ulps of the reference (plus
+    1e-3 of its RMS for values near zero): the two differ only in the order
+    of fp32 sums, then round h, Y and out to bf16."""
+    for i in (1, 2, 3, 4):  # logits, idx, w, aux
+        assert torch.equal(ref[i], got[i])
+    a, b = ref[0].float(), got[0].float()
+    rms = a.pow(2).mean().sqrt()
+    assert ((a - b).abs() <= 2.0 ** -6 * a.abs() + 1e-3 * rms).all()
+
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t4", "decode_t16", "decode_t64",
+                                  "mixtral_decode_t1", "split_a", "prefill_small"])
+def test_q4_forward_is_the_bf16_forward_on_dequantised_weights(moe, name):
+    extra = {"split_a": mi.MoEConfig("split_a", 2, 1024, 16, 2, 512, True, seed=7),
+             "prefill_small": mi.MoEConfig("prefill_small", 1024, 512, 16, 4, 256, True, seed=5)}
+    cfg = extra.get(name) or mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    deq = moe.moe_dequantize_experts_q4(q4)
+    ref = _bf16_forward_on(moe, cfg, inp, deq)
+    got = moe.moe_forward_q4(inp["x"], inp["W_router"], q4, cfg.K, cfg.norm)
+    torch.cuda.synchronize()
+    _same_forward(ref, got)
+    assert moe.moe_device_status() == 0
+
+
+def test_q4_options_capacity_and_bias(moe):
+    cfg = mi.CONFIGS["decode_t16"]
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    deq = moe.moe_dequantize_experts_q4(q4)
+    bias = (torch.arange(cfg.E, device="cuda", dtype=torch.float32) % 7) * 0.01
+    kw = dict(capacity_factor=1.0, expert_bias=bias)
+    ref = _bf16_forward_on(moe, cfg, inp, deq, **kw)
+    got = moe.moe_forward_opts(inp["x"], inp["W_router"], None, None, None, cfg.K, cfg.norm,
+                               q4=q4, **kw)
+    torch.cuda.synchronize()
+    _same_forward(ref, got)
+
+
+@pytest.mark.parametrize("T,H,E,K,I,norm", [(17, 256, 8, 2, 256, True), (1, 512, 4, 2, 384, False),
+                                            (40, 256, 16, 4, 128, True)])
+def test_q4_forward_against_the_oracle(moe, T, H, E, K, I, norm):
+    cfg = mi.MoEConfig("q4o", T, H, E, K, I, norm, seed=T + H)
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    out, lg, idx, w, aux = moe.moe_forward_q4(inp["x"], inp["W_router"], q4, K, norm)
+    torch.cuda.synchronize()
+    b = host_bits(inp)
+    for name in ("W_gate", "W_up", "W_down"):  # the oracle's own quantise + dequantise
+        b[name] = oracle.dequantize_q4(*oracle.quantize_q4(b[name]))
+    g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
+             w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
+    compare(b, g, K, norm)
+
+
+def test_q4_rejects_unsupported_shapes(moe):
+    assert moe.moe_q4_experts_bytes(4096, 128, 1536) > 0
+    assert moe.moe_q4_experts_bytes(128, 8, 256) == 0   # H % 256 != 0
+    assert moe.moe_q4_experts_bytes(256, 8, 192) == 0   # I % 128 != 0
+    W = torch.zeros((2, 192, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        moe.moe_quantize_experts_q4(W, W, torch.zeros((2, 256, 192), dtype=torch.bfloat16,
+                                                      device="cuda"))
