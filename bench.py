@@ -79,7 +79,7 @@ def parse(argv=None):
                          "once to 4 bits in groups of 128 (moe_quantize_experts_q4)")
     ap.add_argument("--expert-path", default="auto",
                     choices=["auto", "streaming", "tcgen05", "tcgen05_wt", "tcgen05_pair",
-                             "tcgen05_decode"],
+                             "tcgen05_decode", "warp_mma"],
                     help="expert MLP kernels (auto picks by rows per expert)")
     return ap.parse_args(argv)
 
@@ -359,7 +359,8 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3,
-                             "tcgen05_pair": 4, "tcgen05_decode": 5}[args.expert_path])
+                             "tcgen05_pair": 4, "tcgen05_decode": 5,
+                             "warp_mma": 6}[args.expert_path])
 
     packed = None
     q4 = None
@@ -470,7 +471,8 @@ def run_ours(args, world, rank, local):
     assert moe.moe_device_status() == 0, "device-side timeout during the benchmark"
 
     pk = peaks()
-    path_name = "tcgen05_wt_q4" if q4 is not None else expert_path_name(args.expert_path, cfg)
+    path_name = (q4_path_name(args.expert_path, cfg) if q4 is not None
+                 else expert_path_name(args.expert_path, cfg))
     wb = WEIGHT_BYTES["q4" if q4 is not None else "bf16"]
     work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode", wb=wb)
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
@@ -547,9 +549,18 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def q4_path_name(flag, cfg):
+    """Which 4-bit expert kernels the library runs for this flag and shape."""
+    if flag == "warp_mma" or (flag != "tcgen05" and cfg.T <= 64):
+        return "warp_mma_q4"
+    return "tcgen05_q4"
+
+
 def expert_path_name(flag, cfg):
     """Which expert kernels the library runs for this flag and shape."""
     wt_ok = cfg.I % 128 == 0 and cfg.H % 256 == 0  # also the CTA-pair kernels' condition
+    if flag == "warp_mma":  # 4-bit experts only; bf16 weights run AUTO's choice
+        flag = "auto"
     if flag == "auto":
         if cfg.T * cfg.K >= 32 * cfg.E:
             pair = wt_ok and cfg.E <= 32 and cfg.T * cfg.K >= 1024 * cfg.E

@@ -329,7 +329,13 @@ int moe_last_cuda_error(void);
  *                         the combine as three kernels;
  *   MOE_PATH_TCGEN05_DECODE  as MOE_PATH_TCGEN05_WT, but with 1 <= T <= 64
  *                         the three run as one cooperative kernel (AUTO's
- *                         choice for T <= 16; bitwise the same results).
+ *                         choice for T <= 16; bitwise the same results);
+ *   MOE_PATH_WARP_MMA     4-bit experts (moe_forward_q4): always the kernels
+ *                         that dequantise the weights into the registers of
+ *                         warp-level MMAs (AUTO's choice for T <= 64); with
+ *                         bf16 weights the same as MOE_PATH_AUTO.
+ * With 4-bit experts, MOE_PATH_TCGEN05 selects the tcgen05 4-bit kernels (AUTO's
+ * choice for T > 64) and every other value acts as MOE_PATH_AUTO.
  * Every path computes the same function; results agree within the fp32
  * accumulation-order tolerance (not bitwise across paths).
  * Returns the previous setting, or -1 for an unknown value. */
@@ -339,7 +345,8 @@ enum moe_path {
     MOE_PATH_TCGEN05 = 2,
     MOE_PATH_TCGEN05_WT = 3,
     MOE_PATH_TCGEN05_PAIR = 4,
-    MOE_PATH_TCGEN05_DECODE = 5
+    MOE_PATH_TCGEN05_DECODE = 5,
+    MOE_PATH_WARP_MMA = 6
 };
 int moe_set_expert_path(int path);
 

@@ -6,6 +6,7 @@ only marshals torch tensors into that ABI.  Build with
 """
 from .binding import (EXPORTS, LIB_PATH, MOE_PATH_AUTO, MOE_PATH_STREAMING,  # noqa: F401
                       MOE_PATH_TCGEN05, MOE_PATH_TCGEN05_DECODE, MOE_PATH_TCGEN05_PAIR,
+                      MOE_PATH_WARP_MMA,
                       MOE_PATH_TCGEN05_WT, MoEError,
                       PackedExperts, Q4Experts, lib, moe_dequantize_experts_q4,
                       moe_forward_q4, moe_q4_experts_bytes, moe_quantize_experts_q4,

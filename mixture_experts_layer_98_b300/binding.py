@@ -24,6 +24,7 @@ MOE_PATH_TCGEN05 = 2
 MOE_PATH_TCGEN05_WT = 3
 MOE_PATH_TCGEN05_PAIR = 4
 MOE_PATH_TCGEN05_DECODE = 5
+MOE_PATH_WARP_MMA = 6
 
 EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_forward_ws", "moe_forward_host",
            "moe_packed_experts_bytes", "moe_pack_experts", "moe_forward_packed",

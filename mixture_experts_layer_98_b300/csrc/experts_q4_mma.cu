@@ -1,0 +1,559 @@
+// experts_q4_mma.cu -- decode batches on 4-bit group-quantised experts:
+// weights dequantised straight into the registers of warp-level tensor-core
+// MMAs (mma.sync m16n8k16, bf16 inputs, fp32 accumulators).
+//
+// Same function as experts_q4.cu (the SwiGLU expert MLP of the csdn page
+// "MoE架构深度解析：128专家与8激活的智能路由", section
+// "128个专家网络的组织结构与参数分布", on the 4-bit weights of its section
+// "参数量化与存储优化", layout and reading in quant.cu; the routing-weight
+// scaling of Qwen3MoeSparseMoeBlock.forward on the cnblogs page
+// "大模型-qwen3 MoE 详细解读").
+//
+// Why a second kernel.  At decode sizes an expert receives 1-8 token rows, so
+// the expert MLP is a matrix-vector product that streams 4.25 bits per
+// weight from HBM: about 40 weights per SM cycle at the measured copy
+// bandwidth.  The tcgen05 kernel of experts_q4.cu needs every dequantised
+// weight in shared memory as bf16 (written by threads, read by the MMA), about
+// 5 bytes of shared-memory traffic per weight, which caps it near 23 weights
+// per cycle (128 B/cycle); with the weights on the MMA's M side instead, an
+// MMA takes about M cycles whatever its N, 16 weights per cycle.  Here the
+// dequantised weights never leave the registers: they are the A fragments of
+// m16n8k16 MMAs whose B fragments are the tile's tokens, 8 per MMA.
+//
+// Fragment mapping.  A thread (g = lane / 4, c = lane % 4) of the warp that
+// owns weight rows R..R+15 reads, per 64-column k-block, the code words c and
+// c + 4 of rows R + g and R + g + 8 (quant.cu: word c' of a row holds columns
+// 8c'..8c'+7, pair j = columns 8c'+2j, 8c'+2j+1).  k-step t (0..3) of the
+// block takes pair 2(t%2) of word c + 4(t/2) as the fragment's columns 2c,
+// 2c+1 and pair 2(t%2)+1 as its columns 2c+8, 2c+9: fragment column f of step
+// t is block column 8((f%8)/2) + 32(t/2) + 4(t%2) + 2(f/8) + f%2, a
+// permutation of the block's 64 columns.  The token fragment applies the same
+// permutation: thread (g, c) loads the 4 consecutive bf16 of token g from
+// column 8c + 32(t/2) + 4(t%2) (8 bytes, 128-byte swizzled rows).  The sum over
+// k is order-free, so the MMA computes the exact products of the bf16 forward
+// on the dequantised weights, accumulated in fp32 in another order.
+//
+// Work items: gate/up (row tile, 128 I rows: the gate rows and the same up
+// rows), down (row tile, 256 H rows), on row tiles of at most 16 tokens
+// (kQ4MmaRows), with K slices fitted to two CTAs per SM (q4mma_plan: an item
+// count that does not fill the grid's last round leaves SMs idle for a whole
+// item, and a decode batch has a few hundred items); warp w of the 8 consumer warps owns two
+// 16-row MMA tiles: gate/up rows 16w.. of W_gate and of W_up (so that
+// silu(gate)·up needs no exchange), down rows 32w.. and 32w+16.. .  With K
+// slices each warp writes its slice accumulators and bumps the item's counter;
+// the warp that arrives last adds the slices in slice order and runs the
+// epilogue.
+//
+// Roles: warp 0 producer (token boxes by TMA, code and scale blocks by bulk
+// copy into a ring of stages), warps 1-8 consumers.  Every wait is bounded
+// (2 s); on expiry the CTA records MOE_ERR_TIMEOUT, lets its copies land and
+// exits (no CTA-wide barrier follows the main loops).
+#include "moe_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kConsumers = 8;
+constexpr int kThreadsM = 32 * (kConsumers + 1);
+constexpr int kBK = 64;
+constexpr int kTokBox = 8;         // token rows per TMA box: one MMA's N
+constexpr int kMaxStages = 16;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+enum { kGateUp = 0, kDown = 1 };
+
+// Stage: NT token boxes (8 rows x 128 bytes, 128-byte swizzled, each on a
+// 1024-byte boundary), the two 4 KB code blocks and two 512-byte scale blocks
+// of the item's 256 weight rows.  Two CTAs per SM.
+template <int NT>
+struct MmaCfg {
+    static_assert(NT * kTokBox <= kQ4MmaRows, "a stage holds a whole row tile");
+    static constexpr int kTokOff = 0;
+    static constexpr int kCodeOff = NT * kTokBox * 128;
+    static constexpr int kScaleOff = kCodeOff + 2 * kQ4CodeBlockBytes;
+    static constexpr int kBytes = kScaleOff + 2 * kQ4ScaleBlockBytes;
+    static constexpr int kCtasPerSm = 2;
+    static constexpr int kBudget = 112 * 1024 - 1024;
+    static constexpr int kStages = kBudget / kBytes < kMaxStages ? kBudget / kBytes : kMaxStages;
+    static constexpr int kSmemBytes = kStages * kBytes + 1024;
+    static_assert(kBytes % 1024 == 0, "stages stay 1024-byte aligned");
+    static_assert(kStages >= 4, "ring depth");
+};
+
+struct MmaParams {
+    const RowTile* tiles;
+    const int32_t* n_tiles;
+    int n_nt;               // items per row tile: I / 128 (gate/up), H / 256 (down)
+    int num_kb;             // k-blocks of 64
+    int ksplit;
+    int kb_per;
+    float* partial;         // [items][ksplit][2][part_rows][128] slice accumulators
+    int part_rows;
+    int32_t* counters;      // per item: arrivals of its warps (all slices)
+    __nv_bfloat16* out;     // h [P, I] or Y [P, H]
+    int out_ld;
+    const float* w_perm;
+    const int32_t* perm_tok;
+    const int32_t* perm_slot;
+    int K;
+    int32_t* status;
+    const char* codes0;     // first / second 128-row block of an item
+    const char* codes1;
+    const char* scales0;
+    const char* scales1;
+    int blocks_per_expert;  // 128-row blocks per expert of the matrix
+    int groups;             // 128-column groups per weight row
+};
+
+struct Item {
+    int pitem, tile, nt, ks, kb0, kb1;
+};
+
+__device__ __forceinline__ Item item_of(const MmaParams& p, int item) {
+    Item it;
+    it.pitem = item / p.ksplit;
+    it.ks = item % p.ksplit;
+    it.tile = it.pitem / p.n_nt;
+    it.nt = it.pitem % p.n_nt;
+    it.kb0 = it.ks * p.kb_per;
+    it.kb1 = min(p.num_kb, it.kb0 + p.kb_per);
+    return it;
+}
+
+// Pair j of a code word dequantised: bf16x2 (column 2j low, 2j+1 high) of
+// bf16(q·s + b), one rounding (as q4_dequant8).
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int j, __nv_bfloat162 s2,
+                                            __nv_bfloat162 b2) {
+    const __nv_bfloat162 k128 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0x4300u));
+    const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&t);
+    v = __hfma2(__hsub2(v, k128), s2, b2);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Output position of accumulator element (tile i, fragment row half fi) of
+// consumer warp cw, thread row g: the item's plane (gate/up: 0 gate, 1 up;
+// down: which 128-row block) and the feature within it (0..127).
+template <int MODE>
+__device__ __forceinline__ int plane_of(int cw, int i) {
+    return MODE == kGateUp ? i : (32 * cw + 16 * i) >> 7;
+}
+template <int MODE>
+__device__ __forceinline__ int row_in_block(int cw, int i) {
+    return MODE == kGateUp ? 16 * cw : (32 * cw + 16 * i) & 127;
+}
+
+// The epilogue of one (token, feature) of an item from its fp32 sums: gate/up
+// h = bf16(silu(g)·u) at feature nt·128 + f; down Y = bf16(w·y) at feature
+// nt·256 + plane·128 + f of the pair's token-major row.
+template <int MODE>
+__device__ __forceinline__ void store_one(const MmaParams& p, const RowTile& tl, int nt,
+                                          int tok, int plane, int f, float a, float b) {
+    const size_t row = (size_t)tl.row0 + tok;
+    if (MODE == kGateUp) {
+        p.out[row * p.out_ld + (size_t)nt * 128 + f] = __float2bfloat16_rn(silu_f(a) * b);
+    } else {
+        const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
+        p.out[yrow * p.out_ld + (size_t)nt * 256 + plane * 128 + f] =
+            __float2bfloat16_rn(p.w_perm[row] * a);
+    }
+}
+
+template <int MODE, int NT>
+__global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
+    expert_q4_mma_kernel(const __grid_constant__ CUtensorMap tmA, const MmaParams p) {
+    using C = MmaCfg<NT>;
+    constexpr int kS = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];   // boxes, codes, scales landed
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];  // all consumer warps read the stage
+    __shared__ volatile int abort_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kS; ++s) {
+            ptx::mbar_init(&full_bar[s], 1);
+            ptx::mbar_init(&empty_bar[s], kConsumers);
+        }
+        abort_s = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmA);
+    }
+    pdl_trigger();
+    __syncthreads();
+    pdl_wait();  // the prologue above overlaps the previous kernel's tail
+    const int total = (*p.n_tiles) * p.n_nt * p.ksplit;
+
+    if (warp == 0) {
+        if (lane != 0) return;
+        // ---------------- producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const Item it = item_of(p, item);
+            const RowTile tl = p.tiles[it.tile];
+            const int nbox = min(NT, (tl.nrows + kTokBox - 1) / kTokBox);  // host: rows <= 8·NT
+            // gate/up: the nt-th 128-row blocks of W_gate and W_up; down: the
+            // blocks 2nt, 2nt + 1 of W_down
+            const int b0 = MODE == kGateUp ? it.nt : 2 * it.nt;
+            const int b1 = MODE == kGateUp ? it.nt : 2 * it.nt + 1;
+            const size_t e0 = (size_t)tl.expert * p.blocks_per_expert;
+            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                // a 128-column group's scales are read at its first k-block of
+                // the slice only (the consumers keep them in registers)
+                const bool new_group = (kb & 1) == 0 || kb == it.kb0;
+                const uint32_t bytes = nbox * kTokBox * 128 + 2 * kQ4CodeBlockBytes +
+                                       (new_group ? 2 * kQ4ScaleBlockBytes : 0);
+                if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_s, kTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + stage * C::kBytes;
+                ptx::mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                for (int b = 0; b < nbox; ++b)
+                    ptx::tma_load_2d(st + C::kTokOff + b * kTokBox * 128, &tmA, &full_bar[stage],
+                                     kb * kBK, tl.row0 + b * kTokBox);
+                const size_t c0 = ((e0 + b0) * p.num_kb + kb) * kQ4CodeBlockBytes;
+                const size_t c1 = ((e0 + b1) * p.num_kb + kb) * kQ4CodeBlockBytes;
+                const size_t s0 = ((e0 + b0) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
+                const size_t s1 = ((e0 + b1) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
+                ptx::bulk_load(st + C::kCodeOff, p.codes0 + c0, kQ4CodeBlockBytes, &full_bar[stage]);
+                ptx::bulk_load(st + C::kCodeOff + kQ4CodeBlockBytes, p.codes1 + c1,
+                               kQ4CodeBlockBytes, &full_bar[stage]);
+                if (new_group) {
+                    ptx::bulk_load(st + C::kScaleOff, p.scales0 + s0, kQ4ScaleBlockBytes,
+                                   &full_bar[stage]);
+                    ptx::bulk_load(st + C::kScaleOff + kQ4ScaleBlockBytes, p.scales1 + s1,
+                                   kQ4ScaleBlockBytes, &full_bar[stage]);
+                }
+                ++issued;
+                if (++stage == kS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            atomicExch(p.status, MOE_ERR_TIMEOUT);
+            // Let the copies already issued land before the CTA exits.
+            int dummy = 0;
+            const long long first = issued > kS ? issued - kS : 0;
+            for (long long n = first; n < issued; ++n)
+                ptx::mbar_wait_bounded(&full_bar[n % kS], (uint32_t)((n / kS) & 1), &dummy,
+                                       kTimeoutNs);
+        }
+        return;
+    }
+
+    // ---------------- consumers (warps 1..8) ----------------
+    const int cw = warp - 1;
+    const int g = lane >> 2, c = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const Item it = item_of(p, item);
+        const RowTile tl = p.tiles[it.tile];
+        const int nn = min(NT, (tl.nrows + kTokBox - 1) / kTokBox);
+        float acc[2][NT][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.f;
+        // scale and bias of rows g, g + 8 of both tiles: one 128-column group
+        // spans two k-blocks
+        __nv_bfloat162 s2[2][2], b2[2][2];
+
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            int good = 1;
+            if (lane == 0) good = ptx::mbar_wait_bounded(&full_bar[stage], phase, &abort_s, kTimeoutNs);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                ok = false;
+                break;
+            }
+            const uint8_t* st = smem + stage * C::kBytes;
+            // code words c, c + 4 of rows g and g + 8 of both 16-row tiles, and
+            // their rows' scale and bias (the k-block's 128-column group)
+            uint32_t wq[2][4];
+            const bool new_group = (kb & 1) == 0 || kb == it.kb0;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int bi = plane_of<MODE>(cw, i), ri = row_in_block<MODE>(cw, i);
+                const uint32_t* r0 = reinterpret_cast<const uint32_t*>(
+                    st + C::kCodeOff + bi * kQ4CodeBlockBytes + (ri + g) * 32);
+                const uint32_t* r1 = r0 + 8 * 8;  // row + 8
+                wq[i][0] = r0[c];
+                wq[i][1] = r0[c + 4];
+                wq[i][2] = r1[c];
+                wq[i][3] = r1[c + 4];
+                if (new_group) {
+                    const uint32_t* sb = reinterpret_cast<const uint32_t*>(
+                        st + C::kScaleOff + bi * kQ4ScaleBlockBytes);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t sbw = sb[ri + g + 8 * h];
+                        s2[i][h] = __bfloat162bfloat162(
+                            __ushort_as_bfloat16((unsigned short)(sbw & 0xFFFFu)));
+                        b2[i][h] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw >> 16)));
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int wi = t >> 1, j = 2 * (t & 1);
+                uint32_t a[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    a[i][0] = dq_pair(wq[i][wi], j, s2[i][0], b2[i][0]);          // row g, cols 2c..
+                    a[i][1] = dq_pair(wq[i][2 + wi], j, s2[i][1], b2[i][1]);      // row g + 8
+                    a[i][2] = dq_pair(wq[i][wi], j + 1, s2[i][0], b2[i][0]);      // row g, cols 2c+8..
+                    a[i][3] = dq_pair(wq[i][2 + wi], j + 1, s2[i][1], b2[i][1]);  // row g + 8
+                }
+                // token g's 4 bf16 from column 8c + 32(t/2) + 4(t%2): chunk
+                // c + 4(t/2) of its 128-byte row, swizzled by the row (g)
+                const int off = g * 128 + (((c + 4 * wi) ^ g) << 4) + 8 * (t & 1);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    if (n < nn) {
+                        const uint2 bv =
+                            *reinterpret_cast<const uint2*>(st + C::kTokOff + n * 1024 + off);
+                        mma_bf16_16816(acc[0][n], a[0], bv.x, bv.y);
+                        mma_bf16_16816(acc[1][n], a[1], bv.x, bv.y);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty_bar[stage]);
+            if (++stage == kS) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+
+        // ---------------- epilogue ----------------
+        // acc[i][n][e]: tile i's row g + 8(e/2) (feature), token 8n + 2c + e%2
+        if (p.ksplit == 1) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                if (n >= nn) continue;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * n + 2 * c + (e & 1);
+                    const int fr = g + 8 * (e >> 1);
+                    if (tok >= tl.nrows) continue;
+                    if (MODE == kGateUp) {
+                        store_one<MODE>(p, tl, it.nt, tok, 0, 16 * cw + fr, acc[0][n][e],
+                                        acc[1][n][e]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+                            store_one<MODE>(p, tl, it.nt, tok, plane_of<MODE>(cw, i),
+                                            row_in_block<MODE>(cw, i) + fr, acc[i][n][e], 0.f);
+                    }
+                }
+            }
+        } else {
+            // slice accumulators partial[pitem][ks][plane][part_rows][128]; the
+            // warp that arrives last (of 8 warps x ksplit slices) adds the slices
+            // in slice order and stores the item's outputs
+            const size_t plane_sz = (size_t)p.part_rows * 128;
+            float* mine = p.partial + ((size_t)it.pitem * p.ksplit + it.ks) * 2 * plane_sz;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                if (n >= nn) continue;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * n + 2 * c + (e & 1);
+                    const int fr = g + 8 * (e >> 1);
+                    if (tok >= tl.nrows) continue;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        __stcg(mine + plane_of<MODE>(cw, i) * plane_sz + (size_t)tok * 128 +
+                                   row_in_block<MODE>(cw, i) + fr,
+                               acc[i][n][e]);
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            int32_t* cnt = p.counters + it.pitem;
+            int last = 0;
+            if (lane == 0) last = atomicAdd(cnt, 1) == kConsumers * p.ksplit - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                const float* all = p.partial + (size_t)it.pitem * p.ksplit * 2 * plane_sz;
+                const int per_tok = MODE == kGateUp ? 128 : 256;
+                for (int o = lane; o < tl.nrows * per_tok; o += 32) {
+                    const int tok = o / per_tok;
+                    const int plane = MODE == kGateUp ? 0 : (o >> 7) & 1;
+                    const int f = o & 127;
+                    float a = 0.f, b = 0.f;
+                    for (int sl = 0; sl < p.ksplit; ++sl) {
+                        const float* src = all + (size_t)sl * 2 * plane_sz + (size_t)tok * 128 + f;
+                        a += __ldcg(src + plane * plane_sz);
+                        if (MODE == kGateUp) b += __ldcg(src + plane_sz);
+                    }
+                    store_one<MODE>(p, tl, it.nt, tok, plane, f, a, b);
+                }
+                if (lane == 0) *cnt = 0;  // ready for the next forward
+            }
+        }
+    }
+    if (!ok && lane == 0) atomicExch(p.status, MOE_ERR_TIMEOUT);
+}
+
+// ---- host side ----------------------------------------------------------------
+
+template <int MODE, int NT>
+cudaError_t launch_mma(const void* A, uint64_t a_rows, uint64_t k_cols, const MmaParams& p,
+                       long long max_items, cudaStream_t st) {
+    CUtensorMap ma;
+    if (!make_tma_2d(&ma, A, a_rows, k_cols, kTokBox)) return cudaErrorInvalidValue;
+    constexpr int smem = MmaCfg<NT>::kSmemBytes;
+    cudaError_t err = ensure_smem((const void*)expert_q4_mma_kernel<MODE, NT>, smem);
+    if (err != cudaSuccess) return err;
+    long long grid = (long long)num_sms() * MmaCfg<NT>::kCtasPerSm;
+    if (grid > max_items) grid = max_items;
+    if (grid < 1) grid = 1;
+    err = launch_pdl(expert_q4_mma_kernel<MODE, NT>, dim3((unsigned)grid), dim3(kThreadsM), smem,
+                     st, ma, p);
+    count_launches(1);
+    return err;
+}
+
+// Token boxes per stage: a row tile holds at most min(T, kQ4MmaRows) rows (one
+// row per token and expert), so one 8-row box covers T <= 8.
+template <int MODE>
+cudaError_t launch_mma_any(const void* A, uint64_t a_rows, uint64_t k_cols, const MmaParams& p,
+                           long long max_items, int T, cudaStream_t st) {
+    static_assert(kQ4MmaRows == 2 * kTokBox, "two token boxes cover a row tile");
+    if (T <= kTokBox) return launch_mma<MODE, 1>(A, a_rows, k_cols, p, max_items, st);
+    return launch_mma<MODE, 2>(A, a_rows, k_cols, p, max_items, st);
+}
+
+// The grid the K split is fitted to: two CTAs on each SM of a 148-SM B300 (a
+// constant: the plan sizes the workspace before any device is known).
+constexpr long long kMmaGrid = 2 * 148;
+
+// Fraction of the persistent grid's rounds that n equal items keep busy.
+double mma_fill(long long n) {
+    const long long rounds = (n + kMmaGrid - 1) / kMmaGrid;
+    return (double)n / (double)(rounds * kMmaGrid);
+}
+
+// K slices for `items` items of num_kb k-blocks: below two rounds of the grid
+// (where an unfilled last round costs the most, and the slice accumulators
+// stay small), the count (at most 6, at least 8 k-blocks a slice, no empty
+// slice) whose items fill the grid's rounds best; ties go to fewer slices.
+int mma_split(long long items, int num_kb) {
+    if (items <= 0 || items >= 2 * kMmaGrid) return 1;
+    int best = 1;
+    double best_fill = mma_fill(items);
+    for (int ks = 2; ks <= 6 && num_kb / ks >= 8; ++ks) {
+        const int kb_per = (num_kb + ks - 1) / ks;
+        if ((num_kb + kb_per - 1) / kb_per != ks) continue;
+        const double f = mma_fill(items * ks);
+        if (f > best_fill + 0.02) {
+            best = ks;
+            best_fill = f;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+Q4MmaPlan q4mma_plan(const Sizes& s) {
+    Q4MmaPlan pl;
+    if (!experts_wt_supported(s) || s.T <= 0) return pl;
+    const long long P = s.P();
+    // Row tiles: sum over experts of ceil(count / 16) <= P / 16 + experts touched.
+    long long tiles = (s.E < P ? s.E : P) + P / kQ4MmaRows;
+    if (tiles > s.max_tiles(kQ4MmaRows)) tiles = s.max_tiles(kQ4MmaRows);
+    pl.items_gu = tiles * (s.I / 128);
+    pl.items_dn = tiles * (s.H / 256);
+    pl.ks_gu = mma_split(pl.items_gu, s.H / kBK);
+    pl.ks_dn = mma_split(pl.items_dn, s.I / kBK);
+    // A tile holds at most min(T, 16) rows.
+    pl.part_rows = s.T < kQ4MmaRows ? (s.T + kTokBox - 1) / kTokBox * kTokBox : kQ4MmaRows;
+    const size_t per_slice = (size_t)2 * pl.part_rows * 128;
+    pl.partial_floats_gu = pl.ks_gu > 1 ? (size_t)pl.items_gu * pl.ks_gu * per_slice : 0;
+    pl.partial_floats = pl.partial_floats_gu +
+                        (pl.ks_dn > 1 ? (size_t)pl.items_dn * pl.ks_dn * per_slice : 0);
+    pl.n_counters_gu = (int)(pl.ks_gu > 1 ? pl.items_gu : 0);
+    pl.n_counters = pl.n_counters_gu + (int)(pl.ks_dn > 1 ? pl.items_dn : 0);
+    return pl;
+}
+
+cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspace& ws,
+                                  cudaStream_t st, cudaEvent_t ev_mid) {
+    if (!q4_supported(s.H, s.E, s.I) || !experts_wt_supported(s)) return cudaErrorInvalidValue;
+    const long long P = s.P();
+    const Q4MmaPlan pl = q4mma_plan(s);
+    const Q4Sections q = q4_sections(q4, s.H, s.E, s.I);
+    MmaParams p{};
+    p.tiles = ws.tiles;
+    p.n_tiles = ws.n_tiles;
+    p.status = ws.status;
+    p.w_perm = ws.w_perm;
+    p.part_rows = pl.part_rows;
+
+    // gate/up: tokens = x_perm rows; weights = the nt-th 128 rows of W_gate and W_up
+    p.n_nt = s.I / 128;
+    p.num_kb = s.H / kBK;
+    p.groups = s.H / 128;
+    p.ksplit = pl.ks_gu;
+    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.partial = ws.wt_partial;
+    p.counters = ws.status + 4;
+    p.out = ws.hbuf;
+    p.out_ld = s.I;
+    p.codes0 = q.codes[0];
+    p.codes1 = q.codes[1];
+    p.scales0 = q.scales[0];
+    p.scales1 = q.scales[1];
+    p.blocks_per_expert = s.I / kPackRows;
+    cudaError_t err =
+        launch_mma_any<kGateUp>(ws.x_perm, P, s.H, p, pl.items_gu * p.ksplit, s.T, st);
+    if (err != cudaSuccess) return err;
+    if (ev_mid) cudaEventRecord(ev_mid, st);
+
+    // down: tokens = h rows; weights = W_down rows [256 nt, 256 nt + 256)
+    p.n_nt = s.H / 256;
+    p.num_kb = s.I / kBK;
+    p.groups = s.I / 128;
+    p.ksplit = pl.ks_dn;
+    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.partial = ws.wt_partial + pl.partial_floats_gu;
+    p.counters = ws.status + 4 + pl.n_counters_gu;
+    p.out = ws.ybuf;
+    p.out_ld = s.H;
+    p.codes0 = p.codes1 = q.codes[2];
+    p.scales0 = p.scales1 = q.scales[2];
+    p.blocks_per_expert = s.H / kPackRows;
+    p.perm_tok = ws.perm_tok;
+    p.perm_slot = ws.perm_slot;
+    p.K = s.K;
+    return launch_mma_any<kDown>(ws.hbuf, P, s.I, p, pl.items_dn * p.ksplit, s.T, st);
+}
+
+}  // namespace moe

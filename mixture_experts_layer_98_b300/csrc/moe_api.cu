@@ -92,10 +92,14 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
     w.offsets = (int32_t*)take(((size_t)s.E + 1) * 4);
     w.tiles = (RowTile*)take((size_t)s.max_tiles(kStreamRows) * sizeof(RowTile));
     w.n_tiles = (int32_t*)take(4);
+    // split-K regions: the weights-as-M plan's or the 4-bit warp-MMA plan's,
+    // whichever needs more (a forward runs one of them)
     const WtPlan plan = wt_plan(s);
-    w.n_clear = 4 + plan.n_counters;
+    const Q4MmaPlan qplan = q4mma_plan(s);
+    w.n_clear = 4 + (plan.n_counters > qplan.n_counters ? plan.n_counters : qplan.n_counters);
     w.status = (int32_t*)take((size_t)w.n_clear * 4);
-    w.wt_partial = (float*)take(plan.partial_floats * 4);
+    w.wt_partial = (float*)take(
+        (plan.partial_floats > qplan.partial_floats ? plan.partial_floats : qplan.partial_floats) * 4);
     w.p_partial = (float*)take((size_t)s.nrouter() * s.E * 4);
     w.perm_tok = (int32_t*)take(P * 4);
     w.perm_slot = (int32_t*)take(P * 4);
@@ -221,6 +225,7 @@ static ExpertPath expert_path(const Sizes& s, bool packed) {
         case MOE_PATH_TCGEN05_PAIR:
             return experts_pair_supported(s) ? ExpertPath::kTokensPair : ExpertPath::kTokensM;
         case MOE_PATH_TCGEN05_DECODE: return small_fused;
+        case MOE_PATH_WARP_MMA: break;  // 4-bit experts only; bf16 weights: AUTO
         default: break;
     }
     // Token rows fill 128-row tiles from ~32 rows per expert on average up;
@@ -247,6 +252,11 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     // 4-bit experts always run their own kernels (tokens as M, weights
     // dequantised in shared memory); otherwise the path by batch size and setting
     const ExpertPath path = W.q4 ? ExpertPath::kWeightsQ4 : expert_path(s, W.packed != nullptr);
+    // 4-bit experts: decode batches on the warp-MMA kernels, larger batches on
+    // the tcgen05 kernels
+    const bool q4_mma = path == ExpertPath::kWeightsQ4 &&
+                        (g_expert_path == MOE_PATH_WARP_MMA ||
+                         (g_expert_path != MOE_PATH_TCGEN05 && s.T <= kQ4MmaTokens));
     // The streaming kernels stage kStreamRows rows of H (gate/up) and of I
     // (down) in shared memory; larger layers go to the tensor-core paths.
     if (path == ExpertPath::kStreaming &&
@@ -259,7 +269,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                           : path == ExpertPath::kTokensPair ? kPairRows
                           : path == ExpertPath::kWeightsM   ? kWtRows
                           : path == ExpertPath::kDecodeFused ? kWtRows
-                          : path == ExpertPath::kWeightsQ4  ? kWtRows
+                          : path == ExpertPath::kWeightsQ4  ? (q4_mma ? kQ4MmaRows : kWtRows)
                                                             : kStreamRows;
     // The tensor-core expert paths read gathered rows (x_perm); streaming reads x.
     const __nv_bfloat16* gather_x = path == ExpertPath::kStreaming ? nullptr : x;
@@ -303,7 +313,10 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         case ExpertPath::kTokensM: e = launch_experts_tcgen05(W, s, ws, st, mid); break;
         case ExpertPath::kTokensPair: e = launch_experts_pair(W, s, ws, st, mid); break;
         case ExpertPath::kWeightsM: e = launch_experts_wt(W, s, ws, st, mid); break;
-        case ExpertPath::kWeightsQ4: e = launch_experts_q4(W.q4, s, ws, st, mid); break;
+        case ExpertPath::kWeightsQ4:
+            e = q4_mma ? launch_experts_q4_mma(W.q4, s, ws, st, mid)
+                       : launch_experts_q4(W.q4, s, ws, st, mid);
+            break;
         case ExpertPath::kDecodeFused: {
             // experts and combine in one kernel: the whole kernel is timed as the
             // gate/up stage; the down and combine stages read zero
@@ -496,7 +509,7 @@ int moe_stage_times(float* ms, int n) {
 }
 
 int moe_set_expert_path(int path) {
-    if (path < MOE_PATH_AUTO || path > MOE_PATH_TCGEN05_DECODE) return -1;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_WARP_MMA) return -1;
     const int prev = g_expert_path;
     g_expert_path = path;
     return prev;

@@ -226,6 +226,25 @@ cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Work
 // launch_quantize_q4; shapes q4_supported and experts_wt_supported.
 cudaError_t launch_experts_q4(const char* q4, const Sizes& s, const Workspace& ws,
                               cudaStream_t st, cudaEvent_t ev_mid);
+// The same on warp-level MMAs with the weights dequantised into registers
+// (experts_q4_mma.cu): decode batches, T <= kQ4MmaTokens under MOE_PATH_AUTO,
+// from a tile table of kQ4MmaRows-row tiles; its own items and K slices
+// (fitted to two CTAs per SM), whose slice accumulators and counters share the
+// weights-as-M plan's workspace regions (sized for the larger of the two).
+constexpr int kQ4MmaTokens = 64;
+constexpr int kQ4MmaRows = 16;
+struct Q4MmaPlan {
+    int ks_gu = 1, ks_dn = 1;
+    long long items_gu = 0, items_dn = 0;   // upper bounds on the items
+    int part_rows = 0;
+    size_t partial_floats_gu = 0;           // gate/up slice accumulators (first)
+    size_t partial_floats = 0;              // gate/up, then down
+    int n_counters_gu = 0;                  // one arrival counter per split item
+    int n_counters = 0;
+};
+Q4MmaPlan q4mma_plan(const Sizes& s);
+cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspace& ws,
+                                  cudaStream_t st, cudaEvent_t ev_mid);
 // Decode batches (1 <= T <= kDecodeFusedTokens, shapes experts_wt_supported):
 // the weights-as-M gate/up and down units and the combine in one cooperative
 // persistent kernel (experts_decode.cu); writes out directly.

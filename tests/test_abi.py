@@ -45,11 +45,13 @@ def test_strerror(L):
 
 
 def test_set_expert_path(L):
+    assert L.moe_set_expert_path(8) == -1
     assert L.moe_set_expert_path(7) == -1
-    assert L.moe_set_expert_path(6) == -1
+    assert L.moe_set_expert_path(-1) == -1
     prev = L.moe_set_expert_path(1)
     assert L.moe_set_expert_path(4) == 1      # MOE_PATH_TCGEN05_PAIR
-    assert L.moe_set_expert_path(prev) == 4
+    assert L.moe_set_expert_path(6) == 4      # MOE_PATH_WARP_MMA
+    assert L.moe_set_expert_path(prev) == 6
 
 
 def test_workspace_bytes(L):
