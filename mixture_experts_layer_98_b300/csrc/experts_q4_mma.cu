@@ -40,9 +40,9 @@
 // item, and a decode batch has a few hundred items); warp w of the 8 consumer warps owns two
 // 16-row MMA tiles: gate/up rows 16w.. of W_gate and of W_up (so that
 // silu(gate)·up needs no exchange), down rows 32w.. and 32w+16.. .  With K
-// slices each warp writes its slice accumulators and bumps the item's counter;
-// the warp that arrives last adds the slices in slice order and runs the
-// epilogue.
+// slices each warp writes its slice accumulators and bumps its own counter of
+// the item; the slice whose warp arrives last adds, for that warp's outputs,
+// the slices in slice order and runs their epilogue.
 //
 // Roles: warp 0 producer (token boxes by TMA, code and scale blocks by bulk
 // copy into a ring of stages), warps 1-8 consumers.  Every wait is bounded
@@ -91,7 +91,7 @@ struct MmaParams {
     int kb_per;
     float* partial;         // [items][ksplit][2][part_rows][128] slice accumulators
     int part_rows;
-    int32_t* counters;      // per item: arrivals of its warps (all slices)
+    int32_t* counters;      // per item and consumer warp: arrivals of its slices
     __nv_bfloat16* out;     // h [P, I] or Y [P, H]
     int out_ld;
     const float* w_perm;
@@ -372,47 +372,69 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
                 }
             }
         } else {
-            // slice accumulators partial[pitem][ks][plane][part_rows][128]; the
-            // warp that arrives last (of 8 warps x ksplit slices) adds the slices
-            // in slice order and stores the item's outputs
+            // slice accumulators partial[pitem][ks][plane][part_rows][128]: this
+            // warp's outputs of every slice; the last slice to arrive (per warp)
+            // adds them in slice order and stores them
             const size_t plane_sz = (size_t)p.part_rows * 128;
-            float* mine = p.partial + ((size_t)it.pitem * p.ksplit + it.ks) * 2 * plane_sz;
+            const size_t slice_sz = 2 * plane_sz;
+            float* base = p.partial + (size_t)it.pitem * p.ksplit * slice_sz;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 if (n >= nn) continue;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = 8 * n + 2 * c + (e & 1);
-                    const int fr = g + 8 * (e >> 1);
                     if (tok >= tl.nrows) continue;
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
-                        __stcg(mine + plane_of<MODE>(cw, i) * plane_sz + (size_t)tok * 128 +
-                                   row_in_block<MODE>(cw, i) + fr,
+                        __stcg(base + (size_t)it.ks * slice_sz + plane_of<MODE>(cw, i) * plane_sz +
+                                   (size_t)tok * 128 + row_in_block<MODE>(cw, i) + g + 8 * (e >> 1),
                                acc[i][n][e]);
                 }
             }
             __threadfence();
             __syncwarp();
-            int32_t* cnt = p.counters + it.pitem;
+            int32_t* cnt = p.counters + (size_t)it.pitem * kConsumers + cw;
             int last = 0;
-            if (lane == 0) last = atomicAdd(cnt, 1) == kConsumers * p.ksplit - 1;
+            if (lane == 0) last = atomicAdd(cnt, 1) == p.ksplit - 1;
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
                 __threadfence();
-                const float* all = p.partial + (size_t)it.pitem * p.ksplit * 2 * plane_sz;
-                const int per_tok = MODE == kGateUp ? 128 : 256;
-                for (int o = lane; o < tl.nrows * per_tok; o += 32) {
-                    const int tok = o / per_tok;
-                    const int plane = MODE == kGateUp ? 0 : (o >> 7) & 1;
-                    const int f = o & 127;
-                    float a = 0.f, b = 0.f;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    if (n >= nn) continue;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.f;
                     for (int sl = 0; sl < p.ksplit; ++sl) {
-                        const float* src = all + (size_t)sl * 2 * plane_sz + (size_t)tok * 128 + f;
-                        a += __ldcg(src + plane * plane_sz);
-                        if (MODE == kGateUp) b += __ldcg(src + plane_sz);
+                        const float* src = base + (size_t)sl * slice_sz;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int tok = 8 * n + 2 * c + (e & 1);
+                            if (tok >= tl.nrows) continue;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i)
+                                acc[i][n][e] += __ldcg(src + plane_of<MODE>(cw, i) * plane_sz +
+                                                       (size_t)tok * 128 +
+                                                       row_in_block<MODE>(cw, i) + g + 8 * (e >> 1));
+                        }
                     }
-                    store_one<MODE>(p, tl, it.nt, tok, plane, f, a, b);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = 8 * n + 2 * c + (e & 1);
+                        const int fr = g + 8 * (e >> 1);
+                        if (tok >= tl.nrows) continue;
+                        if (MODE == kGateUp) {
+                            store_one<MODE>(p, tl, it.nt, tok, 0, 16 * cw + fr, acc[0][n][e],
+                                            acc[1][n][e]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 2; ++i)
+                                store_one<MODE>(p, tl, it.nt, tok, plane_of<MODE>(cw, i),
+                                                row_in_block<MODE>(cw, i) + fr, acc[i][n][e], 0.f);
+                        }
+                    }
                 }
                 if (lane == 0) *cnt = 0;  // ready for the next forward
             }
@@ -499,8 +521,8 @@ Q4MmaPlan q4mma_plan(const Sizes& s) {
     pl.partial_floats_gu = pl.ks_gu > 1 ? (size_t)pl.items_gu * pl.ks_gu * per_slice : 0;
     pl.partial_floats = pl.partial_floats_gu +
                         (pl.ks_dn > 1 ? (size_t)pl.items_dn * pl.ks_dn * per_slice : 0);
-    pl.n_counters_gu = (int)(pl.ks_gu > 1 ? pl.items_gu : 0);
-    pl.n_counters = pl.n_counters_gu + (int)(pl.ks_dn > 1 ? pl.items_dn : 0);
+    pl.n_counters_gu = (int)(pl.ks_gu > 1 ? pl.items_gu * kConsumers : 0);
+    pl.n_counters = pl.n_counters_gu + (int)(pl.ks_dn > 1 ? pl.items_dn * kConsumers : 0);
     return pl;
 }
 

@@ -239,7 +239,7 @@ struct Q4MmaPlan {
     int part_rows = 0;
     size_t partial_floats_gu = 0;           // gate/up slice accumulators (first)
     size_t partial_floats = 0;              // gate/up, then down
-    int n_counters_gu = 0;                  // one arrival counter per split item
+    int n_counters_gu = 0;                  // arrival counters: 8 per split item
     int n_counters = 0;
 };
 Q4MmaPlan q4mma_plan(const Sizes& s);
