@@ -67,6 +67,17 @@ def test_workspace_bytes(L):
     assert ws(1, 128, 8, 2, 256) <= ws(2, 128, 8, 2, 256)
 
 
+def test_noalloc_scratch_limit(L):
+    # moe_forward_noalloc's 32 MiB scratch holds the workspace of every batch up
+    # to T = 212 on the H=4096, E=128, K=8, I=1536 layer (the limit its header
+    # states) and not T = 213.  The split-K plans of the decode kernels size
+    # part of the workspace, so a plan change that grows it shows up here.
+    ws = L.moe_workspace_bytes
+    scratch = 32 << 20
+    assert max(ws(T, 4096, 128, 8, 1536) for T in range(1, 213)) <= scratch
+    assert ws(213, 4096, 128, 8, 1536) > scratch
+
+
 @pytest.mark.parametrize("T,H,E,K,I", [(-1, 128, 8, 2, 256), (4, 96, 8, 2, 256),
                                        (4, 128, 0, 1, 256), (4, 128, 8, 0, 256),
                                        (4, 128, 8, 2, 100), (4, 128, 4, 5, 256)])
