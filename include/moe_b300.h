@@ -232,11 +232,15 @@ int moe_dequantize_experts_q4(const void* q4_experts, int H, int E, int I, moe_b
                               moe_bf16* W_up, moe_bf16* W_down, void* stream);
 
 /* moe_forward with 4-bit expert weights (moe_quantize_experts_q4 with the
- * same H, E, I); workspace as for moe_forward_packed.  The expert MLPs run on
- * tensor-core kernels at any T with a row tile's tokens (<= 64) on the MMA's
- * M side and 256 dequantised weight rows (dequantised in shared memory) on its
- * N side; results are those of the bf16 forward on the dequantised weights up
- * to the order of fp32 sums. */
+ * same H, E, I); workspace as for moe_forward_packed.  Decode batches (T <= 64
+ * under MOE_PATH_AUTO) run the expert MLPs on warp-level tensor-core MMAs whose
+ * weight operands are dequantised straight into registers (row tiles of <= 16
+ * tokens); larger batches on tcgen05 kernels with a row tile's tokens (<= 64)
+ * on the MMA's M side and 256 weight rows, dequantised in shared memory, on its
+ * N side (MOE_PATH_WARP_MMA / MOE_PATH_TCGEN05 force either).  Either way the
+ * results are those of the bf16 forward on the dequantised weights up to the
+ * order of fp32 sums.  4 bits pay at decode, where the expert weights' bytes
+ * bound the forward; at prefill sizes the bf16 forward is faster. */
 int moe_forward_q4(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                    const void* q4_experts, int E, int K, int I, int norm_topk_prob,
                    moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
