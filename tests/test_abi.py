@@ -134,3 +134,34 @@ def test_q4_experts_bytes(L):
     assert L.moe_quantize_experts_q4(None, None, None, 256, 8, 128, None, None) != 0
     assert L.moe_forward_q4(None, 1, 256, None, None, 8, 2, 128, 1, None, None, None, None,
                             None, None, 0, None) != 0
+
+
+def test_q4_argument_checks(L):
+    # every check below runs before the library touches a device (no GPU here);
+    # the pointers are never dereferenced
+    from mixture_experts_layer_98_b300.binding import (MOE_ERR_ALIGNMENT, MOE_ERR_INVALID_ARG,
+                                                        _Options)
+    import ctypes
+    odd = ctypes.c_void_p(0x1008)    # 8-byte aligned only
+    ok = ctypes.c_void_p(0x2000)
+    # quantise / dequantise: unsupported shape, NULL, misaligned
+    assert L.moe_quantize_experts_q4(ok, ok, ok, 128, 8, 256, ok, None) == MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_experts_q4(ok, ok, None, 256, 8, 128, ok, None) == MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_experts_q4(ok, ok, ok, 256, 8, 128, odd, None) == MOE_ERR_ALIGNMENT
+    assert L.moe_dequantize_experts_q4(odd, 256, 8, 128, ok, ok, ok, None) == MOE_ERR_ALIGNMENT
+    assert L.moe_dequantize_experts_q4(ok, 256, 8, 192, ok, ok, ok, None) == MOE_ERR_INVALID_ARG
+    # forward: unsupported shape, misaligned buffer
+    fwd = (ok, 4, 256, ok)
+    rest = (ok, ok, ok, ok, ok, ok, 0, None)
+    assert L.moe_forward_q4(*fwd, ok, 8, 2, 192, 1, *rest) == MOE_ERR_INVALID_ARG
+    assert L.moe_forward_q4(*fwd, odd, 8, 2, 128, 1, *rest) == MOE_ERR_ALIGNMENT
+    # options: 4-bit and packed weights together, 4-bit with an unsupported shape
+    both = _Options(None, 0x2000, None, 0, 0.0, 0x4000)
+    assert L.moe_forward_opts(*fwd, None, None, None, 8, 2, 128, 1, ok, ok, ok, ok, ok,
+                              ctypes.byref(both), None) == MOE_ERR_INVALID_ARG
+    bad_shape = _Options(None, None, None, 0, 0.0, 0x4000)
+    assert L.moe_forward_opts(*fwd, None, None, None, 8, 2, 192, 1, ok, ok, ok, ok, ok,
+                              ctypes.byref(bad_shape), None) == MOE_ERR_INVALID_ARG
+    misaligned = _Options(None, None, None, 0, 0.0, 0x4008)
+    assert L.moe_forward_opts(*fwd, None, None, None, 8, 2, 128, 1, ok, ok, ok, ok, ok,
+                              ctypes.byref(misaligned), None) == MOE_ERR_ALIGNMENT
