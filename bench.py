@@ -583,21 +583,11 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4=None)
     out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     lg_h = torch.empty((T, E), dtype=torch.float32).pin_memory()
     aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
-    if q4 is not None:  # no host-memory 4-bit entry: copies around moe_forward_q4
-        x_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        out_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        lg_d = torch.empty((T, E), dtype=torch.float32, device=dev)
-        aux_d = torch.empty(1, dtype=torch.float32, device=dev)
 
     def call():
         if q4 is not None:
-            x_d.copy_(x_h, non_blocking=True)
-            moe.moe_forward_q4(x_d, inp["W_router"], q4, K, cfg.norm, out=out_d,
-                               router_logits=lg_d, aux=aux_d)
-            out_h.copy_(out_d, non_blocking=True)
-            lg_h.copy_(lg_d, non_blocking=True)
-            aux_h.copy_(aux_d, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+            moe.moe_forward_host_q4(x_h, inp["W_router"], q4, K, cfg.norm, out_h,
+                                    router_logits_host=lg_h, aux_host=aux_h)
         elif packed is not None:
             moe.moe_forward_host_packed(x_h, inp["W_router"], packed, K, cfg.norm, out_h,
                                         router_logits_host=lg_h, aux_host=aux_h)
@@ -619,7 +609,7 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4=None)
     mean = max_over_ranks(mean, world, dev)
     return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
             "d2h_bytes_per_step": T * H * 2 + T * E * 4 + 4, "ms_per_step": mean * 1e3,
-            "api": ("pinned copies around moe_forward_q4" if q4 is not None
+            "api": ("moe_forward_host_q4" if q4 is not None
                     else "moe_forward_host_packed" if packed is not None else "moe_forward_host")
                    + " (pinned host x in; out, router_logits, aux out)"}
 

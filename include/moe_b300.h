@@ -246,6 +246,14 @@ int moe_forward_q4(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
                    moe_bf16* out, float* router_logits, int32_t* topk_idx, float* topk_w,
                    float* aux, void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_forward_host with 4-bit expert weights (q4_experts on the device, from
+ * moe_quantize_experts_q4 with the same H, E, I); host buffers and errors as
+ * moe_forward_host, shapes and kernels as moe_forward_q4. */
+int moe_forward_host_q4(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                        const void* q4_experts, int E, int K, int I, int norm_topk_prob,
+                        moe_bf16* out_host, float* router_logits_host, int32_t* topk_idx_host,
+                        float* topk_w_host, float* aux_host, void* stream);
+
 /* ---- forward with options ------------------------------------------------ */
 
 /* Optional inputs of moe_forward_opts; a zero-initialised struct (or a NULL
@@ -292,8 +300,8 @@ int moe_forward_opts(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
 
 /* Per-expert pair counts ("expert utilisation histogram") of the last
  * forward on `stream` that used the library-owned workspace (moe_forward,
- * moe_forward_host, moe_forward_host_packed, moe_forward_packed without a
- * workspace), copied into counts_host[E]
+ * moe_forward_host, moe_forward_host_packed, moe_forward_host_q4, and
+ * moe_forward_packed / moe_forward_q4 without a workspace), copied into counts_host[E]
  * (waits for the stream).  MOE_ERR_INVALID_ARG if there was no such call. */
 int moe_last_expert_counts(int32_t* counts_host, int E, void* stream);
 

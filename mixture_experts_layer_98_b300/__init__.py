@@ -9,7 +9,8 @@ from .binding import (EXPORTS, LIB_PATH, MOE_PATH_AUTO, MOE_PATH_STREAMING,  # n
                       MOE_PATH_WARP_MMA,
                       MOE_PATH_TCGEN05_WT, MoEError,
                       PackedExperts, Q4Experts, lib, moe_dequantize_experts_q4,
-                      moe_forward_q4, moe_q4_experts_bytes, moe_quantize_experts_q4,
+                      moe_forward_q4, moe_forward_host_q4, moe_q4_experts_bytes,
+                      moe_quantize_experts_q4,
                       moe_dbg_combine, moe_dbg_permute, moe_dbg_wait_timeout, moe_forward_host_packed,
                       moe_forward_opts, moe_forward_packed, moe_pack_experts, moe_packed_experts_bytes,
                       moe_dbg_route_from_logits, moe_device_status, moe_forward,

@@ -30,6 +30,7 @@ EXPORTS = ["moe_forward", "moe_forward_noalloc", "moe_workspace_bytes", "moe_for
            "moe_packed_experts_bytes", "moe_pack_experts", "moe_forward_packed",
            "moe_forward_host_packed", "moe_forward_opts", "moe_q4_experts_bytes",
            "moe_quantize_experts_q4", "moe_dequantize_experts_q4", "moe_forward_q4",
+           "moe_forward_host_q4",
            "moe_last_expert_counts", "moe_device_status", "moe_strerror", "moe_last_cuda_error",
            "moe_set_expert_path", "moe_set_stage_timing", "moe_set_next_stage_events",
            "moe_stage_times",
@@ -84,6 +85,7 @@ def lib():
         L.moe_quantize_experts_q4.argtypes = [P, P, P, i, i, i, P, P]
         L.moe_dequantize_experts_q4.argtypes = [P, i, i, i, P, P, P, P]
         L.moe_forward_q4.argtypes = pfwd + [P, sz, P]
+        L.moe_forward_host_q4.argtypes = pfwd + [P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
         L.moe_last_expert_counts.argtypes = [P, i, P]
@@ -316,6 +318,28 @@ def moe_forward_q4(x, W_router, q4, K, norm_topk_prob, out=None, router_logits=N
                                0 if workspace is None else workspace.numel(),
                                _stream(stream)), "moe_forward_q4")
     return out, router_logits, topk_idx, topk_w, aux
+
+
+def moe_forward_host_q4(x_host, W_router, q4, K, norm_topk_prob, out_host,
+                        router_logits_host=None, topk_idx_host=None, topk_w_host=None,
+                        aux_host=None, stream=None):
+    """moe_forward_host with Q4Experts weights."""
+    T, H = x_host.shape
+    if q4.H != H:
+        raise ValueError("x_host and the 4-bit weights disagree on H")
+    _dev(W_router, torch.bfloat16, "W_router", (q4.E, H))
+    for n, t in (("x_host", x_host), ("out_host", out_host), ("router_logits_host",
+                                                            router_logits_host),
+                 ("topk_idx_host", topk_idx_host), ("topk_w_host", topk_w_host),
+                 ("aux_host", aux_host)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    _call(lib().moe_forward_host_q4(_ptr(x_host), T, H, _ptr(W_router), _ptr(q4.data), q4.E, K,
+                                    q4.I, int(bool(norm_topk_prob)), _ptr(out_host),
+                                    _ptr(router_logits_host), _ptr(topk_idx_host),
+                                    _ptr(topk_w_host), _ptr(aux_host), _stream(stream)),
+          "moe_forward_host_q4")
+    return out_host
 
 
 def moe_forward_opts(x, W_router, W_gate, W_up, W_down, K, norm_topk_prob, expert_bias=None,

@@ -693,6 +693,20 @@ int moe_forward_host_packed(const moe_bf16* x_host, int T, int H, const moe_bf16
                         (cudaStream_t)stream);
 }
 
+int moe_forward_host_q4(const moe_bf16* x_host, int T, int H, const moe_bf16* W_router,
+                        const void* q4_experts, int E, int K, int I, int norm_topk_prob,
+                        moe_bf16* out_host, float* router_logits_host, int32_t* topk_idx_host,
+                        float* topk_w_host, float* aux_host, void* stream) {
+    if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
+    if (!moe_q4_experts_bytes(H, E, I)) return MOE_ERR_INVALID_ARG;
+    if (misaligned(q4_experts)) return MOE_ERR_ALIGNMENT;
+    ExpertWeights W{nullptr, nullptr, nullptr, nullptr};
+    W.q4 = (const char*)q4_experts;
+    return forward_host(x_host, T, H, W_router, W, q4_experts, q4_experts, q4_experts, E, K, I,
+                        norm_topk_prob, nullptr, 0, out_host, router_logits_host, topk_idx_host,
+                        topk_w_host, aux_host, (cudaStream_t)stream);
+}
+
 int moe_last_expert_counts(int32_t* counts_host, int E, void* stream) {
     if (!counts_host || E < 1) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;

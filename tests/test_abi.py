@@ -162,6 +162,11 @@ def test_q4_argument_checks(L):
     bad_shape = _Options(None, None, None, 0, 0.0, 0x4000)
     assert L.moe_forward_opts(*fwd, None, None, None, 8, 2, 192, 1, ok, ok, ok, ok, ok,
                               ctypes.byref(bad_shape), None) == MOE_ERR_INVALID_ARG
+    # host-buffer entry: unsupported shape, misaligned buffer
+    assert L.moe_forward_host_q4(*fwd, ok, 8, 2, 192, 1, ok, ok, ok, ok, ok,
+                                 None) == MOE_ERR_INVALID_ARG
+    assert L.moe_forward_host_q4(*fwd, odd, 8, 2, 128, 1, ok, ok, ok, ok, ok,
+                                 None) == MOE_ERR_ALIGNMENT
     misaligned = _Options(None, None, None, 0, 0.0, 0x4008)
     assert L.moe_forward_opts(*fwd, None, None, None, 8, 2, 128, 1, ok, ok, ok, ok, ok,
                               ctypes.byref(misaligned), None) == MOE_ERR_ALIGNMENT

@@ -186,6 +186,30 @@ def test_q4_forward_against_the_oracle(moe, T, H, E, K, I, norm, kernel):
     compare(b, g, K, norm)
 
 
+@pytest.mark.parametrize("name", ["decode_t4", "prefill_small"])
+def test_q4_host_entry_is_the_device_entry(moe, name):
+    # moe_forward_host_q4 copies x in, runs the same kernels, copies the
+    # results out: bitwise the device-buffer call's results
+    cfg = (mi.MoEConfig("prefill_small", 1024, 512, 16, 4, 256, True, seed=5)
+           if name == "prefill_small" else mi.CONFIGS[name])
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    out, lg, idx, w, aux = [t.clone() for t in
+                            moe.moe_forward_q4(inp["x"], inp["W_router"], q4, cfg.K, cfg.norm)]
+    torch.cuda.synchronize()
+    x_h = inp["x"].cpu().pin_memory()
+    out_h = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    lg_h = torch.empty((cfg.T, cfg.E), dtype=torch.float32).pin_memory()
+    idx_h = torch.empty((cfg.T, cfg.K), dtype=torch.int32).pin_memory()
+    w_h = torch.empty((cfg.T, cfg.K), dtype=torch.float32).pin_memory()
+    aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    moe.moe_forward_host_q4(x_h, inp["W_router"], q4, cfg.K, cfg.norm, out_h,
+                            router_logits_host=lg_h, topk_idx_host=idx_h, topk_w_host=w_h,
+                            aux_host=aux_h)
+    for dev, host in ((out, out_h), (lg, lg_h), (idx, idx_h), (w, w_h), (aux, aux_h)):
+        assert torch.equal(dev.cpu(), host)
+
+
 def test_q4_rejects_unsupported_shapes(moe):
     assert moe.moe_q4_experts_bytes(4096, 128, 1536) > 0
     assert moe.moe_q4_experts_bytes(128, 8, 256) == 0   # H % 256 != 0
