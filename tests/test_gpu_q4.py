@@ -186,6 +186,28 @@ def test_q4_forward_against_the_oracle(moe, T, H, E, K, I, norm, kernel):
     compare(b, g, K, norm)
 
 
+@pytest.mark.parametrize("name,kernel", [("decode_t1", "warp_mma"), ("decode_t1", "tcgen05"),
+                                         ("mixtral_decode_t1", "warp_mma")])
+def test_q4_full_size_against_the_oracle(moe, name, kernel):
+    # a full decode layer: the oracle quantises, with its own quantiser, the
+    # experts the GPU selected (a selection the oracle does not share fails the
+    # index check) and runs the whole block on the dequantised weights
+    cfg = mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, "cuda")
+    q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
+    out, lg, idx, w, aux = _q4_forward(moe, KERNELS[kernel], inp["x"], inp["W_router"], q4,
+                                       cfg.K, cfg.norm)
+    torch.cuda.synchronize()
+    b = host_bits(inp)
+    chosen = sorted(set(idx.cpu().numpy().ravel().tolist()))
+    for m in ("W_gate", "W_up", "W_down"):
+        for e in chosen:
+            b[m][e] = oracle.dequantize_q4(*oracle.quantize_q4(b[m][e]))
+    g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
+             w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
+    compare(b, g, cfg.K, cfg.norm)
+
+
 @pytest.mark.parametrize("name", ["decode_t4", "prefill_small"])
 def test_q4_host_entry_is_the_device_entry(moe, name):
     # moe_forward_host_q4 copies x in, runs the same kernels, copies the
