@@ -4,17 +4,29 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
 A step is one whole forward (router, dispatch, expert MLPs, combine, aux) of
-one synthetic batch of the named layer configuration (default: the Qwen3-style
-prefill layer T=4096 H=2048 E=128 K=8 I=768), inputs resident in HBM.  The K
-timed steps are enqueued back to back (no host wait inside the timed region)
-and each is timed on the device with CUDA events on the launch stream; L2 is
-flushed (256 MB write) between steps, outside the events.  A second pass of K
-steps has the library record stage-boundary events on the same stream, giving
-the live per-kernel times of the roofline object and the stage split (those
-events serialise the boundaries they sit on, so they stay out of the first
-pass).  With N > 1 (torchrun)
-every rank runs an independent replica on its own batch (weak scaling, no
-collective on the data path); value = all ranks' tokens / max-over-ranks time.
+one synthetic batch of the named layer configuration, inputs resident in HBM.
+The default is the skewed-routing layer (T=16384 H=4096 E=128 K=8 I=1536,
+expert loads following Zipf(1.2)), the largest configuration of the workload
+set that fits one GPU; the same line carries the large-expert prefill layer
+(T=8192) and the decode sweep (T = 1, 4, 16, 64 on the same layer, timed as
+CUDA-graph replays, the way a decode server runs) under "extra_configs", each
+measured the same way.  The K timed steps are enqueued back to back (no host
+wait inside the timed region) and each is timed on the device with CUDA events
+on the launch stream; L2 is flushed (256 MB write) between steps, outside the
+events.  A second pass of K steps has the library record stage-boundary events
+on the same stream, giving the live per-kernel times of the roofline object and
+the stage split (those events serialise the boundaries they sit on, so they
+stay out of the first pass).  With N > 1 (torchrun) every rank runs an
+independent replica on its own batch (weak scaling, no collective on the data
+path); value = all ranks' tokens / max-over-ranks time.
+
+Roofline: algorithmic work only -- routed FLOPs, the touched experts' weights,
+the router weights and the block's own inputs and outputs (x read once, out,
+logits, top-k); the intermediates x_perm, h and Y are implementation overhead
+and count for nothing.  Fractions are against the measured burst bf16 peak and
+the measured copy bandwidth (MEASURED_PEAKS.json); the fraction against the
+sustained bf16 figure (cuBLAS looped for seconds under the power limit) is
+reported beside it.
 
 --impl reference times the CPU oracle (the plain fp64 C implementation) on
 bounded token samples of the same workload, on the host cores.
@@ -59,7 +71,9 @@ def parse(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="prefill_h2048", choices=sorted(mi.CONFIGS))
+    ap.add_argument("--config", default="skew", choices=sorted(mi.CONFIGS))
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the main configuration only (no extra_configs)")
     ap.add_argument("--shape", default=None,
                     help="T,H,E,K,I: a custom layer (norm_topk_prob on, seed 0) instead of --config, "
                          "for small profiling cases")
@@ -71,6 +85,8 @@ def parse(argv=None):
     ap.add_argument("--quiet-clocks", action="store_true", help="skip nvidia-smi sampling")
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: oracle seconds per step (default: ~150 s in total)")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0,
+                    help="warm-up lasts at least W steps and this long (0 for profiling runs)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the forward captured as a CUDA graph (decode serving)")
     ap.add_argument("--weights", default="packed", choices=["packed", "row-major", "q4"],
@@ -153,7 +169,13 @@ WEIGHT_BYTES = {"bf16": 2.0, "q4": 0.5 + 4.0 / 128}
 
 
 def stage_work(cfg, counts, fused=False, wb=2.0):
-    """fused: the decode kernel runs gate/up, down and the combine in one launch,
+    """Algorithmic work of each stage's kernel per launch: FLOPs of the
+    contractions it computes and the bytes of the block's own tensors it must
+    touch (expert and router weights, x read once, out, logits, top-k).  The
+    intermediates x_perm, h and Y are implementation overhead and count for
+    nothing, so the stages that only move them (dispatch's gather, combine's
+    reads) carry only the block outputs they write.
+    fused: the decode kernel runs gate/up, down and the combine in one launch,
     timed as the gate_up stage, so that stage carries all three stages' work.
     wb: bytes per expert weight."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
@@ -161,10 +183,10 @@ def stage_work(cfg, counts, fused=False, wb=2.0):
     touched = int((np.asarray(counts) > 0).sum())
     w = {
         "router": dict(flops=2.0 * T * H * E, bytes=T * H * 2 + E * H * 2 + T * E * 4 + T * K * 8),
-        "dispatch": dict(flops=0.0, bytes=T * K * 8 + P * 16 + P * H * 2 * 2),
-        "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * wb + P * H * 2 + P * I * 2),
-        "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * wb + P * I * 2 + P * 4 + P * H * 2),
-        "combine": dict(flops=0.0, bytes=P * H * 2 + P * 4 + T * H * 2),
+        "dispatch": dict(flops=0.0, bytes=T * K * 8 + 4),
+        "gate_up": dict(flops=4.0 * P * H * I, bytes=touched * 2 * I * H * wb + T * H * 2),
+        "down": dict(flops=2.0 * P * I * H, bytes=touched * H * I * wb),
+        "combine": dict(flops=0.0, bytes=T * H * 2),
     }
     if fused:
         w["gate_up"] = {k: w["gate_up"][k] + w["down"][k] + w["combine"][k] for k in ("flops", "bytes")}
@@ -180,6 +202,53 @@ def block_work(cfg, counts, wb=2.0):
     flops = 6.0 * T * K * H * I + 2.0 * T * H * E
     byts = touched * 3 * H * I * wb + E * H * 2 + T * H * 2 * 2 + T * E * 4 + T * K * 8 + 4
     return flops, byts
+
+
+def roofline_of(work, stage_mean, path_name, pk, cfg):
+    """The roofline object of the dominant stage's kernel: algorithmic work per
+    launch over its live mean duration, against the burst tensor peak or the
+    copy bandwidth, whichever bound is slower."""
+    dom = max(stage_mean, key=stage_mean.get)
+    wk = work[dom]
+    t_s = stage_mean[dom] * 1e-3
+    t_flop = wk["flops"] / (pk["bf16_tflops"] * 1e12)
+    t_byte = wk["bytes"] / (pk["hbm_gbs"] * 1e9)
+    if t_flop >= t_byte:
+        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+        if pk["bf16_tflops_sustained"]:
+            roof["frac_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
+    else:
+        roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(dom, cfg.name)
+    roof["kernel"] = "experts_fused" if (dom == "gate_up" and path_name == "tcgen05_decode") else dom
+    roof["kernel_ms"] = stage_mean[dom]
+    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
+    roof["peak_source"] = pk["source"] + (
+        " burst bf16 (frac); sustained bf16 beside it (frac_sustained)" if roof["bound"] == "tensor"
+        else " copy bandwidth")
+    return roof
+
+
+def block_roofline_of(cfg, counts, wb, mean_ms, pk):
+    bf, bb = block_work(cfg, counts, wb=wb)
+    t = mean_ms * 1e-3
+    t_tc = bf / (pk["bf16_tflops"] * 1e12)
+    t_hbm = bb / (pk["hbm_gbs"] * 1e9)
+    t_roof = max(t_tc, t_hbm)
+    out = {"flops": bf, "bytes": bb, "t_roof_us": t_roof * 1e6, "t_us": mean_ms * 1e3,
+           "bound": "tensor" if t_tc >= t_hbm else "hbm",
+           "frac": t_roof / t,
+           "tensor_frac": bf / t / (pk["bf16_tflops"] * 1e12),
+           "hbm_frac": bb / t / (pk["hbm_gbs"] * 1e9),
+           "touched_experts": int((np.asarray(counts) > 0).sum()),
+           "peaks": "burst bf16 and copy bandwidth (frac); sustained bf16 (frac_sustained)"}
+    if pk["bf16_tflops_sustained"]:
+        t_roof_s = max(bf / (pk["bf16_tflops_sustained"] * 1e12), t_hbm)
+        out["frac_sustained"] = t_roof_s / t
+    return out
 
 
 def kernel_source_sha(stage):
@@ -340,15 +409,14 @@ def config_block(cfg, world):
 
 # ---- our arm ------------------------------------------------------------------------
 
-def run_ours(args, world, rank, local):
-    import mixture_experts_layer_98_b300 as moe
-    from mixture_experts_layer_98_b300 import build
-    if rank == 0:
-        build.build()
-    barrier(world)
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    cfg = workload(args)
+# The same line's extra configurations: (name, timed as CUDA-graph replays)
+EXTRA_CONFIGS = [("prefill_h4096", False), ("decode_t1", True), ("decode_t4", True),
+                 ("decode_t16", True), ("decode_t64", True)]
+
+
+def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clocks):
+    """Times K forwards of cfg (after warm-up) and a second pass with stage
+    events; returns the fields of one result (main line or extra entry)."""
     inp = mi.make_inputs(cfg, dev, seed=replica_seed(cfg, rank))
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -358,9 +426,6 @@ def run_ours(args, world, rank, local):
     aux = torch.empty((1,), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3,
-                             "tcgen05_pair": 4, "tcgen05_decode": 5,
-                             "warp_mma": 6}[args.expert_path])
 
     packed = None
     q4 = None
@@ -396,7 +461,7 @@ def run_ours(args, world, rank, local):
     eager()
     launches_per_step = moe.moe_kernel_launch_count() - n0
     step = eager
-    if args.graph:
+    if graph:
         # A serving loop replays the captured forward: the caller owns the
         # workspace, and the host enqueues one graph launch per step.
         ws = torch.empty(moe.moe_workspace_bytes(T, H, E, K, I), dtype=torch.uint8, device=dev)
@@ -406,13 +471,13 @@ def run_ours(args, world, rank, local):
 
         fwd_ws()
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
             fwd_ws()
-        step = graph.replay
+        step = cg.replay
 
     # warm-up: at least W steps and at least ~1 s of work so clocks settle
-    t_end = time.time() + 1.0
+    t_end = time.time() + args.warmup_seconds
     n = 0
     while n < max(3, args.warmup) or time.time() < t_end:
         step()
@@ -428,7 +493,7 @@ def run_ours(args, world, rank, local):
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
-    if not args.quiet_clocks:
+    if want_clocks:
         sampler.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -443,9 +508,9 @@ def run_ours(args, world, rank, local):
     barrier(world)
     t1 = time.time()
     launches = moe.moe_kernel_launch_count() - launches0
-    if args.graph:  # graph replays bypass the library's launch counter
+    if graph:  # graph replays bypass the library's launch counter
         launches = launches_per_step * args.steps
-    rows = sampler.stop() if not args.quiet_clocks else None
+    rows = sampler.stop() if want_clocks else None
     clocks = ClockSampler.summarize(rows, t0, t1) if rows is not None else {"reasons": ["unsampled"]}
 
     # Second timed pass, same workload: per-step stage-boundary events recorded
@@ -476,75 +541,81 @@ def run_ours(args, world, rank, local):
     wb = WEIGHT_BYTES["q4" if q4 is not None else "bf16"]
     work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode", wb=wb)
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
-    dom = max(stage_mean, key=stage_mean.get)
-    wk = work[dom]
-    t_s = stage_mean[dom] * 1e-3
-    # The kernels run inside >= 1 s of back-to-back forwards (the warm-up alone
-    # lasts >= 1 s), i.e. under the board's sustained power limit: a tensor-bound
-    # kernel is measured against the sustained bf16 figure (cuBLAS looped for
-    # seconds), with the burst fraction beside it.
-    tflops = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
-    t_flop = wk["flops"] / (tflops * 1e12)
-    t_byte = wk["bytes"] / (pk["hbm_gbs"] * 1e9)
-    if t_flop >= t_byte:
-        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": tflops,
-                "unit": "TFLOP/s"}
-        roof["frac_burst"] = roof["achieved"] / pk["bf16_tflops"]
-    else:
-        roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_for(dom, cfg.name)
-    roof["kernel"] = "experts_fused" if (dom == "gate_up" and path_name == "tcgen05_decode") else dom
-    roof["kernel_ms"] = stage_mean[dom]
-    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
-    roof["peak_source"] = pk["source"] + (
-        " (tensor: sustained bf16 figure -- the step runs inside >= 1 s of back-to-back "
-        "forwards; frac_burst against the burst figure)" if roof["bound"] == "tensor" else
-        " (HBM: measured copy bandwidth)")
-    bf, bb = block_work(cfg, counts, wb=wb)
-    t_roof = max(bf / (tflops * 1e12), bb / (pk["hbm_gbs"] * 1e9))
-    t_roof_burst = max(bf / (pk["bf16_tflops"] * 1e12), bb / (pk["hbm_gbs"] * 1e9))
-    block = {"flops": bf, "bytes": bb, "t_roof_us": t_roof * 1e6, "t_us": mean_ms * 1e3,
-             "frac": t_roof / (mean_ms * 1e-3),
-             "frac_burst": t_roof_burst / (mean_ms * 1e-3),
-             "tensor_frac": bf / (mean_ms * 1e-3) / (tflops * 1e12),
-             "tensor_frac_burst": bf / (mean_ms * 1e-3) / (pk["bf16_tflops"] * 1e12),
-             "hbm_frac": bb / (mean_ms * 1e-3) / (pk["hbm_gbs"] * 1e9),
-             "touched_experts": touched,
-             "peaks": "HBM measured copy; tensor sustained (frac) and burst (frac_burst)"}
+    roof = roofline_of(work, stage_mean, path_name, pk, cfg)
+    block = block_roofline_of(cfg, counts, wb, mean_ms, pk)
 
     e2e = None
-    if not args.no_e2e:
+    if want_e2e:
         e2e = e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4)
+    res = {
+        "value": value, "unit": UNIT, "ms_per_step": mean_ms_all,
+        "launch": "CUDA graph replay" if graph else "eager launches",
+        "expert_weights": (
+            "quantised once to 4 bits, groups of 128 with a bf16 scale and bias "
+            "(moe_quantize_experts_q4, a model-load step)" if q4 is not None
+            else "packed once into the tile-major layout before timing "
+                 "(moe_pack_experts, a model-load step)" if packed is not None
+            else "row-major"),
+        "roofline": roof, "block_roofline": block, "e2e": e2e, "gpu_launches": launches,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
+        "stage_ms": {k: round(v, 5) for k, v in stage_mean.items()},
+        "expert_path": path_name,
+    }
+    bits = {k: mi.bits(v) for k, v in inp.items()} if (rank == 0 and world == 1) else None
+    del inp, out, logits, idx, w, aux, flush, packed, q4
+    torch.cuda.empty_cache()
+    return res, bits
+
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_layer_98_b300 as moe
+    from mixture_experts_layer_98_b300 import build
+    if rank == 0:
+        build.build()
+    barrier(world)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    moe.moe_set_expert_path({"auto": 0, "streaming": 1, "tcgen05": 2, "tcgen05_wt": 3,
+                             "tcgen05_pair": 4, "tcgen05_decode": 5,
+                             "warp_mma": 6}[args.expert_path])
+    cfg = workload(args)
+    main, bits = measure(moe, cfg, args, world, rank, local, dev, graph=args.graph,
+                         want_e2e=not args.no_e2e, want_clocks=not args.quiet_clocks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        bits = {k: mi.bits(v) for k, v in inp.items()}
         rate, n, dt, threads = oracle_sample_rate(cfg, bits, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"first {n} of {T} tokens of {cfg.name} (full forward for those tokens), "
-                         f"{dt:.1f} s, fp64 C oracle"}
+               "sample": f"first {n} of {cfg.T} tokens of {cfg.name} (full forward for those "
+                         f"tokens), {dt:.1f} s, fp64 C oracle"}
+    del bits
+
+    extras = {}
+    if not args.no_extras and not args.shape:
+        for name, graph in EXTRA_CONFIGS:
+            if name == cfg.name:
+                continue
+            ecfg = mi.CONFIGS[name]
+            r, _ = measure(moe, ecfg, args, world, rank, local, dev, graph=graph, want_e2e=False,
+                           want_clocks=not args.quiet_clocks)
+            r.pop("e2e")
+            r["config"] = config_block(ecfg, world)["workload"]
+            extras[name] = r
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(config_block(cfg, world),
-                           launch="CUDA graph replay" if args.graph else "eager launches",
-                           expert_weights=(
-                               "quantised once to 4 bits, groups of 128 with a bf16 scale and "
-                               "bias (moe_quantize_experts_q4, a model-load step)" if q4 is not None
-                               else "packed once into the tile-major layout before timing "
-                               "(moe_pack_experts, a model-load step)" if packed is not None
-                               else "row-major")),
-            "roofline": roof, "block_roofline": block,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
-                       "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
-            "stage_ms": {k: round(v, 5) for k, v in stage_mean.items()},
-            "expert_path": path_name,
+            "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(config_block(cfg, world), launch=main["launch"],
+                           expert_weights=main["expert_weights"]),
+            "roofline": main["roofline"], "block_roofline": main["block_roofline"],
+            "cpu_baseline": cpu, "e2e": main["e2e"], "gpu_launches": main["gpu_launches"],
+            "clocks": main["clocks"], "stage_ms": main["stage_ms"],
+            "expert_path": main["expert_path"],
+            "extra_configs": extras,
         }
         print(json.dumps(line), flush=True)
 
@@ -607,8 +678,33 @@ def e2e_measure(moe, inp, cfg, args, stream, flush, world, dev, packed, q4=None)
         times.append(time.perf_counter() - t)
     mean = sum(times) / len(times)
     mean = max_over_ranks(mean, world, dev)
-    return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
-            "d2h_bytes_per_step": T * H * 2 + T * E * 4 + 4, "ms_per_step": mean * 1e3,
+    # the link alone: the same bytes as plain pinned copies, one way at a time
+    x_d = torch.empty_like(inp["x"])
+    out_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    lg_d = torch.empty((T, E), dtype=torch.float32, device=dev)
+
+    def timed(fn, n=5):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n):
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t)
+        return min(ts)
+
+    t_h2d = timed(lambda: x_d.copy_(x_h, non_blocking=True))
+    t_d2h = timed(lambda: (out_h.copy_(out_d, non_blocking=True),
+                           lg_h.copy_(lg_d, non_blocking=True)))
+    h2d_b, d2h_b = T * H * 2, T * H * 2 + T * E * 4 + 4
+    return {"value": T * world / mean, "unit": UNIT, "h2d_bytes_per_step": h2d_b,
+            "d2h_bytes_per_step": d2h_b, "ms_per_step": mean * 1e3,
+            "link": {"h2d_gbs": h2d_b / t_h2d / 1e9, "d2h_gbs": (d2h_b - 4) / t_d2h / 1e9,
+                     "copy_ms": (t_h2d + t_d2h) * 1e3,
+                     "note": "plain pinned copies of the same bytes, best of 5; the routing "
+                             "outputs are copied back while the experts run, so e2e can "
+                             "undercut device time + copy_ms by their share"},
             "api": ("moe_forward_host_q4" if q4 is not None
                     else "moe_forward_host_packed" if packed is not None else "moe_forward_host")
                    + " (pinned host x in; out, router_logits, aux out)"}

@@ -99,8 +99,10 @@ int moe_forward(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
  *
  * Scratch: a 32 MiB array that is part of the loaded library (a __device__
  * variable), so nothing is allocated by the call.  Every GPU that loads the
- * library holds those 32 MiB until the process exits.  Sizes whose
- * moe_workspace_bytes(T,H,E,K,I) exceeds 32 MiB are rejected with
+ * library holds those 32 MiB until the process exits.  This call takes no
+ * expert capacity, so it needs the scratch of a forward without one:
+ * moe_workspace_bytes(T,H,E,K,I) less the T·K·H·2 bytes that only a capacity
+ * forward uses.  Sizes whose need exceeds 32 MiB are rejected with
  * MOE_ERR_WORKSPACE before any work (e.g. the H=4096, E=128, K=8, I=1536
  * layer fits up to T = 212 tokens).
  *
@@ -118,7 +120,10 @@ int moe_forward_noalloc(const moe_bf16* x, int T, int H, const moe_bf16* W_route
                         void* stream);
 
 /* Bytes of device workspace moe_forward_ws needs for these sizes (0 on a size
- * error).  The requirement grows with T·K·(H+I); it does not depend on data. */
+ * error).  The requirement grows with T·K·(H+I); it does not depend on data.
+ * It covers every forward of these sizes, including one under an expert
+ * capacity (moe_forward_opts), which keeps the weighted expert outputs in
+ * fp32 (T·K·H·2 bytes more than a forward without a capacity needs). */
 size_t moe_workspace_bytes(int T, int H, int E, int K, int I);
 
 /* moe_forward with caller-provided scratch: `workspace` is device memory of at

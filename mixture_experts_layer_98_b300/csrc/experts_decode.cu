@@ -74,6 +74,7 @@ struct DecParams {
     int32_t* tok_done;     // [T][H/256 * 4] pairs of token t stored, per column block
     __nv_bfloat16* h;      // [P, I]
     __nv_bfloat16* y;      // [P, H] token-major
+    float* y32;            // the same as fp32 under a capacity (null: bf16 y)
     __nv_bfloat16* out;    // [T, H]
     const float* w_perm;
     const int32_t* perm_tok;
@@ -110,9 +111,15 @@ __device__ __forceinline__ void store_out(const DecParams& p, int kind, size_t r
     } else {
         const float wr = p.w_perm[row];
         const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
-        __nv_bfloat16* o = p.y + yrow * p.H + (size_t)blk * (2 * kWM);
-        o[i] = __float2bfloat16_rn(wr * d0);
-        o[kWM + i] = __float2bfloat16_rn(wr * d1);
+        if (p.y32) {
+            float* o = p.y32 + yrow * p.H + (size_t)blk * (2 * kWM);
+            o[i] = wr * d0;
+            o[kWM + i] = wr * d1;
+        } else {
+            __nv_bfloat16* o = p.y + yrow * p.H + (size_t)blk * (2 * kWM);
+            o[i] = __float2bfloat16_rn(wr * d0);
+            o[kWM + i] = __float2bfloat16_rn(wr * d1);
+        }
     }
 }
 
@@ -457,8 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int k = 0; k < kMaxTopK; ++k) {
                                 const size_t pr = (size_t)t * p.K + k;
                                 kp[k] = k < p.K && (!p.inv || __ldcg(p.inv + pr) >= 0);
-                                v0[k] = kp[k] ? ld_bf16_cg(p.y + pr * p.H + c0) : 0.f;
-                                v1[k] = kp[k] ? ld_bf16_cg(p.y + pr * p.H + c1) : 0.f;
+                                if (p.y32) {
+                                    v0[k] = kp[k] ? __ldcg(p.y32 + pr * p.H + c0) : 0.f;
+                                    v1[k] = kp[k] ? __ldcg(p.y32 + pr * p.H + c1) : 0.f;
+                                } else {
+                                    v0[k] = kp[k] ? ld_bf16_cg(p.y + pr * p.H + c0) : 0.f;
+                                    v1[k] = kp[k] ? ld_bf16_cg(p.y + pr * p.H + c1) : 0.f;
+                                }
                             }
                             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -523,6 +535,7 @@ cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const 
     p.tok_done = p.h_ready + pl.n_ready;
     p.h = ws.hbuf;
     p.y = ws.ybuf;
+    p.y32 = ws.ybuf_f32;
     p.out = out;
     p.w_perm = ws.w_perm;
     p.perm_tok = ws.perm_tok;

@@ -85,6 +85,7 @@ struct PairParams {
     const int32_t* perm_tok;
     const int32_t* perm_slot;
     int K;
+    float* out32;           // down: fp32 Y [P, H] (under a capacity); null: bf16 Y in out
 };
 
 __device__ __forceinline__ void store8(__nv_bfloat16* dst, const float (&v)[8]) {
@@ -345,7 +346,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c, v);
                     ptx::tmem_ld_wait();
-                    if (valid) {
+                    if (valid && p.out32) {
+                        float4* dst = reinterpret_cast<float4*>(
+                            p.out32 + yrow * p.out_ld + (size_t)nt * kBN + nh * (kBN / 2) + c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(wr * __uint_as_float(v[4 * j + 0]),
+                                                 wr * __uint_as_float(v[4 * j + 1]),
+                                                 wr * __uint_as_float(v[4 * j + 2]),
+                                                 wr * __uint_as_float(v[4 * j + 3]));
+                    } else if (valid) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             float o[8];
@@ -486,6 +496,7 @@ cudaError_t launch_experts_pair(const ExpertWeights& W, const Sizes& s, const Wo
     p.perm_tok = ws.perm_tok;
     p.perm_slot = ws.perm_slot;
     p.K = s.K;
+    p.out32 = ws.ybuf_f32;
     const void* bd = packed ? (const void*)W.packed_down(s) : W.down;
     return launch_pair<kDown>(ws.hbuf, P, s.I, bd, bd, (uint64_t)s.E * s.H, 128, p,
                               max_tiles * p.n_nt, st);

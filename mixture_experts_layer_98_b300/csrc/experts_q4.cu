@@ -113,6 +113,7 @@ struct Q4Params {
     const int32_t* perm_tok;
     const int32_t* perm_slot;
     int K;
+    float* out32;           // down: fp32 Y [P, H] (under a capacity); null: bf16 Y in out
 };
 
 // Item -> row tile, 256-row weight block, K slice and its k-block range.
@@ -158,6 +159,15 @@ __device__ __forceinline__ void store_cols(const Q4Params& p, size_t row, int nt
     } else {
         const float wr = p.w_perm[row];
         const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
+        if (p.out32) {
+            float4* dst = reinterpret_cast<float4*>(p.out32 + yrow * p.out_ld +
+                                                    (size_t)nt * kBN + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(wr * a[4 * j], wr * a[4 * j + 1], wr * a[4 * j + 2],
+                                     wr * a[4 * j + 3]);
+            return;
+        }
         __nv_bfloat16* dst = p.out + yrow * p.out_ld + (size_t)nt * kBN + c0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -585,6 +595,7 @@ cudaError_t launch_experts_q4(const char* q4, const Sizes& s, const Workspace& w
     p.perm_tok = ws.perm_tok;
     p.perm_slot = ws.perm_slot;
     p.K = s.K;
+    p.out32 = ws.ybuf_f32;
     return launch_q4_any<kDown>(ws.hbuf, P, s.I, p, pl.items_dn * p.ksplit, s.T, st);
 }
 

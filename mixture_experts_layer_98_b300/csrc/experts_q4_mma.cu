@@ -98,6 +98,7 @@ struct MmaParams {
     const int32_t* perm_tok;
     const int32_t* perm_slot;
     int K;
+    float* out32;           // down: fp32 Y [P, H] (under a capacity); null: bf16 Y in out
     int32_t* status;
     const char* codes0;     // first / second 128-row block of an item
     const char* codes1;
@@ -165,8 +166,11 @@ __device__ __forceinline__ void store_one(const MmaParams& p, const RowTile& tl,
         p.out[row * p.out_ld + (size_t)nt * 128 + f] = __float2bfloat16_rn(silu_f(a) * b);
     } else {
         const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
-        p.out[yrow * p.out_ld + (size_t)nt * 256 + plane * 128 + f] =
-            __float2bfloat16_rn(p.w_perm[row] * a);
+        const size_t col = (size_t)nt * 256 + plane * 128 + f;
+        if (p.out32)
+            p.out32[yrow * p.out_ld + col] = p.w_perm[row] * a;
+        else
+            p.out[yrow * p.out_ld + col] = __float2bfloat16_rn(p.w_perm[row] * a);
     }
 }
 
@@ -575,6 +579,7 @@ cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspac
     p.perm_tok = ws.perm_tok;
     p.perm_slot = ws.perm_slot;
     p.K = s.K;
+    p.out32 = ws.ybuf_f32;
     return launch_mma_any<kDown>(ws.hbuf, P, s.I, p, pl.items_dn * p.ksplit, s.T, st);
 }
 

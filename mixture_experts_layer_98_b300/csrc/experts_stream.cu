@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
     const __nv_bfloat16* hbuf, const RowTile* tiles,
     const int32_t* n_tiles_p, const __nv_bfloat16* Wd,
     const float* w_perm, const int32_t* perm_tok, const int32_t* perm_slot, int K,
-    __nv_bfloat16* Y, int H, int I) {
+    __nv_bfloat16* Y, float* Y32, int H, int I) {
     extern __shared__ uint4 hs[];  // [kStreamRows][I/8]
     pdl_trigger();
     pdl_wait();
@@ -174,8 +174,12 @@ __global__ void __launch_bounds__(256) down_stream_kernel(
                     float v = acc[r][m];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                    if (lane == r)
-                        Y[yrow * H + n0 + r] = __float2bfloat16_rn(wr * v);
+                    if (lane == r) {
+                        if (Y32)  // under a capacity: fp32 Y
+                            Y32[yrow * H + n0 + r] = wr * v;
+                        else
+                            Y[yrow * H + n0 + r] = __float2bfloat16_rn(wr * v);
+                    }
                 }
             }
         }
@@ -215,7 +219,7 @@ cudaError_t launch_experts_streaming(const __nv_bfloat16* x, const ExpertWeights
                      (const __nv_bfloat16*)ws.hbuf, (const RowTile*)ws.tiles,
                      (const int32_t*)ws.n_tiles, Wd, (const float*)ws.w_perm,
                      (const int32_t*)ws.perm_tok, (const int32_t*)ws.perm_slot, s.K, ws.ybuf,
-                     s.H, s.I);
+                     ws.ybuf_f32, s.H, s.I);
     count_launches(1);
     return err;
 }

@@ -13,8 +13,9 @@
 //             (the B tile stacks BN/2 gate rows over BN/2 up rows, so one MMA
 //             computes both); epilogue h = bf16(silu(D_gate) · D_up)
 //   down    : D[128, BN] = h[rows, I] · Wd[e, n-block]ᵀ
-//             epilogue Y = bf16(w_row · D), stored token-major (row t*K + k of
-//             the pair in dispatch row r: t = perm_tok[r], k = perm_slot[r])
+//             epilogue Y = bf16(w_row · D) (fp32 under an expert capacity),
+//             stored token-major (row t*K + k of the pair in dispatch row r:
+//             t = perm_tok[r], k = perm_slot[r])
 //
 // Persistent, warp-specialised CTA (one per SM, 192 threads):
 //   warp 0     TMA producer: A tile 128x64 and two B half-tiles (BN/2)x64 per
@@ -63,6 +64,7 @@ struct TcParams {
     const int32_t* perm_tok;
     const int32_t* perm_slot;
     int K;
+    float* out32;           // down: fp32 Y [P, H] (under a capacity); null: bf16 Y in out
 };
 
 template <int MODE, int BN>
@@ -304,7 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c, v);
                     ptx::tmem_ld_wait();
-                    if (valid) {
+                    if (valid && p.out32) {
+                        float4* dst = reinterpret_cast<float4*>(p.out32 + yrow * p.out_ld +
+                                                                (size_t)nt * BN + c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(wr * __uint_as_float(v[4 * j + 0]),
+                                                 wr * __uint_as_float(v[4 * j + 1]),
+                                                 wr * __uint_as_float(v[4 * j + 2]),
+                                                 wr * __uint_as_float(v[4 * j + 3]));
+                    } else if (valid) {
                         uint4* dst = reinterpret_cast<uint4*>(p.out + yrow * p.out_ld +
                                                               (size_t)nt * BN + c);
 #pragma unroll
@@ -413,6 +424,7 @@ cudaError_t launch_experts_tcgen05(const ExpertWeights& W, const Sizes& s, const
     p.perm_tok = ws.perm_tok;
     p.perm_slot = ws.perm_slot;
     p.K = s.K;
+    p.out32 = ws.ybuf_f32;
     if (s.H % 256 == 0) {
         p.n_nt = s.H / 256;
         err = launch_tc<kDown, 256>(ws.hbuf, P, s.I, W.down, W.down, (uint64_t)s.E * s.H, p,

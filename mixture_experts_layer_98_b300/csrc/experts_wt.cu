@@ -90,6 +90,7 @@ struct WtParams {
     const int32_t* perm_tok;
     const int32_t* perm_slot;
     int K;
+    float* out32;           // down: fp32 Y [P, H] (under a capacity); null: bf16 Y in out
 };
 
 // Epilogue of one output row and weight row i of the block: gate/up writes
@@ -102,9 +103,15 @@ __device__ __forceinline__ void store_out(const WtParams& p, size_t row, int blk
     } else {
         const float wr = p.w_perm[row];
         const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
-        __nv_bfloat16* o = p.out + yrow * p.out_ld + (size_t)blk * (2 * kWM);
-        o[i] = __float2bfloat16_rn(wr * d0);
-        o[kWM + i] = __float2bfloat16_rn(wr * d1);
+        if (p.out32) {
+            float* o = p.out32 + yrow * p.out_ld + (size_t)blk * (2 * kWM);
+            o[i] = wr * d0;
+            o[kWM + i] = wr * d1;
+        } else {
+            __nv_bfloat16* o = p.out + yrow * p.out_ld + (size_t)blk * (2 * kWM);
+            o[i] = __float2bfloat16_rn(wr * d0);
+            o[kWM + i] = __float2bfloat16_rn(wr * d1);
+        }
     }
 }
 
@@ -516,6 +523,7 @@ cudaError_t launch_experts_wt(const ExpertWeights& W, const Sizes& s, const Work
     p.perm_tok = ws.perm_tok;
     p.perm_slot = ws.perm_slot;
     p.K = s.K;
+    p.out32 = ws.ybuf_f32;
     return launch_wt<kDown>(W.down, W.down, (uint64_t)s.E * s.H, s.I, ws.hbuf, P, p,
                             pl.items_dn * p.ksplit, st);
 }

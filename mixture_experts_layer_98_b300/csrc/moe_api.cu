@@ -76,7 +76,7 @@ cudaError_t ensure_smem(const void* func, int bytes) {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
+size_t layout_workspace(const Sizes& s, char* base, Workspace* ws, bool y_f32) {
     size_t off = 0;
     auto take = [&](size_t bytes) -> char* {
         char* p = base ? base + off : nullptr;
@@ -110,7 +110,10 @@ size_t layout_workspace(const Sizes& s, char* base, Workspace* ws) {
     w.topk_w = (float*)take(P * 4);
     w.x_perm = (__nv_bfloat16*)take(P * s.H * 2);
     w.hbuf = (__nv_bfloat16*)take(P * s.I * 2);
-    w.ybuf = (__nv_bfloat16*)take(P * s.H * 2);
+    // Y last and unpadded, so that the fp32 form needs exactly P·H·2 bytes more
+    w.ybuf = (__nv_bfloat16*)(base ? base + off : nullptr);
+    w.ybuf_f32 = y_f32 ? (float*)w.ybuf : nullptr;
+    off += P * s.H * (y_f32 ? 4 : 2);
     w.bytes = off;
     if (ws) *ws = w;
     return off;
@@ -163,17 +166,21 @@ struct OwnedWs {
 static std::mutex g_ws_mu;
 static std::unordered_map<unsigned long long, OwnedWs> g_ws;
 
-static unsigned long long ws_key(cudaStream_t st) {
+// slot 0: the forwards' workspace (whose counts and status the query calls
+// read); slot 1: the stage entry points' private scratch, so that a stage call
+// never overwrites what the last forward left for those queries
+static unsigned long long ws_key(cudaStream_t st, int slot = 0) {
     int dev = 0;
     cudaGetDevice(&dev);
-    return ((unsigned long long)(uintptr_t)st) * 64ull + (unsigned long long)dev;
+    return (((unsigned long long)(uintptr_t)st) * 64ull + (unsigned long long)dev) * 2ull +
+           (unsigned long long)slot;
 }
 
 // Returns a workspace of at least `bytes` for `st` (grown with stream-ordered
 // allocation, so earlier work on the stream finishes with the old buffer first).
-static int owned_workspace(cudaStream_t st, size_t bytes, void** out) {
+static int owned_workspace(cudaStream_t st, size_t bytes, void** out, int slot = 0) {
     std::lock_guard<std::mutex> lk(g_ws_mu);
-    OwnedWs& w = g_ws[ws_key(st)];
+    OwnedWs& w = g_ws[ws_key(st, slot)];
     if (w.bytes < bytes) {
         if (w.ptr) {
             cudaError_t e = cudaFreeAsync(w.ptr, st);
@@ -246,7 +253,7 @@ static ExpertPath expert_path(const Sizes& s, bool packed) {
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
                 const Sizes& s, int norm, const float* bias, int cap, __nv_bfloat16* out,
                 float* logits, int32_t* idx, float* w, float* aux, const Workspace& ws,
-                cudaStream_t st) {
+                cudaStream_t st, cudaEvent_t ev_routed) {
     if (!idx) idx = ws.topk_idx;
     if (!w) w = ws.topk_w;
     // 4-bit experts always run their own kernels (tokens as M, weights
@@ -308,6 +315,10 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
+    if (ev_routed) {
+        e = cudaEventRecord(ev_routed, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     cudaEvent_t mid = t_cur_ev[3];
     switch (path) {
         case ExpertPath::kTokensM: e = launch_experts_tcgen05(W, s, ws, st, mid); break;
@@ -333,7 +344,8 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     if (e != cudaSuccess) return cuda_status(e);
     mark(4, st);
     // Y is token-major; with a capacity, inv marks the dropped pairs
-    e = launch_combine(ws.ybuf, cap > 0 ? ws.inv : nullptr, false, s.T, s.K, s.H, out, st);
+    e = launch_combine(ws.ybuf, ws.ybuf_f32, cap > 0 ? ws.inv : nullptr, false, s.T, s.K, s.H,
+                       out, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(5, st);
     if (g_timing) g_timed_once = true;
@@ -375,7 +387,9 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
         return MOE_OK;
     }
     Sizes s{T, H, E, K, I};
-    const size_t need = layout_workspace(s, nullptr, nullptr);
+    // under a capacity the weighted expert outputs stay fp32 until the combine
+    const bool y_f32 = cap > 0;
+    const size_t need = layout_workspace(s, nullptr, nullptr, y_f32);
     const bool owned = workspace == nullptr;
     if (owned) {
         rc = owned_workspace(st, need, &workspace);
@@ -385,16 +399,43 @@ static int forward_device(const void* x, int T, int H, const void* W_router,
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_ALIGNMENT;
     }
     Workspace ws;
-    layout_workspace(s, (char*)workspace, &ws);
+    layout_workspace(s, (char*)workspace, &ws, y_f32);
     rc = run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s, norm, bias,
                      cap, (__nv_bfloat16*)out, logits, idx, w, aux, ws, st);
     if (rc == MOE_OK && owned) remember_counts(st, ws, E);
     return rc;
 }
 
+// A second stream per (device, stream) for the host forward's early copies,
+// and the event after the routing that they wait on (created once, kept).
+struct SideStream {
+    cudaStream_t side = nullptr;
+    cudaEvent_t routed = nullptr;
+};
+static std::mutex g_side_mu;
+static std::unordered_map<unsigned long long, SideStream> g_side;
+
+static int side_stream(cudaStream_t st, SideStream* out) {
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    SideStream& s = g_side[ws_key(st)];
+    if (!s.side) {
+        cudaError_t e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.routed, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            s.side = nullptr;
+            return cuda_status(e);
+        }
+    }
+    *out = s;
+    return MOE_OK;
+}
+
 // The host-pointer forward behind moe_forward_host and moe_forward_host_packed:
 // x is copied in, the forward runs on library-owned scratch, the outputs are
-// copied back, and the call returns after the stream has finished them.
+// copied back, and the call returns after the stream has finished them.  The
+// routing outputs (logits, top-k, aux) are final after the dispatch: they are
+// copied back on a side stream while the expert kernels still run, so only the
+// copy of `out` follows the last kernel.
 static int forward_host(const void* x_host, int T, int H, const void* W_router,
                         const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
                         int E, int K, int I, int norm, const float* bias, int cap,
@@ -414,15 +455,16 @@ static int forward_host(const void* x_host, int T, int H, const void* W_router,
         return MOE_OK;
     }
     Sizes s{T, H, E, K, I};
-    const size_t need = layout_workspace(s, nullptr, nullptr);
+    const bool y_f32 = cap > 0;
+    const size_t need = layout_workspace(s, nullptr, nullptr, y_f32);
     const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4, kb = (size_t)T * K * 4;
     const size_t stage = align_up(xb, 256) * 2 + align_up(lb, 256) + align_up(kb, 256) * 2 + 256;
     void* base = nullptr;
     rc = owned_workspace(st, need + stage, &base);
     if (rc) return rc;
     Workspace ws;
-    layout_workspace(s, (char*)base, &ws);
-    char* p = (char*)base + need;
+    layout_workspace(s, (char*)base, &ws, y_f32);
+    char* p = (char*)base + align_up(need, 256);  // the +256 of `stage` covers the padding
     __nv_bfloat16* x_d = (__nv_bfloat16*)p;
     p += align_up(xb, 256);
     __nv_bfloat16* out_d = (__nv_bfloat16*)p;
@@ -434,23 +476,37 @@ static int forward_host(const void* x_host, int T, int H, const void* W_router,
     float* w_d = (float*)p;
     p += align_up(kb, 256);
     float* aux_d = (float*)p;
+    SideStream side;
+    rc = side_stream(st, &side);
+    if (rc) return rc;
     cudaError_t e = cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_status(e);
     rc = run_forward(x_d, (const __nv_bfloat16*)W_router, W, s, norm, bias, cap, out_d,
                      logits_host ? logits_d : nullptr, idx_d, w_d, aux_host ? aux_d : nullptr, ws,
-                     st);
-    if (rc) return rc;
+                     st, side.routed);
+    if (rc) {
+        cudaStreamSynchronize(st);  // nothing of this call left in flight
+        return rc;
+    }
     remember_counts(st, ws, E);
-    e = cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, st);
+    // the routing outputs on the side stream, behind the routing
+    e = cudaStreamWaitEvent(side.side, side.routed, 0);
     if (e == cudaSuccess && logits_host)
-        e = cudaMemcpyAsync(logits_host, logits_d, lb, cudaMemcpyDeviceToHost, st);
+        e = cudaMemcpyAsync(logits_host, logits_d, lb, cudaMemcpyDeviceToHost, side.side);
     if (e == cudaSuccess && idx_host)
-        e = cudaMemcpyAsync(idx_host, idx_d, kb, cudaMemcpyDeviceToHost, st);
+        e = cudaMemcpyAsync(idx_host, idx_d, kb, cudaMemcpyDeviceToHost, side.side);
     if (e == cudaSuccess && w_host)
-        e = cudaMemcpyAsync(w_host, w_d, kb, cudaMemcpyDeviceToHost, st);
+        e = cudaMemcpyAsync(w_host, w_d, kb, cudaMemcpyDeviceToHost, side.side);
     if (e == cudaSuccess && aux_host)
-        e = cudaMemcpyAsync(aux_host, aux_d, sizeof(float), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        e = cudaMemcpyAsync(aux_host, aux_d, sizeof(float), cudaMemcpyDeviceToHost, side.side);
+    cudaError_t e2 = cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, st);
+    // both streams finish before the call returns (and before the next call
+    // on st can reuse the staging the side copies read)
+    cudaError_t e3 = cudaStreamSynchronize(side.side);
+    cudaError_t e4 = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = e2;
+    if (e == cudaSuccess) e = e3;
+    if (e == cudaSuccess) e = e4;
     return cuda_status(e);
 }
 
@@ -518,7 +574,9 @@ int moe_set_expert_path(int path) {
 size_t moe_workspace_bytes(int T, int H, int E, int K, int I) {
     if (check_sizes(T, H, E, K, I)) return 0;
     Sizes s{T, H, E, K, I};
-    return layout_workspace(s, nullptr, nullptr);
+    // enough for every forward of these sizes, including those under a
+    // capacity (fp32 expert outputs)
+    return layout_workspace(s, nullptr, nullptr, true);
 }
 
 int moe_forward_ws(const moe_bf16* x, int T, int H, const moe_bf16* W_router,
@@ -730,7 +788,7 @@ int moe_device_status(const void* workspace, int T, int H, int E, int K, int I, 
         if (check_sizes(T, H, E, K, I)) return MOE_ERR_INVALID_ARG;
         Sizes s{T, H, E, K, I};
         Workspace ws;
-        layout_workspace(s, (char*)workspace, &ws);
+        layout_workspace(s, (char*)workspace, &ws, false);  // the status word's offset
         status = ws.status;
     } else {
         std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -782,12 +840,13 @@ int moe_dbg_permute(const int32_t* topk_idx, int T, int E, int K, int capacity, 
         return cuda_status(e);
     }
     Sizes s{T, 64, E, K, 64};
-    // Private scratch for the chunk tables and tiles (small), stream-ordered.
+    // Private scratch for the chunk tables and tiles (small), stream-ordered,
+    // apart from the forwards' workspace.
     const size_t nch = (size_t)(s.nchunks() > 0 ? s.nchunks() : 1);
     const size_t tb = (size_t)s.max_tiles(kStreamRows) * sizeof(RowTile);
     const size_t bytes = align_up(nch * E * 4, 256) * 2 + align_up(tb, 256) + 256;
     void* base = nullptr;
-    rc = owned_workspace(st, bytes, &base);
+    rc = owned_workspace(st, bytes, &base, 1);
     if (rc) return rc;
     Workspace ws{};
     char* p = (char*)base;
@@ -817,7 +876,7 @@ int moe_dbg_combine(const moe_bf16* Y, const int32_t* inv, int T, int K, int H, 
     int rc = check_device();
     if (rc) return rc;
     if (T == 0) return MOE_OK;
-    return cuda_status(launch_combine((const __nv_bfloat16*)Y, inv, true, T, K, H,
+    return cuda_status(launch_combine((const __nv_bfloat16*)Y, nullptr, inv, true, T, K, H,
                                       (__nv_bfloat16*)out,
                                       (cudaStream_t)stream));
 }

@@ -112,6 +112,10 @@ struct Workspace {
     __nv_bfloat16* x_perm;  // [P, H] (tcgen05 path)
     __nv_bfloat16* hbuf;    // [P, I]
     __nv_bfloat16* ybuf;    // [P, H] token-major: the pair (t, k) at row t*K + k
+    float* ybuf_f32;        // the same region as fp32 [P, H] when the forward keeps the
+                            // weighted expert outputs in fp32 (under an expert
+                            // capacity), else null; the expert kernels then store Y
+                            // here and the combine reads it from here
     size_t bytes;
 };
 
@@ -141,7 +145,9 @@ cudaError_t launch_pack_experts(const __nv_bfloat16* Wg, const __nv_bfloat16* Wu
                                 cudaStream_t st);
 
 // Lays out (and, when base != nullptr, fills) the workspace; returns bytes.
-size_t layout_workspace(const Sizes& s, char* base, Workspace* ws);
+// y_f32: the Y region holds fp32 values (twice the bytes; Y is the last
+// region, so every other region sits at the same offset either way).
+size_t layout_workspace(const Sizes& s, char* base, Workspace* ws, bool y_f32);
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ------
 // CUDA-core router: expert- and H-split logits kernel (partial logits in
@@ -256,9 +262,10 @@ cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const 
 // out[t] = sum over k of Y row t*K + k (Y token-major, as the expert kernels
 // store it), skipping the pairs with inv[t*K + k] < 0 when inv != null
 // (dropped by a capacity); with y_by_inv, Y is in dispatch order and row
-// inv[t*K + k] is read instead.
-cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* inv, bool y_by_inv, int T,
-                           int K, int H, __nv_bfloat16* out, cudaStream_t st);
+// inv[t*K + k] is read instead.  Y32 != null: Y is fp32 there (Y unused).
+cudaError_t launch_combine(const __nv_bfloat16* Y, const float* Y32, const int32_t* inv,
+                           bool y_by_inv, int T, int K, int H, __nv_bfloat16* out,
+                           cudaStream_t st);
 
 int num_sms();  // of the current device (cached)
 
@@ -283,11 +290,12 @@ int cuda_status(cudaError_t e);
 int check_forward_args(const void* x, int T, int H, const void* Wr, const void* Wg,
                        const void* Wu, const void* Wd, int E, int K, int I, const void* out,
                        const void* logits, const void* idx, const void* w, const void* aux);
-// cap: expert capacity in pairs (0: none).
+// cap: expert capacity in pairs (0: none).  ev_routed (may be null) is
+// recorded on st once logits, idx, w and aux are final (after the dispatch).
 int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWeights& W,
                 const Sizes& s, int norm, const float* bias, int cap, __nv_bfloat16* out,
                 float* logits, int32_t* idx, float* w, float* aux, const Workspace& ws,
-                cudaStream_t st);
+                cudaStream_t st, cudaEvent_t ev_routed = nullptr);
 
 // Every launcher adds the number of kernels it launched.
 void count_launches(int n);

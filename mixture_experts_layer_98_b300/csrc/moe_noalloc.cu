@@ -65,7 +65,7 @@ extern "C" int moe_forward_noalloc(const moe_bf16* x, int T, int H, const moe_bf
                                 router_logits, topk_idx, topk_w, aux);
     if (rc) return rc;
     Sizes s{T, H, E, K, I};
-    const size_t need = T > 0 ? layout_workspace(s, nullptr, nullptr) : 0;
+    const size_t need = T > 0 ? layout_workspace(s, nullptr, nullptr, false) : 0;
     if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;  // before any work or set-up
     void* base = nullptr;
     rc = scratch_address(&base);
@@ -79,7 +79,7 @@ extern "C" int moe_forward_noalloc(const moe_bf16* x, int T, int H, const moe_bf
     // clears the status word, and every other region is written before it is
     // read within the same call.
     Workspace ws;
-    layout_workspace(s, (char*)base, &ws);
+    layout_workspace(s, (char*)base, &ws, false);
     const ExpertWeights W{(const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                           (const __nv_bfloat16*)W_down, nullptr};
     return run_forward((const __nv_bfloat16*)x, (const __nv_bfloat16*)W_router, W, s,

@@ -63,14 +63,53 @@ def gpu_forward(inputs, K, norm):
                 w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=counts)
 
 
-def near_tie_keys(keys, K, rel):
-    """Tokens whose ranking keys (logit + selection bias) at the K/K+1 boundary,
-    or between adjacent kept experts, differ by less than rel·(1 + |key|): the
-    logits' own tolerance can reorder them, so more than one selection is
-    correct."""
-    k = -np.sort(-np.asarray(keys, np.float64), axis=1)[:, :min(K + 1, keys.shape[1])]
+def tile_rows(idx, E, capacity=0, n_random=48, seed=0, tiles=(64, 128, 256)):
+    """Token rows whose outputs exercise every expert's tile boundaries: for
+    each expert, in dispatch order (token order within the expert, kept pairs
+    only under a capacity), the token of its first and last row and of the
+    first row of its last tile for each tile height the expert kernels use
+    (64-row tails, 128-row tiles, 256-row CTA-pair tiles); for experts of
+    >= 1024 rows also the first row of every 8th 128-row tile (the hot
+    experts' long tile runs); plus a seeded random sample of n_random tokens."""
+    idx = np.asarray(idx)
+    T = idx.shape[0]
+    keep = oracle.keep_mask(idx, E, capacity) if capacity else np.ones(idx.shape, bool)
+    rows = set(mi.sample_rows(T, n_random, seed).tolist()) if T else set()
+    tok = np.repeat(np.arange(T), idx.shape[1])
+    ex = idx.ravel()
+    kp = keep.ravel()
+    order = np.lexsort((tok, ex))
+    order = order[kp[order]]
+    ex_sorted = ex[order]
+    tok_sorted = tok[order]
+    starts = np.searchsorted(ex_sorted, np.arange(E + 1))
+    for e in range(E):
+        toks = tok_sorted[starts[e]:starts[e + 1]]
+        n = toks.size
+        if n == 0:
+            continue
+        picks = {0, n - 1}
+        for h in tiles:
+            picks.add((n - 1) // h * h)
+        if n >= 1024:
+            picks.update(range(0, n, 8 * 128))
+        rows.update(int(toks[i]) for i in picks)
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+def near_tie_keys(logits, bias, K, rel):
+    """Tokens where the ranking keys l + b (fp32) of two neighbours at the
+    K/K+1 boundary, or of two adjacent kept experts, differ by less than the
+    two logits' own error bounds rel·(1 + |l|) added: the logits' error can
+    reorder such keys, so more than one selection is correct."""
+    logits = np.asarray(logits, np.float64)
+    keys = (logits + np.asarray(bias, np.float32)[None, :]).astype(np.float32).astype(np.float64)
+    m = min(K + 1, keys.shape[1])
+    order = np.argsort(-keys, axis=1, kind="stable")[:, :m]
+    k = np.take_along_axis(keys, order, axis=1)
+    err = rel * (1 + np.abs(np.take_along_axis(logits, order, axis=1)))
     d = k[:, :-1] - k[:, 1:]
-    return np.where((d < rel * (1 + np.abs(k[:, 1:]))).any(axis=1))[0]
+    return np.where((d < err[:, :-1] + err[:, 1:]).any(axis=1))[0]
 
 
 def compare(b, g, K, norm, rows=None, bias=None, capacity=0):
@@ -92,13 +131,21 @@ def compare(b, g, K, norm, rows=None, bias=None, capacity=0):
     if bias is None:
         ties = set(oracle.near_tie_tokens(probs, K, TIE_GAP).tolist())
     else:
-        keys = (o["logits"] + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
-        ties = set(near_tie_keys(keys, K, 2 * LOGIT_RTOL).tolist())
+        # with a selection bias the experts are ranked by the keys l + b: two
+        # keys can trade places only if they differ by less than the two
+        # logits' errors added, each at most the largest logit error measured
+        # in this very comparison (not the looser test bound)
+        ties = set(near_tie_keys(o["logits"], bias, K, max(rep["logit_err"], 1e-7)).tolist())
     mism = np.where((g["idx"] != o["idx"]).any(axis=1))[0]
     bad = [t for t in mism.tolist() if t not in ties]
     rep["near_ties"] = len(ties)
     rep["idx_mismatch"] = len(mism)
+    print(f"[parity] T={T} near-tie tokens {len(ties)}, selection differs on {len(mism)}")
     assert not bad, f"top-k differs on non-tie tokens {bad[:10]}"
+    # near ties are rare events of the logit distribution (a gap below 1e-6
+    # between neighbouring probabilities): a large count would mean the
+    # exclusion hides real selection errors
+    assert len(ties) <= max(4, T // 100), rep
     keep = np.array([t for t in range(T) if t not in ties], dtype=np.int64)
     if keep.size:
         rep["w_err"] = float(np.abs(g["w"][keep] - o["w"][keep]).max())

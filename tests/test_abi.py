@@ -70,12 +70,23 @@ def test_workspace_bytes(L):
 def test_noalloc_scratch_limit(L):
     # moe_forward_noalloc's 32 MiB scratch holds the workspace of every batch up
     # to T = 212 on the H=4096, E=128, K=8, I=1536 layer (the limit its header
-    # states) and not T = 213.  The split-K plans of the decode kernels size
+    # states) and not T = 213.  It takes no capacity, so it needs
+    # moe_workspace_bytes less the T·K·H·2 bytes of fp32 expert outputs only a
+    # capacity forward keeps.  The split-K plans of the decode kernels size
     # part of the workspace, so a plan change that grows it shows up here.
-    ws = L.moe_workspace_bytes
+    def need(T):
+        return L.moe_workspace_bytes(T, 4096, 128, 8, 1536) - T * 8 * 4096 * 2
     scratch = 32 << 20
-    assert max(ws(T, 4096, 128, 8, 1536) for T in range(1, 213)) <= scratch
-    assert ws(213, 4096, 128, 8, 1536) > scratch
+    assert max(need(T) for T in range(1, 213)) <= scratch
+    assert need(213) > scratch
+
+
+def test_capacity_workspace_keeps_fp32_expert_outputs(L):
+    # the fp32 expert outputs of a capacity forward take twice the bf16 bytes
+    # at the end of the workspace: moe_workspace_bytes covers them
+    for T, H, E, K, I in [(1, 128, 8, 2, 256), (300, 256, 16, 4, 128), (4096, 2048, 128, 8, 768)]:
+        ws = L.moe_workspace_bytes(T, H, E, K, I)
+        assert ws >= T * K * (2 * H * 2 + I * 2) + T * K * H * 2
 
 
 @pytest.mark.parametrize("T,H,E,K,I", [(-1, 128, 8, 2, 256), (4, 96, 8, 2, 256),

@@ -114,3 +114,22 @@ def test_bad_options_are_refused(moe):
     bias = torch.zeros(cfg.E + 1, device="cuda")[1:]  # 4-byte but not 16-byte aligned
     with pytest.raises(moe.MoEError):
         moe.moe_forward_opts(*args, expert_bias=bias)
+
+
+def test_stage_calls_leave_the_forward_queries_intact(moe):
+    # moe_last_expert_counts / moe_device_status read what the last forward on
+    # the stream left in its workspace; a stage entry point called afterwards
+    # on the same stream (with more tokens, so its scratch is larger) uses
+    # scratch of its own and must not overwrite it
+    cfg = mi.CONFIGS["decode_t16"]
+    inp = mi.make_inputs(cfg, "cuda")
+    g = gpu_forward(inp, cfg.K, cfg.norm)
+    rng = np.random.default_rng(3)
+    T = 5000
+    idx = np.array([rng.permutation(cfg.E)[:cfg.K] for _ in range(T)], np.int32)
+    moe.moe_dbg_permute(torch.from_numpy(idx).cuda(), cfg.E)
+    torch.cuda.synchronize()
+    counts = moe.moe_last_expert_counts(cfg.E).numpy()
+    assert np.array_equal(counts, g["counts"])
+    assert np.array_equal(counts, np.bincount(g["idx"].ravel(), minlength=cfg.E))
+    assert moe.moe_device_status() == 0
