@@ -367,11 +367,33 @@ double oracle_aux(const double* probs, const int32_t* counts, int T, int E, int 
  * order, when rows == NULL), into out[n_rows, H] (bf16) and, when out_f64 is
  * not NULL, out_f64[n_rows, H] (the same values before the bf16 rounding).
  * Any of logits / idx / w / aux / counts may be NULL.  Returns 0 on success. */
-int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
-                         int capacity, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
-                         int E, int K, int I, int norm, int flags, const int32_t* rows, int n_rows,
-                         uint16_t* out, double* out_f64, float* logits_out, int32_t* idx_out,
-                         float* w_out, float* aux_out, int32_t* counts_out) {
+/* The expert weights of a forward and the step that turns a token's kept
+ * pairs into its output row: bf16 matrices (oracle_token_output_ex) or 4-bit
+ * groups (token_output_q4 below). */
+typedef struct {
+    const uint16_t *Wg, *Wu, *Wd;                      /* bf16 [E,I,H], [E,I,H], [E,H,I] */
+    const uint8_t *qg, *qu, *qd;                       /* or 4-bit codes of the same shape */
+    const uint16_t *sg, *bg, *su, *bu, *sd, *bd;       /* and their group scales / biases */
+} experts_t;
+
+static int token_output_q4(const uint16_t* x_row, int H, const int32_t* idx_row,
+                           const float* w_row, int K, const experts_t* W, int E, int I,
+                           int flags, uint16_t* out_row, double* out_f64_row);
+
+static int experts_token_output(const experts_t* W, const uint16_t* x_row, int H,
+                                const int32_t* ik, const float* wk, int nk, int E, int I,
+                                int flags, uint16_t* out_row, double* out_f64_row) {
+    if (W->qg)
+        return token_output_q4(x_row, H, ik, wk, nk, W, E, I, flags, out_row, out_f64_row);
+    return oracle_token_output_ex(x_row, H, ik, wk, nk, W->Wg, W->Wu, W->Wd, E, I, flags,
+                                  out_row, out_f64_row);
+}
+
+static int moe_forward_any(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
+                           int capacity, const experts_t* W, int E, int K, int I, int norm,
+                           int flags, const int32_t* rows, int n_rows, uint16_t* out,
+                           double* out_f64, float* logits_out, int32_t* idx_out, float* w_out,
+                           float* aux_out, int32_t* counts_out) {
     if (T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || I < 1) return 1;
     if (T == 0) {
         if (aux_out) *aux_out = 0.0f;
@@ -411,9 +433,9 @@ int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, co
                     wk[nk] = w[(size_t)t * K + k];
                     ++nk;
                 }
-            if (oracle_token_output_ex(x + (size_t)t * H, H, ik, wk, nk, Wg, Wu, Wd, E, I, flags,
-                                       out ? out + (size_t)j * H : NULL,
-                                       out_f64 ? out_f64 + (size_t)j * H : NULL))
+            if (experts_token_output(W, x + (size_t)t * H, H, ik, wk, nk, E, I, flags,
+                                     out ? out + (size_t)j * H : NULL,
+                                     out_f64 ? out_f64 + (size_t)j * H : NULL))
                 fail |= 1;
         }
         if (fail) rc = 3;
@@ -431,6 +453,20 @@ int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, co
     free(counts);
     free(keep);
     return rc;
+}
+
+int oracle_moe_forward_b(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
+                         int capacity, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                         int E, int K, int I, int norm, int flags, const int32_t* rows, int n_rows,
+                         uint16_t* out, double* out_f64, float* logits_out, int32_t* idx_out,
+                         float* w_out, float* aux_out, int32_t* counts_out) {
+    experts_t W;
+    memset(&W, 0, sizeof W);
+    W.Wg = Wg;
+    W.Wu = Wu;
+    W.Wd = Wd;
+    return moe_forward_any(x, T, H, Wr, bias, capacity, &W, E, K, I, norm, flags, rows, n_rows,
+                           out, out_f64, logits_out, idx_out, w_out, aux_out, counts_out);
 }
 
 /* The block forward without a selection bias or a capacity. */
@@ -457,9 +493,13 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
  *     already);
  *   - the code of w is q = clamp(rint(fp32(w - b) / s), 0, 15), every step in
  *     fp32 arithmetic (q = 0 when s = 0);
- *   - the dequantised weight is w' = bf16(q·s + b), rounded once from the
- *     exact value.
- * A forward with quantised experts is the forward with the weights W'.
+ *   - the weight the forward computes with is the exact value q·s + b (no
+ *     rounding of the weight itself: the page stores a scale and a bias per
+ *     group and says nothing of a rounded intermediate weight);
+ *   - oracle_dequantize_q4 also gives the nearest bf16 of that value, the
+ *     form a bf16 kernel consumes.
+ * A forward with quantised experts is the block forward with the expert
+ * weights q·s + b in double (oracle_moe_forward_q4).
  */
 
 static float q4_f32(uint16_t b) {
@@ -521,4 +561,130 @@ int oracle_dequantize_q4(const uint8_t* q, const uint16_t* s, const uint16_t* b,
             W[r * cols + c] = oracle_f64_to_bf16(v);
         }
     return 0;
+}
+
+/* q, s, b as above -> W [rows, cols] in double: w = q·s + b, exact (q·s is a
+ * 4-bit integer times a bf16, exact in double; the sum is exact unless the two
+ * terms lie more than 2^44 apart). */
+int oracle_dequantize_q4_f64(const uint8_t* q, const uint16_t* s, const uint16_t* b, int rows,
+                             int cols, double* W) {
+    if (rows < 0 || cols <= 0 || cols % 128) return 1;
+    const int groups = cols / 128;
+    for (long long r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const long long g = r * groups + c / 128;
+            const uint8_t code = q[r * cols + c];
+            if (code > 15) return 2;
+            W[r * cols + c] = (double)code * oracle_bf16_to_f64(s[g]) + oracle_bf16_to_f64(b[g]);
+        }
+    return 0;
+}
+
+/* Row `row` of a 4-bit matrix with `cols` columns, as exact weights. */
+static void q4_row(const uint8_t* q, const uint16_t* s, const uint16_t* b, size_t row, int cols,
+                   double* out) {
+    const int groups = cols / 128;
+    for (int c = 0; c < cols; ++c) {
+        const size_t g = row * (size_t)groups + (size_t)(c / 128);
+        out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +
+                 oracle_bf16_to_f64(b[g]);
+    }
+}
+
+/* oracle_expert_mlp of expert e on 4-bit weights (exact values q·s + b). */
+static int expert_mlp_q4(const uint16_t* x_row, int H, const experts_t* W, int e, int I,
+                         int flags, double* y) {
+    double* a = (double*)malloc((size_t)I * sizeof(double));
+    double* xr = (double*)malloc((size_t)H * sizeof(double));
+    double* wg = (double*)malloc((size_t)H * sizeof(double));
+    double* wu = (double*)malloc((size_t)H * sizeof(double));
+    double* wd = (double*)malloc((size_t)I * sizeof(double));
+    int rc = (a && xr && wg && wu && wd) ? 0 : 2;
+    if (!rc) {
+        for (int h = 0; h < H; ++h) xr[h] = oracle_bf16_to_f64(x_row[h]);
+        for (int i = 0; i < I; ++i) {
+            const size_t row = (size_t)e * I + i;
+            q4_row(W->qg, W->sg, W->bg, row, H, wg);
+            q4_row(W->qu, W->su, W->bu, row, H, wu);
+            double g = 0.0, u = 0.0;
+            for (int h = 0; h < H; ++h) {
+                g += xr[h] * wg[h];
+                u += xr[h] * wu[h];
+            }
+            double ai = silu(g) * u;
+            if (!(flags & ORACLE_FP64_INTERMEDIATE)) ai = oracle_bf16_to_f64(oracle_f64_to_bf16(ai));
+            a[i] = ai;
+        }
+        for (int h = 0; h < H; ++h) {
+            q4_row(W->qd, W->sd, W->bd, (size_t)e * H + h, I, wd);
+            double acc = 0.0;
+            for (int i = 0; i < I; ++i) acc += a[i] * wd[i];
+            y[h] = acc;
+        }
+    }
+    free(a);
+    free(xr);
+    free(wg);
+    free(wu);
+    free(wd);
+    return rc;
+}
+
+/* oracle_token_output_ex on 4-bit weights. */
+static int token_output_q4(const uint16_t* x_row, int H, const int32_t* idx_row,
+                           const float* w_row, int K, const experts_t* W, int E, int I,
+                           int flags, uint16_t* out_row, double* out_f64_row) {
+    double* acc = (double*)calloc((size_t)H, sizeof(double));
+    double* y = (double*)malloc((size_t)H * sizeof(double));
+    if (!acc || !y) { free(acc); free(y); return 2; }
+    int rc = 0;
+    for (int k = 0; k < K && rc == 0; ++k) {
+        const int e = idx_row[k];
+        if (e < 0 || e >= E) { rc = 3; break; }
+        rc = expert_mlp_q4(x_row, H, W, e, I, flags, y);
+        for (int h = 0; h < H; ++h) acc[h] += (double)w_row[k] * y[h];
+    }
+    for (int h = 0; h < H; ++h) {
+        if (out_row) out_row[h] = oracle_f64_to_bf16(acc[h]);
+        if (out_f64_row) out_f64_row[h] = acc[h];
+    }
+    free(acc);
+    free(y);
+    return rc;
+}
+
+/* The block forward on 4-bit experts: codes q* [E,I,H] / [E,I,H] / [E,H,I]
+ * (one byte per code), scales s* and biases b* [E, rows, cols / 128] bf16, as
+ * oracle_quantize_q4 writes them; every other argument as for
+ * oracle_moe_forward_b. */
+int oracle_moe_forward_q4(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
+                          int capacity, const uint8_t* qg, const uint16_t* sg, const uint16_t* bg,
+                          const uint8_t* qu, const uint16_t* su, const uint16_t* bu,
+                          const uint8_t* qd, const uint16_t* sd, const uint16_t* bd, int E, int K,
+                          int I, int norm, int flags, const int32_t* rows, int n_rows,
+                          uint16_t* out, double* out_f64, float* logits_out, int32_t* idx_out,
+                          float* w_out, float* aux_out, int32_t* counts_out) {
+    if (H % 128 || I % 128) return 1;
+    experts_t W;
+    memset(&W, 0, sizeof W);
+    W.qg = qg; W.sg = sg; W.bg = bg;
+    W.qu = qu; W.su = su; W.bu = bu;
+    W.qd = qd; W.sd = sd; W.bd = bd;
+    return moe_forward_any(x, T, H, Wr, bias, capacity, &W, E, K, I, norm, flags, rows, n_rows,
+                           out, out_f64, logits_out, idx_out, w_out, aux_out, counts_out);
+}
+
+/* One token's output on 4-bit experts (oracle_token_output_ex's contract). */
+int oracle_token_output_q4(const uint16_t* x_row, int H, const int32_t* idx_row,
+                           const float* w_row, int K, const uint8_t* qg, const uint16_t* sg,
+                           const uint16_t* bg, const uint8_t* qu, const uint16_t* su,
+                           const uint16_t* bu, const uint8_t* qd, const uint16_t* sd,
+                           const uint16_t* bd, int E, int I, int flags, uint16_t* out_row,
+                           double* out_f64_row) {
+    experts_t W;
+    memset(&W, 0, sizeof W);
+    W.qg = qg; W.sg = sg; W.bg = bg;
+    W.qu = qu; W.su = su; W.bu = bu;
+    W.qd = qd; W.sd = sd; W.bd = bd;
+    return token_output_q4(x_row, H, idx_row, w_row, K, &W, E, I, flags, out_row, out_f64_row);
 }

@@ -39,6 +39,11 @@ class _Lib:
         lib.oracle_keep_mask.argtypes = [P, i, i, i, i, P]
         lib.oracle_quantize_q4.argtypes = [P, i, i, P, P, P]
         lib.oracle_dequantize_q4.argtypes = [P, P, P, i, i, P]
+        lib.oracle_dequantize_q4_f64.argtypes = [P, P, P, i, i, P]
+        lib.oracle_moe_forward_q4.argtypes = [P, i, i, P, P, i, P, P, P, P, P, P, P, P, P, i, i,
+                                              i, i, i, P, i, P, P, P, P, P, P, P]
+        lib.oracle_token_output_q4.argtypes = [P, i, P, P, i, P, P, P, P, P, P, P, P, P, i, i, i,
+                                               P, P]
         lib.oracle_expert_mlp.argtypes = [P, i, P, P, P, i, i, P]
         lib.oracle_token_output.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P]
         lib.oracle_token_output_ex.argtypes = [P, i, P, P, i, P, P, P, i, i, i, P, P]
@@ -300,7 +305,7 @@ def quantize_q4(W):
 
 
 def dequantize_q4(q, s, b):
-    """W' = bf16(q·s + b) per element (bf16 bits, the shape of q)."""
+    """The nearest bf16 of q·s + b per element (bf16 bits, the shape of q)."""
     q = _c(q, np.uint8)
     s = _c(s, np.uint16)
     b = _c(b, np.uint16)
@@ -309,3 +314,74 @@ def dequantize_q4(q, s, b):
     _check(_L().oracle_dequantize_q4(_p(q), _p(s), _p(b), q.size // cols, cols, _p(W)),
            "dequantize_q4")
     return W
+
+
+def dequantize_q4_f64(q, s, b):
+    """The exact weights q·s + b (float64, the shape of q): the values the
+    4-bit forward computes with."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint16)
+    b = _c(b, np.uint16)
+    cols = q.shape[-1]
+    W = np.empty(q.shape, dtype=np.float64)
+    _check(_L().oracle_dequantize_q4_f64(_p(q), _p(s), _p(b), q.size // cols, cols, _p(W)),
+           "dequantize_q4_f64")
+    return W
+
+
+def quantize_experts_q4(Wg, Wu, Wd):
+    """quantize_q4 of the three expert matrices: {"gate": (q, s, b), "up": ..., "down": ...}."""
+    return {"gate": quantize_q4(Wg), "up": quantize_q4(Wu), "down": quantize_q4(Wd)}
+
+
+def _q4_args(q4):
+    out = []
+    for name in ("gate", "up", "down"):
+        q, s, b = q4[name]
+        out += [_c(q, np.uint8), _c(s, np.uint16), _c(b, np.uint16)]
+    return out
+
+
+def moe_forward_q4(x, Wr, q4, K, norm, rows=None, flags=0, bias=None, capacity=0):
+    """moe_forward on 4-bit experts (q4 from quantize_experts_q4): the expert
+    weights are the exact values q·s + b.  Same results dict as moe_forward."""
+    x = _c(x, np.uint16)
+    Wr = _c(Wr, np.uint16)
+    a9 = _q4_args(q4)
+    T, H = x.shape
+    E, I, _ = a9[0].shape
+    assert Wr.shape == (E, H) and a9[3].shape == (E, I, H) and a9[6].shape == (E, H, I)
+    if rows is not None:
+        rows = _c(rows, np.int32)
+        n = rows.shape[0]
+    else:
+        n = T
+    out = np.empty((n, H), np.uint16)
+    out_f64 = np.empty((n, H), np.float64)
+    logits = np.empty((T, E), np.float32)
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float32)
+    counts = np.empty(E, np.int32)
+    a = np.zeros(1, np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    _check(_L().oracle_moe_forward_q4(_p(x), T, H, _p(Wr), _p(b), int(capacity),
+                                      *[_p(v) for v in a9], E, K, I, int(bool(norm)), flags,
+                                      _p(rows), n, _p(out), _p(out_f64), _p(logits), _p(idx),
+                                      _p(w), _p(a), _p(counts)), "forward_q4")
+    return dict(out=out, out_f64=out_f64, logits=logits, idx=idx, w=w, aux=float(a[0]),
+                counts=counts)
+
+
+def token_output_q4(x_row, idx_row, w_row, q4, flags=0, unrounded=False):
+    """token_output on 4-bit experts (exact weights q·s + b)."""
+    x_row = _c(x_row, np.uint16)
+    idx_row = _c(idx_row, np.int32)
+    w_row = _c(w_row, np.float32)
+    a9 = _q4_args(q4)
+    E, I, H = a9[0].shape
+    out = np.empty(H, np.uint16)
+    f64 = np.empty(H, np.float64) if unrounded else None
+    _check(_L().oracle_token_output_q4(_p(x_row), H, _p(idx_row), _p(w_row), idx_row.shape[0],
+                                       *[_p(v) for v in a9], E, I, flags, _p(out), _p(f64)),
+           "token_output_q4")
+    return (out, f64) if unrounded else out

@@ -485,7 +485,7 @@ def test_router_exact_ties_zero_weights(moe, T, norm):
     assert (g["idx"] == np.arange(cfg.K)).all()
     assert np.abs(g["w"] - (1.0 / cfg.K if norm else 1.0 / cfg.E)).max() < 1e-6
     assert abs(g["aux"] - 1.0) < 1e-5
-    compare(host_bits(inp), g, cfg.K, norm)
+    compare(host_bits(inp), g, cfg.K, norm, max_near_ties=T)  # every token ties
 
 
 @pytest.mark.parametrize("T", [100, 700])
@@ -501,4 +501,4 @@ def test_router_exact_ties_duplicate_rows(moe, T):
         for k, e in enumerate(row):
             if e % 2 == 1:
                 assert k > 0 and row[k - 1] == e - 1, (t, row)
-    compare(host_bits(inp), g, cfg.K, cfg.norm)
+    compare(host_bits(inp), g, cfg.K, cfg.norm, max_near_ties=T)  # exact ties by construction

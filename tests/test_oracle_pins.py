@@ -475,6 +475,74 @@ def pin_q4_error_bound():
             assert qq[np.argmin(grp)] == 0 and qq[np.argmax(grp)] == 15
 
 
+def pin_q4_exact_weights():
+    # The 4-bit forward computes with q·s + b exactly: on a grid the exact
+    # weights are the original ones; for random weights they lie within s/2 of
+    # them (no bf16 term), and the bf16 dequantisation is their nearest bf16.
+    rng = np.random.default_rng(42)
+    rows, cols = 4, 256
+    k = rng.integers(0, 16, size=(rows, cols))
+    vals = np.empty((rows, cols))
+    for r in range(rows):
+        for g in range(cols // 128):
+            kk = k[r, g * 128:(g + 1) * 128]
+            kk[0], kk[1] = 0, 15
+            vals[r, g * 128:(g + 1) * 128] = -0.5 * (1 + r + g) + kk * 2.0 ** -(2 + (r + 2 * g) % 4)
+    W = _bf16_of(vals)
+    q, s, b = oracle.quantize_q4(W)
+    assert np.array_equal(oracle.dequantize_q4_f64(q, s, b), bf16_bits_to_f64(W))
+    W = _bf16_of((rng.standard_normal((8, 384)) * 0.02).astype(np.float32).view(np.uint32)
+                 .__and__(np.uint32(0xFFFF0000)).view(np.float32))
+    q, s, b = oracle.quantize_q4(W)
+    we = oracle.dequantize_q4_f64(q, s, b)
+    sv = np.repeat(bf16_bits_to_f64(s), 128, axis=1)
+    bv = np.repeat(bf16_bits_to_f64(b), 128, axis=1)
+    assert np.array_equal(we, q.astype(np.float64) * sv + bv)
+    assert (np.abs(we - bf16_bits_to_f64(W)) <= sv / 2 + 1e-12).all()
+    assert np.array_equal(bf16_bits_to_f64(oracle.dequantize_q4(q, s, b)), f64_rne_bf16_value(we))
+
+
+def pin_q4_forward_single_expert_is_swiglu():
+    # E = K = 1 on 4-bit weights: one SwiGLU MLP (numpy float64) with the weights
+    # q·s + b, every 128-column group with its own scale and bias.
+    _, b = rand_case(9, 256, 1, 1, 256, seed=43, norm=True)
+    q4 = oracle.quantize_experts_q4(b["W_gate"], b["W_up"], b["W_down"])
+    r = oracle.moe_forward_q4(b["x"], b["W_router"], q4, 1, True)
+    Wg, Wu, Wd = (q4[n][0].astype(np.float64) * np.repeat(bf16_bits_to_f64(q4[n][1]), 128, -1)
+                  + np.repeat(bf16_bits_to_f64(q4[n][2]), 128, -1) for n in ("gate", "up", "down"))
+    y = np_swiglu(bf16_bits_to_f64(b["x"]), Wg[0], Wu[0], Wd[0])
+    assert np.abs(r["out_f64"] - y).max() <= 1e-9 * np.abs(y).max()
+    # and not the bf16 forward on the original weights (the quantisation shows)
+    r0 = oracle.moe_forward(b["x"], b["W_router"], b["W_gate"], b["W_up"], b["W_down"], 1, True)
+    assert np.abs(r0["out_f64"] - y).max() > 1e-3 * np.abs(y).max()
+
+
+def pin_q4_forward_on_grid_is_the_bf16_forward():
+    # Weights already on each group's 4-bit grid (so q·s + b is the bf16 weight
+    # itself): the 4-bit forward is the bf16 forward, to the last bit, routing,
+    # selection, combine and all.
+    rng = np.random.default_rng(44)
+    T, H, E, K, I = 6, 256, 4, 2, 128
+    _, b = rand_case(T, H, E, K, I, seed=45, norm=True)
+
+    def on_grid(shape):
+        # each group: lo + k·st with its minimum at k = 0 and its maximum at
+        # k = 15 (so the quantiser finds lo and st again); all values bf16
+        k = rng.integers(0, 16, size=shape)
+        k[..., 0::128] = 0
+        k[..., 1::128] = 15
+        lo = -2.0 ** -5 * (1 + rng.integers(0, 4, size=shape[:-1] + (shape[-1] // 128,)))
+        st = 2.0 ** -rng.integers(7, 10, size=lo.shape).astype(np.float64)
+        return _bf16_of(np.repeat(lo, 128, -1) + k * np.repeat(st, 128, -1))
+
+    Wg, Wu, Wd = on_grid((E, I, H)), on_grid((E, I, H)), on_grid((E, H, I))
+    q4 = oracle.quantize_experts_q4(Wg, Wu, Wd)
+    r4 = oracle.moe_forward_q4(b["x"], b["W_router"], q4, K, True)
+    r = oracle.moe_forward(b["x"], b["W_router"], Wg, Wu, Wd, K, True)
+    assert np.array_equal(r4["out_f64"], r["out_f64"]) and np.array_equal(r4["out"], r["out"])
+    assert np.array_equal(r4["idx"], r["idx"]) and r4["aux"] == r["aux"]
+
+
 PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equal_logits,
         pin_weights_closed_form, pin_router_logits, pin_dispatch_bruteforce,
         pin_single_expert_is_swiglu, pin_dense_equivalence, pin_soft_router,
@@ -482,7 +550,8 @@ PINS = [pin_bf16_rounding, pin_worked_example, pin_topk_bruteforce, pin_all_equa
         pin_bias_zero_is_unbiased, pin_biased_topk_bruteforce,
         pin_biased_weights_are_unbiased_probs, pin_bias_forces_selection_and_aux,
         pin_capacity_bruteforce, pin_capacity_dispatch, pin_q4_exact_grid,
-        pin_q4_round_half_even_and_constant_group, pin_q4_error_bound]
+        pin_q4_round_half_even_and_constant_group, pin_q4_error_bound, pin_q4_exact_weights,
+        pin_q4_forward_single_expert_is_swiglu, pin_q4_forward_on_grid_is_the_bf16_forward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -536,6 +605,14 @@ MUTATIONS = {
     "q4_codes_truncate": ("rintf((q4_f32(w[j]) - bf) / sf)", "truncf((q4_f32(w[j]) - bf) / sf)"),
     "q4_wrong_group": ("const long long gi = r * groups + c / 128;",
                        "const long long gi = r * groups + c % groups;"),
+    "q4_forward_bias_dropped": ("out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g]);",
+                                "out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]);"),
+    "q4_forward_wrong_group": ("const size_t g = row * (size_t)groups + (size_t)(c / 128);",
+                               "const size_t g = row * (size_t)groups + (size_t)(c % groups);"),
+    "q4_forward_gate_up_swapped": ("q4_row(W->qg, W->sg, W->bg, row, H, wg);",
+                                   "q4_row(W->qu, W->su, W->bu, row, H, wg);"),
+    "q4_forward_rounds_weights": ("out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g]);",
+                                  "out[c] = oracle_bf16_to_f64(oracle_f64_to_bf16((double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g])));"),
     "weights_from_biased_keys": (
         "logits[i];\n    oracle_softmax(logits, T, E, probs);",
         "logits[i];\n    oracle_softmax(keys, T, E, probs);"),
