@@ -186,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // the weights are read once per forward: their lines go first when
+            // L2 needs room, so they do not push out the activations, h, the
+            // slice accumulators and Y that the forward reads back
+            const uint64_t pol_once = ptx::l2_policy_evict_first();
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
                 const Unit x = unit_of(p, u, n_gu);
                 const RowTile tl = p.tiles[x.tile];
@@ -252,10 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sB = sA + 2 * kABytes;
                     ptx::mbar_arrive_expect_tx(&full_bar[stage], bytes);
                     if (pk0) {  // packed: each weight tile is one contiguous 16 KB block
-                        ptx::bulk_load(sA, pk0 + ((e0 + a0b) * nkb + kb) * kPackBlockBytes,
-                                       kABytes, &full_bar[stage]);
-                        ptx::bulk_load(sA + kABytes, pk1 + ((e0 + a1b) * nkb + kb) * kPackBlockBytes,
-                                       kABytes, &full_bar[stage]);
+                        ptx::bulk_load_hint(sA, pk0 + ((e0 + a0b) * nkb + kb) * kPackBlockBytes,
+                                            kABytes, &full_bar[stage], pol_once);
+                        ptx::bulk_load_hint(sA + kABytes,
+                                            pk1 + ((e0 + a1b) * nkb + kb) * kPackBlockBytes,
+                                            kABytes, &full_bar[stage], pol_once);
                     } else {
                         ptx::tma_load_2d(sA, mw0, &full_bar[stage], kb * kBK, a0);
                         ptx::tma_load_2d(sA + kABytes, mw1, &full_bar[stage], kb * kBK, a1);

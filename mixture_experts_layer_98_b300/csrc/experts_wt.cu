@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            const uint64_t pol_once = ptx::l2_policy_evict_first();
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
                 const int pitem = item / p.ksplit, ks = item % p.ksplit;
                 const RowTile tl = p.tiles[pitem / p.n_blk];
@@ -196,12 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sB = sA + 2 * kABytes;
                     ptx::mbar_arrive_expect_tx(&full_bar[stage], bytes);
                     if (p.apk0) {  // packed: each weight tile is one contiguous 16 KB block
+                        // (read once per forward: evicted first, ahead of the
+                        // activations and h the forward reads back)
                         const size_t e0 = (size_t)tl.expert * p.a_blocks_per_expert;
-                        ptx::bulk_load(sA, p.apk0 + ((e0 + a0b) * p.num_kb + kb) * kPackBlockBytes,
-                                       kABytes, &full_bar[stage]);
-                        ptx::bulk_load(sA + kABytes,
-                                       p.apk1 + ((e0 + a1b) * p.num_kb + kb) * kPackBlockBytes,
-                                       kABytes, &full_bar[stage]);
+                        ptx::bulk_load_hint(
+                            sA, p.apk0 + ((e0 + a0b) * p.num_kb + kb) * kPackBlockBytes, kABytes,
+                            &full_bar[stage], pol_once);
+                        ptx::bulk_load_hint(
+                            sA + kABytes, p.apk1 + ((e0 + a1b) * p.num_kb + kb) * kPackBlockBytes,
+                            kABytes, &full_bar[stage], pol_once);
                     } else {
                         ptx::tma_load_2d(sA, &tmA0, &full_bar[stage], kb * kBK, a0);
                         ptx::tma_load_2d(sA + kABytes, &tmA1, &full_bar[stage], kb * kBK, a1);
