@@ -53,17 +53,26 @@ METRIC = "MoE-layer tokens/s on 1 B300 and % of roofline (tensor peak or HBM GB/
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-# the sources each stage's kernels are built from (a recorded DRAM-traffic figure
-# is only reported while these are unchanged)
+# The sources a stage's kernel is built from, per expert path: a recorded DRAM
+# traffic figure is reported only while these files are unchanged.
+_COMMON = ["moe_common.cuh", "sm100_ptx.cuh"]
 STAGE_SOURCES = {
-    "router": ["router.cu", "moe_common.cuh"],
-    "dispatch": ["dispatch.cu", "moe_common.cuh"],
-    "gate_up": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_decode.cu",
-                "experts_stream.cu", "sm100_ptx.cuh", "moe_common.cuh"],
-    "down": ["experts_tc.cu", "experts_pair.cu", "experts_wt.cu", "experts_stream.cu",
-             "sm100_ptx.cuh", "moe_common.cuh"],
-    "combine": ["combine.cu", "moe_common.cuh"],
+    "router": ["router_tc.cu", "router.cu", "routing.cuh"] + _COMMON,
+    "dispatch": ["dispatch.cu"] + _COMMON,
+    "combine": ["combine.cu"] + _COMMON,
 }
+PATH_SOURCES = {
+    "tcgen05": ["experts_tc.cu"], "tcgen05_pair": ["experts_pair.cu"],
+    "tcgen05_wt": ["experts_wt.cu"], "tcgen05_decode": ["experts_decode.cu"],
+    "streaming": ["experts_stream.cu"], "warp_mma_q4": ["experts_q4_mma.cu", "quant.cu"],
+    "tcgen05_q4": ["experts_q4.cu", "quant.cu"],
+}
+
+
+def stage_sources(stage, path):
+    if stage in ("gate_up", "down"):
+        return PATH_SOURCES.get(path, []) + _COMMON
+    return STAGE_SOURCES[stage]
 
 
 def parse(argv=None):
@@ -204,7 +213,7 @@ def block_work(cfg, counts, wb=2.0):
     return flops, byts
 
 
-def roofline_of(work, stage_mean, path_name, pk, cfg):
+def roofline_of(work, stage_mean, path_name, pk, cfg, weights="packed"):
     """The roofline object of the dominant stage's kernel: algorithmic work per
     launch over its live mean duration, against the burst tensor peak or the
     copy bandwidth, whichever bound is slower."""
@@ -222,7 +231,7 @@ def roofline_of(work, stage_mean, path_name, pk, cfg):
         roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_for(dom, cfg.name)
+    roof["traffic"] = traffic_for(dom, cfg.name, path_name, weights)
     roof["kernel"] = "experts_fused" if (dom == "gate_up" and path_name == "tcgen05_decode") else dom
     roof["kernel_ms"] = stage_mean[dom]
     roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
@@ -251,22 +260,22 @@ def block_roofline_of(cfg, counts, wb, mean_ms, pk):
     return out
 
 
-def kernel_source_sha(stage):
+def kernel_source_sha(stage, path):
     h = hashlib.sha256()
-    for n in STAGE_SOURCES[stage]:
+    for n in stage_sources(stage, path):
         with open(os.path.join(ROOT, "mixture_experts_layer_98_b300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(stage, config):
+def traffic_for(stage, config, path, weights="packed"):
     """DRAM bytes per launch of the stage's kernel from the committed ncu summary,
-    or None when there is none or the kernel sources changed since."""
+    or None when there is none or the kernel's sources changed since."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     d = json.load(open(TRAFFIC_FILE))
-    e = d.get("entries", {}).get(f"{config}:{stage}")
-    if e is None or e.get("source_sha") != kernel_source_sha(stage):
+    e = d.get("entries", {}).get(f"{config}:{weights}:{path}:{stage}")
+    if e is None or e.get("source_sha") != kernel_source_sha(stage, path):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -541,7 +550,8 @@ def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clock
     wb = WEIGHT_BYTES["q4" if q4 is not None else "bf16"]
     work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode", wb=wb)
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
-    roof = roofline_of(work, stage_mean, path_name, pk, cfg)
+    roof = roofline_of(work, stage_mean, path_name, pk, cfg,
+                       "q4" if q4 is not None else args.weights)
     block = block_roofline_of(cfg, counts, wb, mean_ms, pk)
 
     e2e = None

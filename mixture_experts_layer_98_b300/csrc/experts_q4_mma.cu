@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
+        const uint64_t pol_once = ptx::l2_policy_evict_first();
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
             const Item it = item_of(p, item);
             const RowTile tl = p.tiles[it.tile];
@@ -236,14 +237,16 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
                 const size_t c1 = ((e0 + b1) * p.num_kb + kb) * kQ4CodeBlockBytes;
                 const size_t s0 = ((e0 + b0) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
                 const size_t s1 = ((e0 + b1) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
-                ptx::bulk_load(st + C::kCodeOff, p.codes0 + c0, kQ4CodeBlockBytes, &full_bar[stage]);
-                ptx::bulk_load(st + C::kCodeOff + kQ4CodeBlockBytes, p.codes1 + c1,
-                               kQ4CodeBlockBytes, &full_bar[stage]);
+                // codes and scales are read once per forward: evicted first
+                ptx::bulk_load_hint(st + C::kCodeOff, p.codes0 + c0, kQ4CodeBlockBytes,
+                                    &full_bar[stage], pol_once);
+                ptx::bulk_load_hint(st + C::kCodeOff + kQ4CodeBlockBytes, p.codes1 + c1,
+                                    kQ4CodeBlockBytes, &full_bar[stage], pol_once);
                 if (new_group) {
-                    ptx::bulk_load(st + C::kScaleOff, p.scales0 + s0, kQ4ScaleBlockBytes,
-                                   &full_bar[stage]);
-                    ptx::bulk_load(st + C::kScaleOff + kQ4ScaleBlockBytes, p.scales1 + s1,
-                                   kQ4ScaleBlockBytes, &full_bar[stage]);
+                    ptx::bulk_load_hint(st + C::kScaleOff, p.scales0 + s0, kQ4ScaleBlockBytes,
+                                        &full_bar[stage], pol_once);
+                    ptx::bulk_load_hint(st + C::kScaleOff + kQ4ScaleBlockBytes, p.scales1 + s1,
+                                        kQ4ScaleBlockBytes, &full_bar[stage], pol_once);
                 }
                 ++issued;
                 if (++stage == kS) {

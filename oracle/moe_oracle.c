@@ -493,13 +493,11 @@ int oracle_moe_forward(const uint16_t* x, int T, int H, const uint16_t* Wr, cons
  *     already);
  *   - the code of w is q = clamp(rint(fp32(w - b) / s), 0, 15), every step in
  *     fp32 arithmetic (q = 0 when s = 0);
- *   - the weight the forward computes with is the exact value q·s + b (no
- *     rounding of the weight itself: the page stores a scale and a bias per
- *     group and says nothing of a rounded intermediate weight);
- *   - oracle_dequantize_q4 also gives the nearest bf16 of that value, the
- *     form a bf16 kernel consumes.
- * A forward with quantised experts is the block forward with the expert
- * weights q·s + b in double (oracle_moe_forward_q4).
+ *   - the dequantised weight is w' = bf16(q·s + b), rounded once from the
+ *     exact value (oracle_dequantize_q4; oracle_dequantize_q4_f64 gives the
+ *     exact value itself).
+ * A forward with quantised experts is the forward with the weights W'
+ * (oracle_moe_forward_q4 computes it from the codes, scales and biases).
  */
 
 static float q4_f32(uint16_t b) {
@@ -580,18 +578,20 @@ int oracle_dequantize_q4_f64(const uint8_t* q, const uint16_t* s, const uint16_t
     return 0;
 }
 
-/* Row `row` of a 4-bit matrix with `cols` columns, as exact weights. */
+/* Row `row` of a 4-bit matrix with `cols` columns, as the dequantised
+ * weights w' = bf16(q·s + b). */
 static void q4_row(const uint8_t* q, const uint16_t* s, const uint16_t* b, size_t row, int cols,
                    double* out) {
     const int groups = cols / 128;
     for (int c = 0; c < cols; ++c) {
         const size_t g = row * (size_t)groups + (size_t)(c / 128);
-        out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +
-                 oracle_bf16_to_f64(b[g]);
+        const double v = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +
+                         oracle_bf16_to_f64(b[g]);
+        out[c] = oracle_bf16_to_f64(oracle_f64_to_bf16(v));
     }
 }
 
-/* oracle_expert_mlp of expert e on 4-bit weights (exact values q·s + b). */
+/* oracle_expert_mlp of expert e on 4-bit weights (the dequantised w'). */
 static int expert_mlp_q4(const uint16_t* x_row, int H, const experts_t* W, int e, int I,
                          int flags, double* y) {
     double* a = (double*)malloc((size_t)I * sizeof(double));
@@ -655,8 +655,8 @@ static int token_output_q4(const uint16_t* x_row, int H, const int32_t* idx_row,
 
 /* The block forward on 4-bit experts: codes q* [E,I,H] / [E,I,H] / [E,H,I]
  * (one byte per code), scales s* and biases b* [E, rows, cols / 128] bf16, as
- * oracle_quantize_q4 writes them; every other argument as for
- * oracle_moe_forward_b. */
+ * oracle_quantize_q4 writes them; the weights are w' = bf16(q·s + b); every
+ * other argument as for oracle_moe_forward_b. */
 int oracle_moe_forward_q4(const uint16_t* x, int T, int H, const uint16_t* Wr, const float* bias,
                           int capacity, const uint8_t* qg, const uint16_t* sg, const uint16_t* bg,
                           const uint8_t* qu, const uint16_t* su, const uint16_t* bu,

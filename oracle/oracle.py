@@ -305,7 +305,7 @@ def quantize_q4(W):
 
 
 def dequantize_q4(q, s, b):
-    """The nearest bf16 of q·s + b per element (bf16 bits, the shape of q)."""
+    """W' = bf16(q·s + b) per element, rounded once (bf16 bits, the shape of q)."""
     q = _c(q, np.uint8)
     s = _c(s, np.uint16)
     b = _c(b, np.uint16)
@@ -317,8 +317,8 @@ def dequantize_q4(q, s, b):
 
 
 def dequantize_q4_f64(q, s, b):
-    """The exact weights q·s + b (float64, the shape of q): the values the
-    4-bit forward computes with."""
+    """The exact values q·s + b (float64, the shape of q), before the one
+    rounding to bf16 that gives the dequantised weights."""
     q = _c(q, np.uint8)
     s = _c(s, np.uint16)
     b = _c(b, np.uint16)
@@ -344,7 +344,7 @@ def _q4_args(q4):
 
 def moe_forward_q4(x, Wr, q4, K, norm, rows=None, flags=0, bias=None, capacity=0):
     """moe_forward on 4-bit experts (q4 from quantize_experts_q4): the expert
-    weights are the exact values q·s + b.  Same results dict as moe_forward."""
+    weights are w' = bf16(q·s + b).  Same results dict as moe_forward."""
     x = _c(x, np.uint16)
     Wr = _c(Wr, np.uint16)
     a9 = _q4_args(q4)
@@ -373,7 +373,7 @@ def moe_forward_q4(x, Wr, q4, K, norm, rows=None, flags=0, bias=None, capacity=0
 
 
 def token_output_q4(x_row, idx_row, w_row, q4, flags=0, unrounded=False):
-    """token_output on 4-bit experts (exact weights q·s + b)."""
+    """token_output on 4-bit experts (weights w' = bf16(q·s + b))."""
     x_row = _c(x_row, np.uint16)
     idx_row = _c(idx_row, np.int32)
     w_row = _c(w_row, np.float32)

@@ -9,8 +9,8 @@
   (tokens on the MMA's M side instead of the weights, so only the fp32
   summation order differs): routing outputs bitwise equal, the block output
   within two bf16 ulps, at decode sizes, with K splits, at a prefill size,
-  with a capacity and a selection bias; and it is compared with the oracle
-  run on the oracle's dequantised weights.
+  with a capacity and a selection bias; and it is compared with the
+  oracle's 4-bit forward (on its own codes) at small and full decode sizes.
 """
 import numpy as np
 import pytest
@@ -179,19 +179,22 @@ def test_q4_forward_against_the_oracle(moe, T, H, E, K, I, norm, kernel):
                                        norm)
     torch.cuda.synchronize()
     b = host_bits(inp)
-    for name in ("W_gate", "W_up", "W_down"):  # the oracle's own quantise + dequantise
-        b[name] = oracle.dequantize_q4(*oracle.quantize_q4(b[name]))
+    # the oracle's own quantiser, and its forward on the codes
+    q4o = oracle.quantize_experts_q4(b["W_gate"], b["W_up"], b["W_down"])
     g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
              w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
-    compare(b, g, K, norm)
+    compare(b, g, K, norm, q4=q4o)
 
 
 @pytest.mark.parametrize("name,kernel", [("decode_t1", "warp_mma"), ("decode_t1", "tcgen05"),
+                                         ("decode_t4", "warp_mma"), ("decode_t16", "warp_mma"),
+                                         ("decode_t64", "warp_mma"),
                                          ("mixtral_decode_t1", "warp_mma")])
 def test_q4_full_size_against_the_oracle(moe, name, kernel):
     # a full decode layer: the oracle quantises, with its own quantiser, the
     # experts the GPU selected (a selection the oracle does not share fails the
-    # index check) and runs the whole block on the dequantised weights
+    # index check; the other experts' codes stay zero and are never read) and
+    # runs the whole block on the codes
     cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, "cuda")
     q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
@@ -200,12 +203,18 @@ def test_q4_full_size_against_the_oracle(moe, name, kernel):
     torch.cuda.synchronize()
     b = host_bits(inp)
     chosen = sorted(set(idx.cpu().numpy().ravel().tolist()))
-    for m in ("W_gate", "W_up", "W_down"):
+    q4o = {}
+    for m, name_q in (("W_gate", "gate"), ("W_up", "up"), ("W_down", "down")):
+        E, R, C = b[m].shape
+        q = np.zeros((E, R, C), np.uint8)
+        sc = np.zeros((E, R, C // 128), np.uint16)
+        bi = np.zeros((E, R, C // 128), np.uint16)
         for e in chosen:
-            b[m][e] = oracle.dequantize_q4(*oracle.quantize_q4(b[m][e]))
+            q[e], sc[e], bi[e] = oracle.quantize_q4(b[m][e])
+        q4o[name_q] = (q, sc, bi)
     g = dict(out=mi.bits(out), logits=lg.cpu().numpy(), idx=idx.cpu().numpy(),
              w=w.cpu().numpy(), aux=float(aux.cpu()[0]), counts=None)
-    compare(b, g, cfg.K, cfg.norm)
+    compare(b, g, cfg.K, cfg.norm, q4=q4o)
 
 
 @pytest.mark.parametrize("name", ["decode_t4", "prefill_small"])

@@ -476,9 +476,9 @@ def pin_q4_error_bound():
 
 
 def pin_q4_exact_weights():
-    # The 4-bit forward computes with q·s + b exactly: on a grid the exact
-    # weights are the original ones; for random weights they lie within s/2 of
-    # them (no bf16 term), and the bf16 dequantisation is their nearest bf16.
+    # The exact values q·s + b: on a grid they are the original weights; for
+    # random weights they lie within s/2 of them (no bf16 term), and the
+    # dequantised weights are their nearest bf16.
     rng = np.random.default_rng(42)
     rows, cols = 4, 256
     k = rng.integers(0, 16, size=(rows, cols))
@@ -504,12 +504,13 @@ def pin_q4_exact_weights():
 
 def pin_q4_forward_single_expert_is_swiglu():
     # E = K = 1 on 4-bit weights: one SwiGLU MLP (numpy float64) with the weights
-    # q·s + b, every 128-column group with its own scale and bias.
+    # bf16(q·s + b), every 128-column group with its own scale and bias.
     _, b = rand_case(9, 256, 1, 1, 256, seed=43, norm=True)
     q4 = oracle.quantize_experts_q4(b["W_gate"], b["W_up"], b["W_down"])
     r = oracle.moe_forward_q4(b["x"], b["W_router"], q4, 1, True)
-    Wg, Wu, Wd = (q4[n][0].astype(np.float64) * np.repeat(bf16_bits_to_f64(q4[n][1]), 128, -1)
-                  + np.repeat(bf16_bits_to_f64(q4[n][2]), 128, -1) for n in ("gate", "up", "down"))
+    Wg, Wu, Wd = (f64_rne_bf16_value(
+        q4[n][0].astype(np.float64) * np.repeat(bf16_bits_to_f64(q4[n][1]), 128, -1)
+        + np.repeat(bf16_bits_to_f64(q4[n][2]), 128, -1)) for n in ("gate", "up", "down"))
     y = np_swiglu(bf16_bits_to_f64(b["x"]), Wg[0], Wu[0], Wd[0])
     assert np.abs(r["out_f64"] - y).max() <= 1e-9 * np.abs(y).max()
     # and not the bf16 forward on the original weights (the quantisation shows)
@@ -605,14 +606,14 @@ MUTATIONS = {
     "q4_codes_truncate": ("rintf((q4_f32(w[j]) - bf) / sf)", "truncf((q4_f32(w[j]) - bf) / sf)"),
     "q4_wrong_group": ("const long long gi = r * groups + c / 128;",
                        "const long long gi = r * groups + c % groups;"),
-    "q4_forward_bias_dropped": ("out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g]);",
-                                "out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]);"),
+    "q4_forward_bias_dropped": ("const double v = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                         oracle_bf16_to_f64(b[g]);",
+                                "const double v = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]);"),
     "q4_forward_wrong_group": ("const size_t g = row * (size_t)groups + (size_t)(c / 128);",
                                "const size_t g = row * (size_t)groups + (size_t)(c % groups);"),
     "q4_forward_gate_up_swapped": ("q4_row(W->qg, W->sg, W->bg, row, H, wg);",
                                    "q4_row(W->qu, W->su, W->bu, row, H, wg);"),
-    "q4_forward_rounds_weights": ("out[c] = (double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g]);",
-                                  "out[c] = oracle_bf16_to_f64(oracle_f64_to_bf16((double)q[row * (size_t)cols + c] * oracle_bf16_to_f64(s[g]) +\n                 oracle_bf16_to_f64(b[g])));"),
+    "q4_forward_unrounded_weights": ("out[c] = oracle_bf16_to_f64(oracle_f64_to_bf16(v));",
+                                     "out[c] = v;"),
     "weights_from_biased_keys": (
         "logits[i];\n    oracle_softmax(logits, T, E, probs);",
         "logits[i];\n    oracle_softmax(keys, T, E, probs);"),
