@@ -193,5 +193,8 @@ def compare(b, g, K, norm, rows=None, bias=None, capacity=0, max_near_ties=None,
         rep["out_rms"] = rms
         rep["out_rel"] = rel
         rep["out_excess"] = excess
+        # the plain figure beside the bound's verdict: max|err| / RMS(oracle)
+        print(f"[parity] {rows_arr.size} rows: max|err|/RMS = {rel:.3e}, "
+              f"excess over 2e-2·RMS + half-ulp = {excess:.2e}")
         assert excess <= 0.0, rep
     return rep
