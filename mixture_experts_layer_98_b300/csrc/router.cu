@@ -53,21 +53,39 @@ __global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
     const int c0 = blockIdx.z * vps;
     const int t0 = blockIdx.x * kSplitTokens;
     const int nt = min(kSplitTokens, T - t0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.y * kSplitWarps + warp;
+    const uint4* wr = reinterpret_cast<const uint4*>(Wr) + (size_t)min(e, E - 1) * vpr + c0;
+    // the first router-weight vectors of this warp's row are requested before
+    // the tokens are staged, so the two memory round trips overlap
+    constexpr int kEarly = 4;
+    uint4 w_early[kEarly];
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j) {
+        const int c = lane + 32 * j;
+        if (c < vps) w_early[j] = wr[c];
+    }
     const uint4* xg = reinterpret_cast<const uint4*>(x) + (size_t)t0 * vpr + c0;
     for (int i = threadIdx.x; i < nt * vps; i += blockDim.x) {
         const int m = i / vps, c = i - m * vps;
         xs[i] = xg[(size_t)m * vpr + c];
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = blockIdx.y * kSplitWarps + warp;
     if (e >= E) return;
-    const uint4* wr = reinterpret_cast<const uint4*>(Wr) + (size_t)e * vpr + c0;
     float acc[kSplitTokens];
 #pragma unroll
     for (int m = 0; m < kSplitTokens; ++m) acc[m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j) {
+        const int c = lane + 32 * j;
+        if (c < vps) {
+#pragma unroll
+            for (int m = 0; m < kSplitTokens; ++m)
+                if (m < nt) acc[m] = dot8_bf16(w_early[j], xs[m * vps + c], acc[m]);
+        }
+    }
 #pragma unroll 4
-    for (int c = lane; c < vps; c += 32) {
+    for (int c = lane + 32 * kEarly; c < vps; c += 32) {
         const uint4 wv = wr[c];
 #pragma unroll
         for (int m = 0; m < kSplitTokens; ++m)
