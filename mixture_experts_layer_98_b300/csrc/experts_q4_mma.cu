@@ -21,17 +21,18 @@
 // m16n8k16 MMAs whose B fragments are the tile's tokens, 8 per MMA.
 //
 // Fragment mapping.  A thread (g = lane / 4, c = lane % 4) of the warp that
-// owns weight rows R..R+15 reads, per 64-column k-block, the code words c and
-// c + 4 of rows R + g and R + g + 8 (quant.cu: word c' of a row holds columns
-// 8c'..8c'+7, pair j = columns 8c'+2j, 8c'+2j+1).  k-step t (0..3) of the
-// block takes pair 2(t%2) of word c + 4(t/2) as the fragment's columns 2c,
-// 2c+1 and pair 2(t%2)+1 as its columns 2c+8, 2c+9: fragment column f of step
-// t is block column 8((f%8)/2) + 32(t/2) + 4(t%2) + 2(f/8) + f%2, a
-// permutation of the block's 64 columns.  The token fragment applies the same
-// permutation: thread (g, c) loads the 4 consecutive bf16 of token g from
-// column 8c + 32(t/2) + 4(t%2) (8 bytes, 128-byte swizzled rows).  The sum over
-// k is order-free, so the MMA computes the exact products of the bf16 forward
-// on the dequantised weights, accumulated in fp32 in another order.
+// owns weight rows R..R+15 reads, per 64-column k-block, the adjacent code
+// words 2c and 2c + 1 of rows R + g and R + g + 8 (one 8-byte load per row;
+// quant.cu: word c' of a row holds columns 8c'..8c'+7, pair j = columns
+// 8c'+2j, 8c'+2j+1).  k-step t (0..3) of the block takes pair 2(t%2) of word
+// 2c + t/2 as the fragment's columns 2c, 2c+1 and pair 2(t%2)+1 as its columns
+// 2c+8, 2c+9: fragment column f of step t is block column
+// 16((f%8)/2) + 8(t/2) + 4(t%2) + 2(f/8) + f%2, a permutation of the block's
+// 64 columns.  The token fragment applies the same permutation: thread (g, c)
+// needs, over the four steps, the 16 consecutive bf16 of token g from column
+// 16c, two 16-byte loads from the 128-byte swizzled row.  The sum over k is
+// order-free, so the MMA computes the exact products of the bf16 forward on
+// the dequantised weights, accumulated in fp32 in another order.
 //
 // Work items: gate/up (row tile, 128 I rows: the gate rows and the same up
 // rows), down (row tile, 256 H rows), on row tiles of at most 16 tokens
@@ -45,7 +46,9 @@
 // the slices in slice order and runs their epilogue.
 //
 // Roles: warp 0 producer (token boxes by TMA, code and scale blocks by bulk
-// copy into a ring of stages), warps 1-8 consumers.  Every wait is bounded
+// copy into a ring of stages, one 128-column group a stage: a group's scales
+// serve both its k-blocks, and the per-stage waits and releases are paid once
+// per 128 columns), warps 1-8 consumers.  Every wait is bounded
 // (2 s); on expiry the CTA records MOE_ERR_TIMEOUT, lets its copies land and
 // exits (no CTA-wide barrier follows the main loops).
 #include "moe_common.cuh"
@@ -64,15 +67,20 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum { kGateUp = 0, kDown = 1 };
 
-// Stage: NT token boxes (8 rows x 128 bytes, 128-byte swizzled, each on a
-// 1024-byte boundary), the two 4 KB code blocks and two 512-byte scale blocks
-// of the item's 256 weight rows.  Two CTAs per SM.
+constexpr int kKbPerStage = 2;     // k-blocks per stage: one 128-column scale group
+
+// Stage (one 128-column group of the item's 256 weight rows): for each of its
+// two k-blocks NT token boxes (8 rows x 128 bytes, 128-byte swizzled, each on
+// a 1024-byte boundary; box n of k-block h at (h·NT + n)·1024), then per plane
+// the group's two 4 KB code blocks (contiguous in the packed layout, one 8 KB
+// copy) and its 512-byte scale block.  Two CTAs per SM.
 template <int NT>
 struct MmaCfg {
     static_assert(NT * kTokBox <= kQ4MmaRows, "a stage holds a whole row tile");
     static constexpr int kTokOff = 0;
-    static constexpr int kCodeOff = NT * kTokBox * 128;
-    static constexpr int kScaleOff = kCodeOff + 2 * kQ4CodeBlockBytes;
+    static constexpr int kCodeOff = kKbPerStage * NT * kTokBox * 128;
+    static constexpr int kPlaneCodeBytes = kKbPerStage * kQ4CodeBlockBytes;
+    static constexpr int kScaleOff = kCodeOff + 2 * kPlaneCodeBytes;
     static constexpr int kBytes = kScaleOff + 2 * kQ4ScaleBlockBytes;
     static constexpr int kCtasPerSm = 2;
     static constexpr int kBudget = 112 * 1024 - 1024;
@@ -88,7 +96,7 @@ struct MmaParams {
     int n_nt;               // items per row tile: I / 128 (gate/up), H / 256 (down)
     int num_kb;             // k-blocks of 64
     int ksplit;
-    int kb_per;
+    int grp_per;            // 128-column groups per K slice
     float* partial;         // [items][ksplit][2][part_rows][128] slice accumulators
     int part_rows;
     int32_t* counters;      // per item and consumer warp: arrivals of its slices
@@ -109,7 +117,7 @@ struct MmaParams {
 };
 
 struct Item {
-    int pitem, tile, nt, ks, kb0, kb1;
+    int pitem, tile, nt, ks, g0, g1;  // groups [g0, g1) of the slice
 };
 
 __device__ __forceinline__ Item item_of(const MmaParams& p, int item) {
@@ -118,8 +126,8 @@ __device__ __forceinline__ Item item_of(const MmaParams& p, int item) {
     it.ks = item % p.ksplit;
     it.tile = it.pitem / p.n_nt;
     it.nt = it.pitem % p.n_nt;
-    it.kb0 = it.ks * p.kb_per;
-    it.kb1 = min(p.num_kb, it.kb0 + p.kb_per);
+    it.g0 = it.ks * p.grp_per;
+    it.g1 = min(p.groups, it.g0 + p.grp_per);
     return it;
 }
 
@@ -174,6 +182,69 @@ __device__ __forceinline__ void store_one(const MmaParams& p, const RowTile& tl,
     }
 }
 
+// One stage (a 128-column group) of a consumer warp: its two 16-row weight
+// tiles against NN token boxes.  code_off / scale_off: this thread's code and
+// scale words of each tile within the stage; tok0 / tok1: its two 16-byte
+// chunks of token row g within a box.
+template <int NT, int NN>
+__device__ __forceinline__ void stage_mma(const uint8_t* st, const int (&code_off)[2],
+                                          const int (&scale_off)[2], int tok0, int tok1,
+                                          float (&acc)[2][NT][4]) {
+    static_assert(NN <= NT, "boxes of a stage");
+    using C = MmaCfg<NT>;
+    // scale and bias of rows g, g + 8 of both tiles (the group's)
+    __nv_bfloat162 s2[2][2], b2[2][2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t sbw = *reinterpret_cast<const uint32_t*>(st + scale_off[i] + 32 * h);
+            s2[i][h] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw & 0xFFFFu)));
+            b2[i][h] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw >> 16)));
+        }
+#pragma unroll
+    for (int h = 0; h < kKbPerStage; ++h) {
+        // words 2c (x) and 2c + 1 (y) of rows g and g + 8 of both tiles
+        uint2 wq[2][2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint8_t* cp = st + code_off[i] + h * kQ4CodeBlockBytes;
+            wq[i][0] = *reinterpret_cast<const uint2*>(cp);
+            wq[i][1] = *reinterpret_cast<const uint2*>(cp + 8 * 32);
+        }
+        // token g, columns 16c..16c+7 (chunk 0) and 16c+8..16c+15 (chunk 1)
+        uint4 tk[NN][2];
+#pragma unroll
+        for (int n = 0; n < NN; ++n) {
+            const uint8_t* tp = st + C::kTokOff + (h * NT + n) * (kTokBox * 128);
+            tk[n][0] = *reinterpret_cast<const uint4*>(tp + tok0);
+            tk[n][1] = *reinterpret_cast<const uint4*>(tp + tok1);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int j = 2 * (t & 1);
+            uint32_t a[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t w0 = (t >> 1) ? wq[i][0].y : wq[i][0].x;  // row g
+                const uint32_t w1 = (t >> 1) ? wq[i][1].y : wq[i][1].x;  // row g + 8
+                a[i][0] = dq_pair(w0, j, s2[i][0], b2[i][0]);          // cols 2c, 2c+1
+                a[i][1] = dq_pair(w1, j, s2[i][1], b2[i][1]);
+                a[i][2] = dq_pair(w0, j + 1, s2[i][0], b2[i][0]);      // cols 2c+8, 2c+9
+                a[i][3] = dq_pair(w1, j + 1, s2[i][1], b2[i][1]);
+            }
+#pragma unroll
+            for (int n = 0; n < NN; ++n) {
+                const uint4& v = tk[n][t >> 1];
+                const uint32_t b0 = (t & 1) ? v.z : v.x;
+                const uint32_t b1 = (t & 1) ? v.w : v.y;
+                mma_bf16_16816(acc[0][n], a[0], b0, b1);
+                mma_bf16_16816(acc[1][n], a[1], b0, b1);
+            }
+        }
+    }
+}
+
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
     expert_q4_mma_kernel(const __grid_constant__ CUtensorMap tmA, const MmaParams p) {
@@ -218,36 +289,33 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
             const int b0 = MODE == kGateUp ? it.nt : 2 * it.nt;
             const int b1 = MODE == kGateUp ? it.nt : 2 * it.nt + 1;
             const size_t e0 = (size_t)tl.expert * p.blocks_per_expert;
-            for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                // a 128-column group's scales are read at its first k-block of
-                // the slice only (the consumers keep them in registers)
-                const bool new_group = (kb & 1) == 0 || kb == it.kb0;
-                const uint32_t bytes = nbox * kTokBox * 128 + 2 * kQ4CodeBlockBytes +
-                                       (new_group ? 2 * kQ4ScaleBlockBytes : 0);
+            for (int gi = it.g0; gi < it.g1; ++gi) {
+                const int kb = kKbPerStage * gi;
+                const uint32_t bytes = kKbPerStage * nbox * kTokBox * 128 +
+                                       2 * C::kPlaneCodeBytes + 2 * kQ4ScaleBlockBytes;
                 if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_s, kTimeoutNs)) {
                     ok = false;
                     break;
                 }
                 uint8_t* st = smem + stage * C::kBytes;
                 ptx::mbar_arrive_expect_tx(&full_bar[stage], bytes);
-                for (int b = 0; b < nbox; ++b)
-                    ptx::tma_load_2d(st + C::kTokOff + b * kTokBox * 128, &tmA, &full_bar[stage],
-                                     kb * kBK, tl.row0 + b * kTokBox);
+                for (int h = 0; h < kKbPerStage; ++h)
+                    for (int b = 0; b < nbox; ++b)
+                        ptx::tma_load_2d(st + C::kTokOff + (h * NT + b) * kTokBox * 128, &tmA,
+                                         &full_bar[stage], (kb + h) * kBK, tl.row0 + b * kTokBox);
                 const size_t c0 = ((e0 + b0) * p.num_kb + kb) * kQ4CodeBlockBytes;
                 const size_t c1 = ((e0 + b1) * p.num_kb + kb) * kQ4CodeBlockBytes;
-                const size_t s0 = ((e0 + b0) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
-                const size_t s1 = ((e0 + b1) * p.groups + kb / 2) * kQ4ScaleBlockBytes;
+                const size_t s0 = ((e0 + b0) * p.groups + gi) * kQ4ScaleBlockBytes;
+                const size_t s1 = ((e0 + b1) * p.groups + gi) * kQ4ScaleBlockBytes;
                 // codes and scales are read once per forward: evicted first
-                ptx::bulk_load_hint(st + C::kCodeOff, p.codes0 + c0, kQ4CodeBlockBytes,
+                ptx::bulk_load_hint(st + C::kCodeOff, p.codes0 + c0, C::kPlaneCodeBytes,
                                     &full_bar[stage], pol_once);
-                ptx::bulk_load_hint(st + C::kCodeOff + kQ4CodeBlockBytes, p.codes1 + c1,
-                                    kQ4CodeBlockBytes, &full_bar[stage], pol_once);
-                if (new_group) {
-                    ptx::bulk_load_hint(st + C::kScaleOff, p.scales0 + s0, kQ4ScaleBlockBytes,
-                                        &full_bar[stage], pol_once);
-                    ptx::bulk_load_hint(st + C::kScaleOff + kQ4ScaleBlockBytes, p.scales1 + s1,
-                                        kQ4ScaleBlockBytes, &full_bar[stage], pol_once);
-                }
+                ptx::bulk_load_hint(st + C::kCodeOff + C::kPlaneCodeBytes, p.codes1 + c1,
+                                    C::kPlaneCodeBytes, &full_bar[stage], pol_once);
+                ptx::bulk_load_hint(st + C::kScaleOff, p.scales0 + s0, kQ4ScaleBlockBytes,
+                                    &full_bar[stage], pol_once);
+                ptx::bulk_load_hint(st + C::kScaleOff + kQ4ScaleBlockBytes, p.scales1 + s1,
+                                    kQ4ScaleBlockBytes, &full_bar[stage], pol_once);
                 ++issued;
                 if (++stage == kS) {
                     stage = 0;
@@ -284,11 +352,20 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.f;
-        // scale and bias of rows g, g + 8 of both tiles: one 128-column group
-        // spans two k-blocks
-        __nv_bfloat162 s2[2][2], b2[2][2];
+        // this thread's bytes of a stage: code words 2c, 2c + 1 of row g of
+        // both 16-row tiles, their rows' scale words, token g's 32 bytes from
+        // column 16c (two swizzled 16-byte chunks)
+        int code_off[2], scale_off[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int bi = plane_of<MODE>(cw, i), ri = row_in_block<MODE>(cw, i);
+            code_off[i] = C::kCodeOff + bi * C::kPlaneCodeBytes + (ri + g) * 32 + 8 * c;
+            scale_off[i] = C::kScaleOff + bi * kQ4ScaleBlockBytes + (ri + g) * 4;
+        }
+        const int tok0 = g * 128 + (((2 * c) ^ g) << 4);
+        const int tok1 = g * 128 + (((2 * c + 1) ^ g) << 4);
 
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        for (int gi = it.g0; gi < it.g1; ++gi) {
             int good = 1;
             if (lane == 0) good = ptx::mbar_wait_bounded(&full_bar[stage], phase, &abort_s, kTimeoutNs);
             good = __shfl_sync(0xffffffffu, good, 0);
@@ -297,55 +374,13 @@ __global__ void __launch_bounds__(kThreadsM, MmaCfg<NT>::kCtasPerSm)
                 break;
             }
             const uint8_t* st = smem + stage * C::kBytes;
-            // code words c, c + 4 of rows g and g + 8 of both 16-row tiles, and
-            // their rows' scale and bias (the k-block's 128-column group)
-            uint32_t wq[2][4];
-            const bool new_group = (kb & 1) == 0 || kb == it.kb0;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int bi = plane_of<MODE>(cw, i), ri = row_in_block<MODE>(cw, i);
-                const uint32_t* r0 = reinterpret_cast<const uint32_t*>(
-                    st + C::kCodeOff + bi * kQ4CodeBlockBytes + (ri + g) * 32);
-                const uint32_t* r1 = r0 + 8 * 8;  // row + 8
-                wq[i][0] = r0[c];
-                wq[i][1] = r0[c + 4];
-                wq[i][2] = r1[c];
-                wq[i][3] = r1[c + 4];
-                if (new_group) {
-                    const uint32_t* sb = reinterpret_cast<const uint32_t*>(
-                        st + C::kScaleOff + bi * kQ4ScaleBlockBytes);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t sbw = sb[ri + g + 8 * h];
-                        s2[i][h] = __bfloat162bfloat162(
-                            __ushort_as_bfloat16((unsigned short)(sbw & 0xFFFFu)));
-                        b2[i][h] = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)(sbw >> 16)));
-                    }
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int wi = t >> 1, j = 2 * (t & 1);
-                uint32_t a[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    a[i][0] = dq_pair(wq[i][wi], j, s2[i][0], b2[i][0]);          // row g, cols 2c..
-                    a[i][1] = dq_pair(wq[i][2 + wi], j, s2[i][1], b2[i][1]);      // row g + 8
-                    a[i][2] = dq_pair(wq[i][wi], j + 1, s2[i][0], b2[i][0]);      // row g, cols 2c+8..
-                    a[i][3] = dq_pair(wq[i][2 + wi], j + 1, s2[i][1], b2[i][1]);  // row g + 8
-                }
-                // token g's 4 bf16 from column 8c + 32(t/2) + 4(t%2): chunk
-                // c + 4(t/2) of its 128-byte row, swizzled by the row (g)
-                const int off = g * 128 + (((c + 4 * wi) ^ g) << 4) + 8 * (t & 1);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    if (n < nn) {
-                        const uint2 bv =
-                            *reinterpret_cast<const uint2*>(st + C::kTokOff + n * 1024 + off);
-                        mma_bf16_16816(acc[0][n], a[0], bv.x, bv.y);
-                        mma_bf16_16816(acc[1][n], a[1], bv.x, bv.y);
-                    }
-                }
+            if constexpr (NT == 2) {
+                if (nn == 2)
+                    stage_mma<NT, 2>(st, code_off, scale_off, tok0, tok1, acc);
+                else
+                    stage_mma<NT, 1>(st, code_off, scale_off, tok0, tok1, acc);
+            } else {
+                stage_mma<NT, 1>(st, code_off, scale_off, tok0, tok1, acc);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty_bar[stage]);
@@ -489,17 +524,18 @@ double mma_fill(long long n) {
     return (double)n / (double)(rounds * kMmaGrid);
 }
 
-// K slices for `items` items of num_kb k-blocks: below two rounds of the grid
-// (where an unfilled last round costs the most, and the slice accumulators
-// stay small), the count (at most 6, at least 8 k-blocks a slice, no empty
-// slice) whose items fill the grid's rounds best; ties go to fewer slices.
-int mma_split(long long items, int num_kb) {
+// K slices for `items` items of ngroups 128-column groups: below two rounds of
+// the grid (where an unfilled last round costs the most, and the slice
+// accumulators stay small), the count (at most 6, at least 4 groups a slice,
+// no empty slice) whose items fill the grid's rounds best; ties go to fewer
+// slices.
+int mma_split(long long items, int ngroups) {
     if (items <= 0 || items >= 2 * kMmaGrid) return 1;
     int best = 1;
     double best_fill = mma_fill(items);
-    for (int ks = 2; ks <= 6 && num_kb / ks >= 8; ++ks) {
-        const int kb_per = (num_kb + ks - 1) / ks;
-        if ((num_kb + kb_per - 1) / kb_per != ks) continue;
+    for (int ks = 2; ks <= 6 && ngroups / ks >= 4; ++ks) {
+        const int g_per = (ngroups + ks - 1) / ks;
+        if ((ngroups + g_per - 1) / g_per != ks) continue;
         const double f = mma_fill(items * ks);
         if (f > best_fill + 0.02) {
             best = ks;
@@ -520,8 +556,8 @@ Q4MmaPlan q4mma_plan(const Sizes& s) {
     if (tiles > s.max_tiles(kQ4MmaRows)) tiles = s.max_tiles(kQ4MmaRows);
     pl.items_gu = tiles * (s.I / 128);
     pl.items_dn = tiles * (s.H / 256);
-    pl.ks_gu = mma_split(pl.items_gu, s.H / kBK);
-    pl.ks_dn = mma_split(pl.items_dn, s.I / kBK);
+    pl.ks_gu = mma_split(pl.items_gu, s.H / 128);
+    pl.ks_dn = mma_split(pl.items_dn, s.I / 128);
     // A tile holds at most min(T, 16) rows.
     pl.part_rows = s.T < kQ4MmaRows ? (s.T + kTokBox - 1) / kTokBox * kTokBox : kQ4MmaRows;
     const size_t per_slice = (size_t)2 * pl.part_rows * 128;
@@ -551,7 +587,7 @@ cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspac
     p.num_kb = s.H / kBK;
     p.groups = s.H / 128;
     p.ksplit = pl.ks_gu;
-    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.grp_per = (p.groups + p.ksplit - 1) / p.ksplit;
     p.partial = ws.wt_partial;
     p.counters = ws.status + 4;
     p.out = ws.hbuf;
@@ -571,7 +607,7 @@ cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspac
     p.num_kb = s.I / kBK;
     p.groups = s.I / 128;
     p.ksplit = pl.ks_dn;
-    p.kb_per = (p.num_kb + p.ksplit - 1) / p.ksplit;
+    p.grp_per = (p.groups + p.ksplit - 1) / p.ksplit;
     p.partial = ws.wt_partial + pl.partial_floats_gu;
     p.counters = ws.status + 4 + pl.n_counters_gu;
     p.out = ws.ybuf;
