@@ -504,7 +504,12 @@ cudaError_t launch_small(const float* parts, int nparts, float* logits_out, int 
                          const float* bias, int32_t* idx, float* w, const Sizes& s,
                          const Workspace& ws, int rows_per_tile, float* aux,
                          const __nv_bfloat16* x, int cap, cudaStream_t st) {
-    cudaError_t e = launch_pdl(dispatch_small_kernel<EPL, true>, dim3(1), dim3(kSmallThreads), 0,
+    // one warp per token and one thread per expert; no more warps than that
+    // (each one more party to every barrier), at least eight
+    int threads = 32 * s.T > s.E ? 32 * s.T : (s.E + 31) / 32 * 32;
+    if (threads < 256) threads = 256;
+    if (threads > kSmallThreads) threads = kSmallThreads;
+    cudaError_t e = launch_pdl(dispatch_small_kernel<EPL, true>, dim3(1), dim3(threads), 0,
                                st, parts, nparts, logits_out, norm, bias, idx, w,
                                (const float*)nullptr,
                                0, s.T, s.E, s.K, rows_per_tile, ws.counts, ws.offsets, ws.tiles,

@@ -30,6 +30,13 @@
 // every CTA is resident.  The counters are in the workspace's status region,
 // zeroed by the router kernel at the start of every forward.
 //
+// Up to kDecodeDirectTokens (= one 16-row box) tokens, the gate/up units take
+// their token box from x itself, rows 0..T-1, rather than from gathered rows:
+// the MMA computes every token of the batch against the tile's weights (the
+// same N = 16 columns a gathered tile would occupy) and the epilogue keeps the
+// columns of the tile's tokens, writing column perm_tok[row] to h row `row`.
+// No gather runs at all.
+//
 // Roles per CTA (192 threads, one CTA per SM) as in experts_wt.cu: warp 0 TMA
 // producer (5-stage ring: two 128x64 weight tiles and ceil(rows/16) 16-row
 // token boxes per k-block), warp 1 TMEM owner and MMA issuer, warps 2-5
@@ -86,6 +93,7 @@ struct DecParams {
     const char* pk_up;
     const char* pk_down;
     int a_blocks[2];       // 128-row weight blocks per expert: I/128, H/128
+    int x_direct;          // gate/up token boxes: x rows 0..T-1 (T <= kBox), not x_perm
 };
 
 struct Unit {
@@ -265,9 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tma_load_2d(sA, mw0, &full_bar[stage], kb * kBK, a0);
                         ptx::tma_load_2d(sA + kABytes, mw1, &full_bar[stage], kb * kBK, a1);
                     }
+                    // x read directly: one box, the whole batch (nrows <= T <= kBox)
+                    const int brow = (p.x_direct && x.kind == kGateUp) ? 0 : tl.row0;
                     for (int b = 0; b < nbox; ++b)
                         ptx::tma_load_2d(sB + b * kBoxBytes, mb, &full_bar[stage], kb * kBK,
-                                         tl.row0 + b * kBox);
+                                         brow + b * kBox);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -352,6 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit x = unit_of(p, u, n_gu);
             const RowTile tl = p.tiles[x.tile];
+            // Accumulator column -> tile row: the identity, except for gate/up
+            // units on x itself, where column cc is token cc and lane cc holds
+            // its row in the tile (-1: the token is not in the tile).  Read
+            // before the accumulator wait, so the loads overlap the MMAs.
+            const bool direct = p.x_direct && x.kind == kGateUp;
+            int jm = -1;
+            if (direct) {
+                const int tok = lane < tl.nrows ? p.perm_tok[tl.row0 + lane] : -1;
+                for (int j = 0; j < tl.nrows; ++j)
+                    if (__shfl_sync(0xffffffffu, tok, j) == lane) jm = j;
+            }
             int ok = 1;
             if (lane == 0)
                 ok = ptx::mbar_wait_bounded(&tfull_bar[acc], acc_phase, &abort_s, kTimeoutNs);
@@ -374,10 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld16(t1 + c, v1);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < kBox; ++j)
-                        if (c + j < tl.nrows)
-                            store_out(p, x.kind, (size_t)tl.row0 + c + j, x.blk, i,
-                                      __uint_as_float(v0[j]), __uint_as_float(v1[j]));
+                    for (int cc = 0; cc < kBox; ++cc) {
+                        const int j = direct ? __shfl_sync(0xffffffffu, jm, cc)
+                                             : (c + cc < tl.nrows ? c + cc : -1);
+                        if (j >= 0)
+                            store_out(p, x.kind, (size_t)tl.row0 + j, x.blk, i,
+                                      __uint_as_float(v0[cc]), __uint_as_float(v1[cc]));
+                    }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -396,12 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld16(t1 + c, v1);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < kBox; ++j)
-                        if (c + j < tl.nrows) {
-                            __stcg(mine + (size_t)(c + j) * kWM + i, __uint_as_float(v0[j]));
-                            __stcg(mine + ((size_t)p.part_rows + c + j) * kWM + i,
-                                   __uint_as_float(v1[j]));
+                    for (int cc = 0; cc < kBox; ++cc) {
+                        const int j = direct ? __shfl_sync(0xffffffffu, jm, cc)
+                                             : (c + cc < tl.nrows ? c + cc : -1);
+                        if (j >= 0) {
+                            __stcg(mine + (size_t)j * kWM + i, __uint_as_float(v0[cc]));
+                            __stcg(mine + ((size_t)p.part_rows + j) * kWM + i,
+                                   __uint_as_float(v1[cc]));
                         }
+                    }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -510,7 +537,8 @@ bool experts_decode_supported(const Sizes& s) {
 }
 
 cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
-                                  const int32_t* inv, __nv_bfloat16* out, cudaStream_t st) {
+                                  const __nv_bfloat16* x, const int32_t* inv,
+                                  __nv_bfloat16* out, cudaStream_t st) {
     if (!experts_decode_supported(s)) return cudaErrorInvalidValue;
     const bool packed = W.packed != nullptr;
     const long long P = s.P();
@@ -552,10 +580,13 @@ cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const 
     p.pk_down = packed ? W.packed_down(s) : nullptr;
     p.a_blocks[0] = s.I / kPackRows;
     p.a_blocks[1] = s.H / kPackRows;
+    static_assert(kDecodeDirectTokens <= kBox, "the whole batch in one token box");
+    p.x_direct = s.T <= kDecodeDirectTokens ? 1 : 0;
 
     CUtensorMap mx, mh, mg, mu, md;
-    if (!make_tma_2d(&mx, ws.x_perm, P, s.H, kBox) || !make_tma_2d(&mh, ws.hbuf, P, s.I, kBox))
-        return cudaErrorInvalidValue;
+    const bool mx_ok = p.x_direct ? make_tma_2d(&mx, x, s.T, s.H, kBox)
+                                  : make_tma_2d(&mx, ws.x_perm, P, s.H, kBox);
+    if (!mx_ok || !make_tma_2d(&mh, ws.hbuf, P, s.I, kBox)) return cudaErrorInvalidValue;
     if (packed) {  // the weight maps are not used
         mg = mu = md = mx;
     } else if (!make_tma_2d(&mg, W.gate, (uint64_t)s.E * s.I, s.H, kWM) ||

@@ -278,8 +278,11 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
                           : path == ExpertPath::kDecodeFused ? kWtRows
                           : path == ExpertPath::kWeightsQ4  ? (q4_mma ? kQ4MmaRows : kWtRows)
                                                             : kStreamRows;
-    // The tensor-core expert paths read gathered rows (x_perm); streaming reads x.
-    const __nv_bfloat16* gather_x = path == ExpertPath::kStreaming ? nullptr : x;
+    // The tensor-core expert paths read gathered rows (x_perm); streaming reads
+    // x, and so does the fused decode kernel up to kDecodeDirectTokens tokens.
+    const bool x_direct = path == ExpertPath::kStreaming ||
+                          (path == ExpertPath::kDecodeFused && s.T <= kDecodeDirectTokens);
+    const __nv_bfloat16* gather_x = x_direct ? nullptr : x;
     // Router logits: tensor cores from one full 128-token tile up (E <= 128),
     // else the CUDA-core kernel split over H.  Then routing and dispatch: one
     // CTA for at most 32 tokens, else the routing kernel and the dispatch
@@ -331,7 +334,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         case ExpertPath::kDecodeFused: {
             // experts and combine in one kernel: the whole kernel is timed as the
             // gate/up stage; the down and combine stages read zero
-            e = launch_experts_decode(W, s, ws, cap > 0 ? ws.inv : nullptr, out, st);
+            e = launch_experts_decode(W, s, ws, x, cap > 0 ? ws.inv : nullptr, out, st);
             if (e != cudaSuccess) return cuda_status(e);
             if (mid) cudaEventRecord(mid, st);
             mark(4, st);

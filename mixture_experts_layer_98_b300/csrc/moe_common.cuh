@@ -253,12 +253,16 @@ cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspac
                                   cudaStream_t st, cudaEvent_t ev_mid);
 // Decode batches (1 <= T <= kDecodeFusedTokens, shapes experts_wt_supported):
 // the weights-as-M gate/up and down units and the combine in one cooperative
-// persistent kernel (experts_decode.cu); writes out directly.
+// persistent kernel (experts_decode.cu); writes out directly.  Up to
+// kDecodeDirectTokens tokens its gate/up units read x itself (all tokens in
+// one MMA column block) and no gathered rows are needed; above, x_perm.
 constexpr int kDecodeFusedTokens = 64;
 constexpr int kDecodeAutoTokens = 16;  // MOE_PATH_AUTO uses the fused kernel up to here
+constexpr int kDecodeDirectTokens = 16;
 bool experts_decode_supported(const Sizes& s);
 cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
-                                  const int32_t* inv, __nv_bfloat16* out, cudaStream_t st);
+                                  const __nv_bfloat16* x, const int32_t* inv,
+                                  __nv_bfloat16* out, cudaStream_t st);
 // out[t] = sum over k of Y row t*K + k (Y token-major, as the expert kernels
 // store it), skipping the pairs with inv[t*K + k] < 0 when inv != null
 // (dropped by a capacity); with y_by_inv, Y is in dispatch order and row
