@@ -261,8 +261,15 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
             for (int q = 0; q < EPL; ++q) {
                 const int e = lane + 32 * q;
                 if (e < E) {
-                    float v = parts[(size_t)t * E + e];
-                    for (int sl = 1; sl < nparts; ++sl) v += parts[((size_t)sl * T + t) * E + e];
+                    // every slice loaded before the first add, summed in slice order
+                    float pv[kRouterMaxSplits];
+#pragma unroll
+                    for (int sl = 0; sl < kRouterMaxSplits; ++sl)
+                        pv[sl] = sl < nparts ? parts[((size_t)sl * T + t) * E + e] : 0.f;
+                    float v = pv[0];
+#pragma unroll
+                    for (int sl = 1; sl < kRouterMaxSplits; ++sl)
+                        if (sl < nparts) v += pv[sl];
                     l[q] = v;
                     if (logits_out) logits_out[(size_t)t * E + e] = v;
                 } else {
@@ -559,7 +566,8 @@ cudaError_t launch_route_dispatch_small(const float* parts, int nparts, float* l
                                         const __nv_bfloat16* x, const Sizes& s,
                                         const Workspace& ws, int rows_per_tile, float* aux,
                                         int cap, cudaStream_t st) {
-    if (s.T > kRouteDispatchTokens) return cudaErrorInvalidValue;
+    if (s.T > kRouteDispatchTokens || nparts < 1 || nparts > kRouterMaxSplits)
+        return cudaErrorInvalidValue;
     // Up to 128 KB of gathered rows are copied by the routing CTA itself (one
     // or two decode tokens); more go to the gather kernel, which spreads them
     // over the SMs.

@@ -37,12 +37,24 @@
 // columns of the tile's tokens, writing column perm_tok[row] to h row `row`.
 // No gather runs at all.
 //
+// Up to kDecodeRouteTokens tokens (one per warp) the kernel also routes and
+// dispatches the batch itself (launched straight after the router logits):
+// every CTA sums the partial logits, routes each token (routing.cuh: softmax,
+// top-k, renormalisation), counts, scans and scatters the pairs into its own
+// shared memory -- the same arithmetic, in the same order, as the one-CTA
+// routing kernel of dispatch.cu, so every CTA holds the same tile table --
+// and the grid's last CTAs (the ones with the fewest units) write the
+// forward's routing outputs (logits, top-k, counts, offsets, tile table,
+// permutation) and aux, each a share.  The expert weights then start
+// streaming one kernel boundary earlier.
+//
 // Roles per CTA (192 threads, one CTA per SM) as in experts_wt.cu: warp 0 TMA
 // producer (5-stage ring: two 128x64 weight tiles and ceil(rows/16) 16-row
 // token boxes per k-block), warp 1 TMEM owner and MMA issuer, warps 2-5
 // epilogue.  Every wait is bounded (2 s); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include "moe_common.cuh"
+#include "routing.cuh"
 #include "sm100_ptx.cuh"
 
 namespace moe {
@@ -94,7 +106,205 @@ struct DecParams {
     const char* pk_down;
     int a_blocks[2];       // 128-row weight blocks per expert: I/128, H/128
     int x_direct;          // gate/up token boxes: x rows 0..T-1 (T <= kBox), not x_perm
+    // routing in the kernel (routed != 0): inputs, and the outputs CTA 0 writes
+    int routed;
+    int E, cap, norm, nparts;
+    const float* parts;    // [nparts][T][E] partial logits, summed in slice order
+    const float* bias;     // selection-only expert bias [E] or null
+    float* logits_out;     // [T][E] or null
+    int32_t* idx_out;      // [T][K]
+    float* w_out;          // [T][K]
+    float* aux_out;        // [1] or null
+    int32_t* counts_out;   // [E]
+    int32_t* offsets_out;  // [E + 1]
+    RowTile* tiles_out;
+    int32_t* n_tiles_out;
+    int32_t* perm_tok_out;
+    int32_t* perm_slot_out;
+    int32_t* inv_out;
+    float* w_perm_out;
 };
+
+// The dispatch of a batch routed inside the kernel, in each CTA's shared
+// memory (at most kDecodeRouteTokens tokens, so a token bitmap is one word).
+constexpr int kRoutePairs = kDecodeRouteTokens * kMaxTopK;
+struct RouteSmem {
+    RowTile tiles[kRoutePairs];
+    int32_t perm_tok[kRoutePairs];
+    int32_t perm_slot[kRoutePairs];
+    int32_t inv[kRoutePairs];
+    float w_perm[kRoutePairs];
+    int32_t idx[kRoutePairs];
+    float w[kRoutePairs];
+    int32_t cnt[kMaxExperts];
+    int32_t base[kMaxExperts];
+    uint32_t sel[kMaxExperts];
+    int n_tiles;
+};
+
+template <int EPL>
+__device__ __forceinline__ void route_one(const DecParams& p, int t, RouteSmem& rs,
+                                          float* prob) {
+    const int lane = threadIdx.x & 31;
+    float l[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        if (e < p.E) {
+            // every slice loaded before the first add (one memory round trip),
+            // then summed in slice order
+            float pv[kRouterMaxSplits];
+#pragma unroll
+            for (int sl = 0; sl < kRouterMaxSplits; ++sl)
+                pv[sl] = sl < p.nparts ? p.parts[((size_t)sl * p.T + t) * p.E + e] : 0.f;
+            float v = pv[0];
+#pragma unroll
+            for (int sl = 1; sl < kRouterMaxSplits; ++sl)
+                if (sl < p.nparts) v += pv[sl];
+            l[q] = v;
+            if (p.logits_out && blockIdx.x == gridDim.x - 1)
+                p.logits_out[(size_t)t * p.E + e] = v;
+        } else {
+            l[q] = -INFINITY;
+        }
+    }
+    route_token<EPL>(l, p.E, p.K, p.norm, p.bias, rs.idx + t * p.K, rs.w + t * p.K,
+                     prob + (size_t)t * p.E);
+}
+
+// Routing and dispatch of the whole batch by one CTA (all its threads), into
+// rs; scratch: [T][E] + [E] floats of free shared memory.  The grid's last
+// CTAs also write the forward's routing outputs (the logits, the tile table
+// and offsets, the top-k and permutation, aux: one share each, so that no
+// CTA waits on all the stores).  Ends with a CTA barrier.
+__device__ void route_batch(const DecParams& p, RouteSmem& rs, float* scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = p.T, E = p.E, K = p.K, P = T * K;
+    const int last = (int)gridDim.x - 1;
+    const bool w_tab = (int)blockIdx.x == max(0, last - 1);
+    const bool w_perm = (int)blockIdx.x == max(0, last - 2);
+    const bool w_aux = (int)blockIdx.x == max(0, last - 3);
+    float* prob = scratch;               // [T][E]
+    float* term = scratch + (size_t)T * E;  // [E]
+    for (int e = tid; e < E; e += blockDim.x) {
+        rs.cnt[e] = 0;
+        rs.sel[e] = 0u;
+    }
+    const int epl = (E + 31) / 32;
+    for (int t = warp; t < T; t += blockDim.x / 32) {  // warp-uniform
+        if (epl <= 1) route_one<1>(p, t, rs, prob);
+        else if (epl <= 2) route_one<2>(p, t, rs, prob);
+        else if (epl <= 4) route_one<4>(p, t, rs, prob);
+        else route_one<8>(p, t, rs, prob);
+    }
+    __syncthreads();
+    for (int i = tid; i < P; i += blockDim.x) {
+        const int e = rs.idx[i];
+        atomicAdd(&rs.cnt[e], 1);
+        atomicOr(&rs.sel[e], 1u << (i / K));
+    }
+    __syncthreads();
+    // rows and tiles in expert order: one warp, lane l owning the run of
+    // experts [l·epl, (l+1)·epl), one shuffle scan over the lanes' totals
+    if (warp == 0) {
+        const int e0 = lane * epl, e1 = min(E, e0 + epl);
+        int sk = 0, st = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int c = rs.cnt[e];
+            const int kept = (p.cap > 0 && c > p.cap) ? p.cap : c;  // first cap pairs, token order
+            sk += kept;
+            st += (kept + kWtRows - 1) / kWtRows;
+        }
+        int ik = sk, it = st;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ik, off);
+            const int b = __shfl_up_sync(0xffffffffu, it, off);
+            if (lane >= off) {
+                ik += a;
+                it += b;
+            }
+        }
+        int base = ik - sk, tb = it - st;
+        for (int e = e0; e < e1; ++e) {
+            const int c = rs.cnt[e];
+            const int kept = (p.cap > 0 && c > p.cap) ? p.cap : c;
+            const int nt = (kept + kWtRows - 1) / kWtRows;
+            rs.base[e] = base;
+            for (int j = 0; j < nt; ++j) {
+                RowTile tl;
+                tl.expert = e;
+                tl.row0 = base + j * kWtRows;
+                tl.nrows = min(kWtRows, kept - j * kWtRows);
+                tl.pad = 0;
+                rs.tiles[tb + j] = tl;
+            }
+            if (w_tab) {
+                p.counts_out[e] = c;
+                p.offsets_out[e] = base;
+            }
+            base += kept;
+            tb += nt;
+        }
+        if (lane == 31) {
+            rs.n_tiles = it;
+            if (w_tab) {
+                p.offsets_out[E] = ik;
+                *p.n_tiles_out = it;
+            }
+        }
+    }
+    __syncthreads();
+    // scatter: a pair's row is its expert's base + the tokens before it that chose the expert
+    for (int i = tid; i < P; i += blockDim.x) {
+        const int t = i / K, k = i - t * K, e = rs.idx[i];
+        const int rank = __popc(rs.sel[e] & ((1u << t) - 1u));
+        if (p.cap > 0 && rank >= p.cap) {
+            rs.inv[i] = -1;
+            continue;
+        }
+        const int row = rs.base[e] + rank;
+        rs.perm_tok[row] = t;
+        rs.perm_slot[row] = k;
+        rs.w_perm[row] = rs.w[i];
+        rs.inv[i] = row;
+    }
+    if (w_aux && p.aux_out) {
+        // aux = E · sum_e f_e · P_e, f_e = counts/(T·K), P_e the mean probability
+        // (token order), the expert terms summed in a fixed order
+        for (int e = tid; e < E; e += blockDim.x) {
+            float psum = 0.f;
+            for (int t = 0; t < T; ++t) psum += prob[(size_t)t * E + e];
+            const float f = (float)rs.cnt[e] / ((float)T * (float)K);
+            term[e] = f * (psum / (float)T);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float v = 0.f;
+            for (int j = lane; j < E; j += 32) v += term[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) *p.aux_out = (float)E * v;
+        }
+    }
+    if (w_perm || w_tab) __syncthreads();  // the scatter's rows, for the stores below
+    if (w_perm) {
+        for (int i = tid; i < P; i += blockDim.x) {
+            p.idx_out[i] = rs.idx[i];
+            p.w_out[i] = rs.w[i];
+            const int row = rs.inv[i];
+            p.inv_out[i] = row;
+            if (row >= 0) {
+                p.perm_tok_out[row] = rs.perm_tok[row];
+                p.perm_slot_out[row] = rs.perm_slot[row];
+                p.w_perm_out[row] = rs.w_perm[row];
+            }
+        }
+    }
+    if (w_tab)
+        for (int j = tid; j < rs.n_tiles; j += blockDim.x) p.tiles_out[j] = rs.tiles[j];
+    __syncthreads();
+}
 
 struct Unit {
     int kind, pitem, ks, tile, blk;
@@ -112,13 +322,15 @@ __device__ __forceinline__ Unit unit_of(const DecParams& p, int u, int n_gu) {
 }
 
 // Epilogue of one output row and weight row i of the block (experts_wt.cu).
-__device__ __forceinline__ void store_out(const DecParams& p, int kind, size_t row, int blk, int i,
-                                          float d0, float d1) {
+__device__ __forceinline__ void store_out(const DecParams& p, const float* w_perm,
+                                          const int32_t* perm_tok, const int32_t* perm_slot,
+                                          int kind, size_t row, int blk, int i, float d0,
+                                          float d1) {
     if (kind == kGateUp) {
         p.h[row * p.I + (size_t)blk * kWM + i] = __float2bfloat16_rn(silu_f(d0) * d1);
     } else {
-        const float wr = p.w_perm[row];
-        const size_t yrow = (size_t)p.perm_tok[row] * p.K + (size_t)p.perm_slot[row];
+        const float wr = w_perm[row];
+        const size_t yrow = (size_t)perm_tok[row] * p.K + (size_t)perm_slot[row];
         if (p.y32) {
             float* o = p.y32 + yrow * p.H + (size_t)blk * (2 * kWM);
             o[i] = wr * d0;
@@ -152,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
+    __shared__ RouteSmem rs;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -183,7 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     pdl_wait();  // the prologue above overlaps the previous kernel's tail
-    const int n_tiles = *p.n_tiles;
+    // the dispatch: routed here (the ring is still free: scratch), or read
+    // from the dispatch kernel's outputs
+    if (p.routed) route_batch(p, rs, reinterpret_cast<float*>(smem));
+    const RowTile* tiles = p.routed ? rs.tiles : p.tiles;
+    const int32_t* perm_tok = p.routed ? rs.perm_tok : p.perm_tok;
+    const int32_t* perm_slot = p.routed ? rs.perm_slot : p.perm_slot;
+    const float* w_perm = p.routed ? rs.w_perm : p.w_perm;
+    const int32_t* inv = p.routed ? (p.cap > 0 ? rs.inv : nullptr) : p.inv;
+    const int n_tiles = p.routed ? rs.n_tiles : *p.n_tiles;
     const int n_gu = n_tiles * p.n_blk[0] * p.ksplit[0];
     const int total = n_gu + n_tiles * p.n_blk[1] * p.ksplit[1];
 
@@ -200,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_once = ptx::l2_policy_evict_first();
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
                 const Unit x = unit_of(p, u, n_gu);
-                const RowTile tl = p.tiles[x.tile];
+                const RowTile tl = tiles[x.tile];
                 const int kb0 = x.ks * p.kb_per[x.kind];
                 const int kb1 = min(p.num_kb[x.kind], kb0 + p.kb_per[x.kind]);
                 const int nbox = (tl.nrows + kBox - 1) / kBox;
@@ -307,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit x = unit_of(p, u, n_gu);
                 const int kb0 = x.ks * p.kb_per[x.kind];
                 const int kb1 = min(p.num_kb[x.kind], kb0 + p.kb_per[x.kind]);
-                const int nrows = p.tiles[x.tile].nrows;
+                const int nrows = tiles[x.tile].nrows;
                 const int n = ((nrows + kBox - 1) / kBox) * kBox;
                 const uint32_t idesc = ptx::idesc_bf16_f32(kWM, n);
                 if (!ptx::mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_s,
@@ -361,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit x = unit_of(p, u, n_gu);
-            const RowTile tl = p.tiles[x.tile];
+            const RowTile tl = tiles[x.tile];
             // Accumulator column -> tile row: the identity, except for gate/up
             // units on x itself, where column cc is token cc and lane cc holds
             // its row in the tile (-1: the token is not in the tile).  Read
@@ -369,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool direct = p.x_direct && x.kind == kGateUp;
             int jm = -1;
             if (direct) {
-                const int tok = lane < tl.nrows ? p.perm_tok[tl.row0 + lane] : -1;
+                const int tok = lane < tl.nrows ? perm_tok[tl.row0 + lane] : -1;
                 for (int j = 0; j < tl.nrows; ++j)
                     if (__shfl_sync(0xffffffffu, tok, j) == lane) jm = j;
             }
@@ -399,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int j = direct ? __shfl_sync(0xffffffffu, jm, cc)
                                              : (c + cc < tl.nrows ? c + cc : -1);
                         if (j >= 0)
-                            store_out(p, x.kind, (size_t)tl.row0 + j, x.blk, i,
+                            store_out(p, w_perm, perm_tok, perm_slot, x.kind, (size_t)tl.row0 + j, x.blk, i,
                                       __uint_as_float(v0[cc]), __uint_as_float(v1[cc]));
                     }
                 }
@@ -451,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             s0 += __ldcg(src + (size_t)j * kWM + i);
                             s1 += __ldcg(src + ((size_t)p.part_rows + j) * kWM + i);
                         }
-                        store_out(p, x.kind, (size_t)tl.row0 + j, x.blk, i, s0, s1);
+                        store_out(p, w_perm, perm_tok, perm_slot, x.kind, (size_t)tl.row0 + j, x.blk, i, s0, s1);
                     }
                     if (lane == 0) *cnt = 0;
                 }
@@ -472,12 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // lane: row r0 + lane of the tile -> its token's count
                         int tok = -1;
                         if (r0 + lane < tl.nrows) {
-                            const int t = p.perm_tok[tl.row0 + r0 + lane];
+                            const int t = perm_tok[tl.row0 + r0 + lane];
                             int kept = p.K;
-                            if (p.inv) {
+                            if (inv) {
                                 kept = 0;
                                 for (int k = 0; k < p.K; ++k)
-                                    kept += __ldcg(p.inv + (size_t)t * p.K + k) >= 0 ? 1 : 0;
+                                    kept += inv[(size_t)t * p.K + k] >= 0 ? 1 : 0;
                             }
                             if (atomicAdd(&p.tok_done[(size_t)t * ncb + cb], 1) == kept - 1)
                                 tok = t;
@@ -495,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < kMaxTopK; ++k) {
                                 const size_t pr = (size_t)t * p.K + k;
-                                kp[k] = k < p.K && (!p.inv || __ldcg(p.inv + pr) >= 0);
+                                kp[k] = k < p.K && (!inv || inv[pr] >= 0);
                                 if (p.y32) {
                                     v0[k] = kp[k] ? __ldcg(p.y32 + pr * p.H + c0) : 0.f;
                                     v1[k] = kp[k] ? __ldcg(p.y32 + pr * p.H + c1) : 0.f;
@@ -538,8 +759,12 @@ bool experts_decode_supported(const Sizes& s) {
 
 cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                                   const __nv_bfloat16* x, const int32_t* inv,
-                                  __nv_bfloat16* out, cudaStream_t st) {
+                                  __nv_bfloat16* out, cudaStream_t st, const DecodeRouting* route) {
     if (!experts_decode_supported(s)) return cudaErrorInvalidValue;
+    static_assert(kThreads / 32 >= kDecodeRouteTokens, "one routing warp per token");
+    if (route && (s.T > kDecodeRouteTokens || s.K > kMaxTopK || s.E > kMaxExperts ||
+                  route->nparts < 1 || route->nparts > kRouterMaxSplits))
+        return cudaErrorInvalidValue;
     const bool packed = W.packed != nullptr;
     const long long P = s.P();
     const WtPlan pl = wt_plan(s);
@@ -581,7 +806,29 @@ cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const 
     p.a_blocks[0] = s.I / kPackRows;
     p.a_blocks[1] = s.H / kPackRows;
     static_assert(kDecodeDirectTokens <= kBox, "the whole batch in one token box");
+    static_assert(kDecodeRouteTokens <= 32, "a token bitmap is one word");
     p.x_direct = s.T <= kDecodeDirectTokens ? 1 : 0;
+    if (route) {
+        p.routed = 1;
+        p.E = s.E;
+        p.cap = route->cap;
+        p.norm = route->norm;
+        p.nparts = route->nparts;
+        p.parts = route->parts;
+        p.bias = route->bias;
+        p.logits_out = route->logits;
+        p.idx_out = route->idx;
+        p.w_out = route->w;
+        p.aux_out = route->aux;
+        p.counts_out = ws.counts;
+        p.offsets_out = ws.offsets;
+        p.tiles_out = ws.tiles;
+        p.n_tiles_out = ws.n_tiles;
+        p.perm_tok_out = ws.perm_tok;
+        p.perm_slot_out = ws.perm_slot;
+        p.inv_out = ws.inv;
+        p.w_perm_out = ws.w_perm;
+    }
 
     CUtensorMap mx, mh, mg, mu, md;
     const bool mx_ok = p.x_direct ? make_tma_2d(&mx, x, s.T, s.H, kBox)

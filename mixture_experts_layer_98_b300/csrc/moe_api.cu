@@ -289,6 +289,12 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     // kernels.
     const bool router_tc = s.T >= 128 && router_tc_supported(s);
     const int n_partials = s.nrouter();
+    // Up to kDecodeRouteTokens tokens on the fused decode kernel, that kernel
+    // routes and dispatches the batch itself, straight after the router logits.
+    const bool route_in_experts = path == ExpertPath::kDecodeFused &&
+                                  s.T <= kDecodeRouteTokens && s.K <= kMaxTopK &&
+                                  s.E <= kMaxExperts && !router_tc;
+    DecodeRouting droute{};
     cudaError_t e;
     if (router_tc) {
         const int nsplit = router_tc_splits(s);
@@ -305,8 +311,11 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         e = launch_router_logits(x, Wr, s, nsplit, ws.logit_parts, ws.status, ws.n_clear, st);
         if (e != cudaSuccess) return cuda_status(e);
         mark(1, st);
-        e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, bias, idx, w,
-                                        gather_x, s, ws, tile_rows, aux, cap, st);
+        if (route_in_experts)
+            droute = DecodeRouting{ws.logit_parts, nsplit, logits, norm, bias, idx, w, aux, cap};
+        else
+            e = launch_route_dispatch_small(ws.logit_parts, nsplit, logits, norm, bias, idx, w,
+                                            gather_x, s, ws, tile_rows, aux, cap, st);
     } else {
         e = launch_router(x, Wr, s, norm, bias, logits, ws.logit_parts, idx, w, ws.p_partial,
                           ws.status,
@@ -318,7 +327,7 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
     }
     if (e != cudaSuccess) return cuda_status(e);
     mark(2, st);
-    if (ev_routed) {
+    if (ev_routed && !route_in_experts) {
         e = cudaEventRecord(ev_routed, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
@@ -334,8 +343,14 @@ int run_forward(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const ExpertWei
         case ExpertPath::kDecodeFused: {
             // experts and combine in one kernel: the whole kernel is timed as the
             // gate/up stage; the down and combine stages read zero
-            e = launch_experts_decode(W, s, ws, x, cap > 0 ? ws.inv : nullptr, out, st);
+            e = launch_experts_decode(W, s, ws, x, cap > 0 ? ws.inv : nullptr, out, st,
+                                      route_in_experts ? &droute : nullptr);
             if (e != cudaSuccess) return cuda_status(e);
+            // with the routing in the kernel, its outputs are final only now
+            if (ev_routed && route_in_experts) {
+                e = cudaEventRecord(ev_routed, st);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
             if (mid) cudaEventRecord(mid, st);
             mark(4, st);
             mark(5, st);

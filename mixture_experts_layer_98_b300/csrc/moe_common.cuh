@@ -259,10 +259,27 @@ cudaError_t launch_experts_q4_mma(const char* q4, const Sizes& s, const Workspac
 constexpr int kDecodeFusedTokens = 64;
 constexpr int kDecodeAutoTokens = 16;  // MOE_PATH_AUTO uses the fused kernel up to here
 constexpr int kDecodeDirectTokens = 16;
+// ... and up to kDecodeRouteTokens tokens it also routes and dispatches the
+// batch itself (one routing warp per token), right after the router logits.
+constexpr int kDecodeRouteTokens = 6;
 bool experts_decode_supported(const Sizes& s);
+// Routing done by the fused decode kernel itself (T <= kDecodeDirectTokens):
+// its inputs (the router's partial logits) and the forward's routing outputs.
+struct DecodeRouting {
+    const float* parts;
+    int nparts;
+    float* logits;       // may be null
+    int norm;
+    const float* bias;   // may be null
+    int32_t* idx;
+    float* w;
+    float* aux;          // may be null
+    int cap;
+};
 cudaError_t launch_experts_decode(const ExpertWeights& W, const Sizes& s, const Workspace& ws,
                                   const __nv_bfloat16* x, const int32_t* inv,
-                                  __nv_bfloat16* out, cudaStream_t st);
+                                  __nv_bfloat16* out, cudaStream_t st,
+                                  const DecodeRouting* route = nullptr);
 // out[t] = sum over k of Y row t*K + k (Y token-major, as the expert kernels
 // store it), skipping the pairs with inv[t*K + k] < 0 when inv != null
 // (dropped by a capacity); with y_by_inv, Y is in dispatch order and row

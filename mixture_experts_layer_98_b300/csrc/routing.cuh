@@ -66,8 +66,7 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
     }
     // K rounds of a warp-wide arg-max: the largest key, then the lowest expert
     // index among the lanes holding it (two redux.sync per round).  The
-    // winner's probability is recomputed in every lane from its unbiased
-    // logit, fetched from the lane that holds it.
+    // winner's (unbiased) probability is fetched from the lane that holds it.
     uint32_t key[EPL];
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
@@ -88,15 +87,14 @@ __device__ __forceinline__ void route_token(const float (&l)[EPL], int E, int K,
             }
         const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
         const int we = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)be : 0x7fffffffu);
-        float lw = 0.f;
+        float pw = 0.f;
 #pragma unroll
-        for (int q = 0; q < EPL; ++q)  // taken; the winner's unbiased logit
+        for (int q = 0; q < EPL; ++q)  // taken; the winner's probability
             if (we == lane + 32 * q) {
                 key[q] = 0u;
-                lw = l[q];
+                pw = p[q];
             }
-        lw = __shfl_sync(0xffffffffu, lw, we & 31);
-        const float pk = expf(lw - m) * inv_s;
+        const float pk = __shfl_sync(0xffffffffu, pw, we & 31);
         wsum += pk;  // same value and order in every lane
         if (lane == k) {
             my_e = we;
