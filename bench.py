@@ -58,12 +58,12 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 _COMMON = ["moe_common.cuh", "sm100_ptx.cuh"]
 STAGE_SOURCES = {
     "router": ["router_tc.cu", "router.cu", "routing.cuh"] + _COMMON,
-    "dispatch": ["dispatch.cu"] + _COMMON,
+    "dispatch": ["dispatch.cu", "routing.cuh"] + _COMMON,
     "combine": ["combine.cu"] + _COMMON,
 }
 PATH_SOURCES = {
     "tcgen05": ["experts_tc.cu"], "tcgen05_pair": ["experts_pair.cu"],
-    "tcgen05_wt": ["experts_wt.cu"], "tcgen05_decode": ["experts_decode.cu"],
+    "tcgen05_wt": ["experts_wt.cu"], "tcgen05_decode": ["experts_decode.cu", "routing.cuh"],
     "streaming": ["experts_stream.cu"], "warp_mma_q4": ["experts_q4_mma.cu", "quant.cu"],
     "tcgen05_q4": ["experts_q4.cu", "quant.cu"],
 }
