@@ -38,6 +38,26 @@ namespace {
 
 constexpr int kWords = kChunkTokens / 32;
 
+// Sum of column pe over the rows j, j+4, j+8, ... of p_partial (the routing
+// CTAs' per-expert probability sums), in a fixed order: eight running sums
+// (row j + 4i goes to sum i mod 8, so eight loads are in flight), added
+// pairwise at the end.
+__device__ __forceinline__ float psum_rows(const float* p_partial, int nrouter, int E, int pe,
+                                           int j) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.f;
+    int b = j;
+    for (; b + 28 < nrouter; b += 32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] += p_partial[(size_t)(b + 4 * i) * E + pe];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (b + 4 * i < nrouter) a[i] += p_partial[(size_t)(b + 4 * i) * E + pe];
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
 __global__ void __launch_bounds__(kChunkTokens) dispatch_count_kernel(
     const int32_t* idx, int T, int E, int K, int32_t* chunk_counts) {
     pdl_trigger();
@@ -89,16 +109,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     pdl_wait();
     if (aux) {
         const int pe = threadIdx.x % kMaxExperts, pj = threadIdx.x / kMaxExperts;
-        if (pe < E) {
-            float a0 = 0.f, a1 = 0.f;
-            int b = pj;
-            for (; b + 4 < nrouter; b += 8) {
-                a0 += p_partial[(size_t)b * E + pe];
-                a1 += p_partial[(size_t)(b + 4) * E + pe];
-            }
-            if (b < nrouter) a0 += p_partial[(size_t)b * E + pe];
-            psum_s[pj][pe] = a0 + a1;
-        }
+        if (pe < E) psum_s[pj][pe] = psum_rows(p_partial, nrouter, E, pe, pj);
         __syncthreads();
     }
     // threads past kMaxExperts own no expert but still take part in the barriers
@@ -107,16 +118,17 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int run = 0;
     if (own) {
         int c = 0;
-        for (; c + 4 <= nchunks; c += 4) {
-            const int v0 = chunk_counts[(size_t)(c + 0) * E + e];
-            const int v1 = chunk_counts[(size_t)(c + 1) * E + e];
-            const int v2 = chunk_counts[(size_t)(c + 2) * E + e];
-            const int v3 = chunk_counts[(size_t)(c + 3) * E + e];
-            chunk_base[(size_t)(c + 0) * E + e] = run;
-            chunk_base[(size_t)(c + 1) * E + e] = run + v0;
-            chunk_base[(size_t)(c + 2) * E + e] = run + v0 + v1;
-            chunk_base[(size_t)(c + 3) * E + e] = run + v0 + v1 + v2;
-            run += v0 + v1 + v2 + v3;
+        // eight chunks' counts loaded before their bases are stored (the
+        // stores may alias the loads as far as the compiler knows)
+        for (; c + 8 <= nchunks; c += 8) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = chunk_counts[(size_t)(c + i) * E + e];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                chunk_base[(size_t)(c + i) * E + e] = run;
+                run += v[i];
+            }
         }
         for (; c < nchunks; ++c) {
             const int v = chunk_counts[(size_t)c * E + e];
@@ -281,16 +293,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     } else if (aux) {
         // four threads per expert add up rows j, j+4, ... of p_partial
         const int pe = tid % kMaxExperts, pj = tid / kMaxExperts;
-        if (pe < E) {
-            float a0 = 0.f, a1 = 0.f;
-            int b = pj;
-            for (; b + 4 < nrouter; b += 8) {
-                a0 += p_partial[(size_t)b * E + pe];
-                a1 += p_partial[(size_t)(b + 4) * E + pe];
-            }
-            if (b < nrouter) a0 += p_partial[(size_t)b * E + pe];
-            prob_s[pj * kMaxExperts + pe] = a0 + a1;
-        }
+        if (pe < E) prob_s[pj * kMaxExperts + pe] = psum_rows(p_partial, nrouter, E, pe, pj);
     }
     __syncthreads();  // routing results visible to the CTA
     const int P = T * K;

@@ -123,8 +123,15 @@ __global__ void __launch_bounds__(kRouterTokens * 32) route_from_logits_kernel(
         for (int q = 0; q < EPL; ++q) {
             const int e = lane + 32 * q;
             if (e < E) {
-                float v = parts[(size_t)t * E + e];
-                for (int sidx = 1; sidx < nparts; ++sidx) v += parts[sidx * part_stride + (size_t)t * E + e];
+                // every slice loaded before the first add, summed in slice order
+                float pv[kRouterMaxSplits];
+#pragma unroll
+                for (int sl = 0; sl < kRouterMaxSplits; ++sl)
+                    pv[sl] = sl < nparts ? parts[sl * part_stride + (size_t)t * E + e] : 0.f;
+                float v = pv[0];
+#pragma unroll
+                for (int sl = 1; sl < kRouterMaxSplits; ++sl)
+                    if (sl < nparts) v += pv[sl];
                 l[q] = v;
                 if (logits_out) logits_out[(size_t)t * E + e] = v;
             } else {
@@ -196,6 +203,7 @@ cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wr, const
 cudaError_t launch_route_from_logits(const float* parts, int nparts, float* logits_out,
                                      const Sizes& s, int norm, const float* bias, int32_t* idx,
                                      float* w, float* p_partial, cudaStream_t st) {
+    if (nparts < 1 || nparts > kRouterMaxSplits) return cudaErrorInvalidValue;
     const int epl = (s.E + 31) / 32;
     if (epl <= 1)
         return launch_route_t<1>(parts, nparts, logits_out, s, norm, bias, idx, w, p_partial, st);
