@@ -236,28 +236,41 @@ def test_pair_path_large_sampled(moe, name, cf):
 # the same units with the same arithmetic as the three separate kernels: the
 # results must agree bit for bit -- one token with a 3-way K split of gate/up,
 # a few tokens, 64 tokens (one 64-row tile per expert), two experts of 14336
-# rows, split shapes from the fuzz list, and a capacity that drops pairs.
+# rows, split shapes from the fuzz list, and a capacity that drops pairs.  Up
+# to six tokens the fused kernel also routes the batch itself (the separate
+# path runs the one-CTA routing kernel): logits, top-k, aux and the expert
+# counts must agree bit for bit too, with and without a capacity, at the
+# largest batch routed in the kernel (6) and the smallest that is not (7).
 @pytest.mark.parametrize("name,cf", [("decode_t1", 0.0), ("decode_t4", 0.0), ("decode_t16", 0.0),
                                      ("decode_t64", 0.0), ("mixtral_decode_t1", 0.0),
                                      ("decode_t16", 1.0), ("decode_t64", 1.0),
+                                     ("decode_t4", 1.0), ("split_b", 1.0),
+                                     ("edge_t6", 0.0), ("edge_t6", 1.25), ("edge_t7", 0.0),
                                      ("split_a", 0.0), ("split_b", 0.0)])
 def test_decode_fused_is_bitwise_the_three_kernels(moe, name, cf):
     extra = {"split_a": mi.MoEConfig("split_a", 2, 1024, 16, 2, 512, True, seed=7),
-             "split_b": mi.MoEConfig("split_b", 3, 1280, 8, 2, 640, True, seed=8)}
+             "split_b": mi.MoEConfig("split_b", 3, 1280, 8, 2, 640, True, seed=8),
+             "edge_t6": mi.MoEConfig("edge_t6", 6, 1024, 32, 4, 512, True, seed=9),
+             "edge_t7": mi.MoEConfig("edge_t7", 7, 1024, 32, 4, 512, True, seed=10)}
     cfg = extra.get(name) or mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, "cuda")
-    res = {}
+    res, counts = {}, {}
     for p in (moe.MOE_PATH_TCGEN05_WT, moe.MOE_PATH_TCGEN05_DECODE):
         prev = moe.moe_set_expert_path(p)
         try:
             res[p] = [t.clone() for t in moe.moe_forward_opts(
                 inp["x"], inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"], cfg.K,
                 cfg.norm, capacity_factor=cf)]
+            torch.cuda.synchronize()
+            counts[p] = moe.moe_last_expert_counts(cfg.E).clone()
         finally:
             moe.moe_set_expert_path(prev)
-    torch.cuda.synchronize()
     for u, v in zip(res[moe.MOE_PATH_TCGEN05_WT], res[moe.MOE_PATH_TCGEN05_DECODE]):
         assert torch.equal(u, v)
+    assert torch.equal(counts[moe.MOE_PATH_TCGEN05_WT], counts[moe.MOE_PATH_TCGEN05_DECODE])
+    idx = res[moe.MOE_PATH_TCGEN05_DECODE][2].cpu().numpy()
+    assert np.array_equal(counts[moe.MOE_PATH_TCGEN05_DECODE].numpy(),
+                          np.bincount(idx.ravel(), minlength=cfg.E))
     assert moe.moe_device_status() == 0
 
 
