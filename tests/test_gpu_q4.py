@@ -149,9 +149,12 @@ def test_q4_forward_is_the_bf16_forward_on_dequantised_weights(moe, name, kernel
     assert moe.moe_device_status() == 0
 
 
+# decode_t4 on the warp-MMA kernels: the gate/up kernel routes the batch itself
+# (capacity drops and the selection bias inside the expert kernel)
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
-def test_q4_options_capacity_and_bias(moe, kernel):
-    cfg = mi.CONFIGS["decode_t16"]
+@pytest.mark.parametrize("name", ["decode_t16", "decode_t4"])
+def test_q4_options_capacity_and_bias(moe, kernel, name):
+    cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, "cuda")
     q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
     deq = moe.moe_dequantize_experts_q4(q4)
