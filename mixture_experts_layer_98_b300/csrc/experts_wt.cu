@@ -462,6 +462,17 @@ WtPlan wt_plan(const Sizes& s) {
     pl.items_dn = tiles * (s.H / (2 * kWM));
     pl.ks_gu = split_for(pl.items_gu, s.H / kBK);
     pl.ks_dn = split_for(pl.items_dn, s.I / kBK);
+    if (s.T <= kDecodeAutoTokens) {
+        // The fused decode kernel runs both GEMMs in one grid and a down unit
+        // waits for its tile's gate/up units, so there round fill is not the
+        // whole story: measured (graph replay, the fused kernel), two slices
+        // of gate/up while its items are under four rounds (four tokens:
+        // 193.5 -> 187.3 us) and of down while its items are under one round
+        // (one token: 80.8 -> 76.4 us) are faster; more slices, or down slices
+        // with a round of items or more, measured slower.
+        if (pl.items_gu < 4 * kSplitBelow && pl.ks_gu < 2 && s.H / kBK >= 16) pl.ks_gu = 2;
+        if (pl.items_dn < kSplitBelow && pl.ks_dn < 2 && s.I / kBK >= 16) pl.ks_dn = 2;
+    }
     // A tile holds at most one row per token, so at most min(kWtRows, T) rows.
     pl.part_rows = s.T < kWtRows ? ((s.T + kBox - 1) / kBox) * kBox : kWtRows;
     // Separate gate/up and down regions: the fused decode kernel runs units of
