@@ -63,7 +63,8 @@ STAGE_SOURCES = {
 }
 PATH_SOURCES = {
     "tcgen05": ["experts_tc.cu"], "tcgen05_pair": ["experts_pair.cu"],
-    "tcgen05_wt": ["experts_wt.cu"], "tcgen05_decode": ["experts_decode.cu", "routing.cuh"],
+    "tcgen05_wt": ["experts_wt.cu"],
+    "tcgen05_decode": ["experts_decode.cu", "experts_wt.cu", "routing.cuh"],
     "streaming": ["experts_stream.cu"], "warp_mma_q4": ["experts_q4_mma.cu", "quant.cu"],
     "tcgen05_q4": ["experts_q4.cu", "quant.cu"],
 }
