@@ -131,12 +131,15 @@ __device__ __forceinline__ Item item_of(const MmaParams& p, int item) {
     return it;
 }
 
-// Pair j of a code word dequantised: bf16x2 (column 2j low, 2j+1 high) of
-// bf16(q·s + b), one rounding (as q4_dequant8).
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int j, __nv_bfloat162 s2,
+// A code pair dequantised: bf16x2 of bf16(q·s + b), one rounding (as
+// q4_dequant8).  m is a code word with one code per byte (its low or its
+// high nibbles, masked and shifted to bits 0-3 of each byte); sel picks the
+// pair's two bytes (0x4240: bytes 0 and 2, 0x4341: bytes 1 and 3) and puts
+// the bf16 exponent byte of 128.0 above each, so the halves read 128 + q.
+__device__ __forceinline__ uint32_t dq_perm(uint32_t m, uint32_t sel, __nv_bfloat162 s2,
                                             __nv_bfloat162 b2) {
     const __nv_bfloat162 k128 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0x4300u));
-    const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t t = __byte_perm(m, 0x43434343u, sel);
     __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&t);
     v = __hfma2(__hsub2(v, k128), s2, b2);
     return *reinterpret_cast<const uint32_t*>(&v);
@@ -220,18 +223,33 @@ __device__ __forceinline__ void stage_mma(const uint8_t* st, const int (&code_of
             tk[n][0] = *reinterpret_cast<const uint4*>(tp + tok0);
             tk[n][1] = *reinterpret_cast<const uint4*>(tp + tok1);
         }
+        // each code word split into its low and its high nibbles, one code per
+        // byte: pair j of the word (codes at bits 4j and 16 + 4j) is then bytes
+        // 0, 2 (j = 0, 1) or 1, 3 (j = 2, 3) of the low (even j) or high (odd j)
+        // nibbles: a byte permute each (shifting and masking each pair into
+        // place instead measured 7 % slower at 16 and 64 tokens)
+        uint32_t lo[2][2][2], hi[2][2][2];  // [tile][row g / g + 8][word 2c / 2c + 1]
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                lo[i][r][0] = wq[i][r].x & 0x0F0F0F0Fu;
+                hi[i][r][0] = (wq[i][r].x >> 4) & 0x0F0F0F0Fu;
+                lo[i][r][1] = wq[i][r].y & 0x0F0F0F0Fu;
+                hi[i][r][1] = (wq[i][r].y >> 4) & 0x0F0F0F0Fu;
+            }
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            const int j = 2 * (t & 1);
+            // step t: pairs 2(t%2) (low nibbles) and 2(t%2)+1 (high) of word 2c + t/2
+            const uint32_t sel = (t & 1) ? 0x4341u : 0x4240u;
+            const int wi = t >> 1;
             uint32_t a[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const uint32_t w0 = (t >> 1) ? wq[i][0].y : wq[i][0].x;  // row g
-                const uint32_t w1 = (t >> 1) ? wq[i][1].y : wq[i][1].x;  // row g + 8
-                a[i][0] = dq_pair(w0, j, s2[i][0], b2[i][0]);          // cols 2c, 2c+1
-                a[i][1] = dq_pair(w1, j, s2[i][1], b2[i][1]);
-                a[i][2] = dq_pair(w0, j + 1, s2[i][0], b2[i][0]);      // cols 2c+8, 2c+9
-                a[i][3] = dq_pair(w1, j + 1, s2[i][1], b2[i][1]);
+                a[i][0] = dq_perm(lo[i][0][wi], sel, s2[i][0], b2[i][0]);  // row g, cols 2c, 2c+1
+                a[i][1] = dq_perm(lo[i][1][wi], sel, s2[i][1], b2[i][1]);  // row g + 8
+                a[i][2] = dq_perm(hi[i][0][wi], sel, s2[i][0], b2[i][0]);  // row g, cols 2c+8, 2c+9
+                a[i][3] = dq_perm(hi[i][1][wi], sel, s2[i][1], b2[i][1]);  // row g + 8
             }
 #pragma unroll
             for (int n = 0; n < NN; ++n) {
