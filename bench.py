@@ -420,13 +420,20 @@ def config_block(cfg, world):
 # ---- our arm ------------------------------------------------------------------------
 
 # The same line's extra configurations: (name, timed as CUDA-graph replays)
-EXTRA_CONFIGS = [("prefill_h4096", False), ("decode_t1", True), ("decode_t4", True),
-                 ("decode_t16", True), ("decode_t64", True)]
+# (config, CUDA-graph replay, expert weights: None = the run's --weights); an
+# entry with its own weights is keyed "config:weights"
+EXTRA_CONFIGS = [("prefill_h4096", False, None), ("decode_t1", True, None),
+                 ("decode_t4", True, None), ("decode_t16", True, None), ("decode_t64", True, None),
+                 ("decode_t1", True, "q4"), ("decode_t4", True, "q4"), ("decode_t16", True, "q4"),
+                 ("decode_t64", True, "q4")]
 
 
-def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clocks):
+def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clocks,
+            weights=None):
     """Times K forwards of cfg (after warm-up) and a second pass with stage
-    events; returns the fields of one result (main line or extra entry)."""
+    events; returns the fields of one result (main line or extra entry).
+    weights: the expert weight format (default: --weights)."""
+    weights = weights or args.weights
     inp = mi.make_inputs(cfg, dev, seed=replica_seed(cfg, rank))
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -439,11 +446,11 @@ def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clock
 
     packed = None
     q4 = None
-    if args.weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
+    if weights == "packed" and moe.moe_packed_experts_bytes(H, E, I):
         # one-time weight layout transform (model load), outside every timed region
         packed = moe.moe_pack_experts(inp["W_gate"], inp["W_up"], inp["W_down"])
         torch.cuda.synchronize()
-    if args.weights == "q4":
+    if weights == "q4":
         q4 = moe.moe_quantize_experts_q4(inp["W_gate"], inp["W_up"], inp["W_down"])
         torch.cuda.synchronize()
 
@@ -552,7 +559,7 @@ def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clock
     work, touched = stage_work(cfg, counts, fused=path_name == "tcgen05_decode", wb=wb)
     stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     roof = roofline_of(work, stage_mean, path_name, pk, cfg,
-                       "q4" if q4 is not None else args.weights)
+                       "q4" if q4 is not None else weights)
     block = block_roofline_of(cfg, counts, wb, mean_ms, pk)
 
     e2e = None
@@ -604,15 +611,15 @@ def run_ours(args, world, rank, local):
 
     extras = {}
     if not args.no_extras and not args.shape:
-        for name, graph in EXTRA_CONFIGS:
-            if name == cfg.name:
+        for name, graph, ew in EXTRA_CONFIGS:
+            if name == cfg.name and ew in (None, args.weights):
                 continue
             ecfg = mi.CONFIGS[name]
             r, _ = measure(moe, ecfg, args, world, rank, local, dev, graph=graph, want_e2e=False,
-                           want_clocks=not args.quiet_clocks)
+                           want_clocks=not args.quiet_clocks, weights=ew)
             r.pop("e2e")
             r["config"] = config_block(ecfg, world)["workload"]
-            extras[name] = r
+            extras[name if ew is None else f"{name}:{ew}"] = r
 
     if rank == 0:
         line = {
