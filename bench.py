@@ -422,10 +422,12 @@ def config_block(cfg, world):
 # The same line's extra configurations: (name, timed as CUDA-graph replays)
 # (config, CUDA-graph replay, expert weights: None = the run's --weights); an
 # entry with its own weights is keyed "config:weights"
-EXTRA_CONFIGS = [("prefill_h4096", False, None), ("decode_t1", True, None),
-                 ("decode_t4", True, None), ("decode_t16", True, None), ("decode_t64", True, None),
+EXTRA_CONFIGS = [("prefill_h4096", False, None), ("prefill_h2048", False, None),
+                 ("mixtral_prefill", False, None),
+                 ("decode_t1", True, None), ("decode_t4", True, None), ("decode_t16", True, None),
+                 ("decode_t64", True, None), ("mixtral_decode_t1", True, None),
                  ("decode_t1", True, "q4"), ("decode_t4", True, "q4"), ("decode_t16", True, "q4"),
-                 ("decode_t64", True, "q4")]
+                 ("decode_t64", True, "q4"), ("mixtral_decode_t1", True, "q4")]
 
 
 def measure(moe, cfg, args, world, rank, local, dev, graph, want_e2e, want_clocks,
