@@ -453,7 +453,9 @@ static int side_stream(cudaStream_t st, SideStream* out) {
 // copied back, and the call returns after the stream has finished them.  The
 // routing outputs (logits, top-k, aux) are final after the dispatch: they are
 // copied back on a side stream while the expert kernels still run, so only the
-// copy of `out` follows the last kernel.
+// copy of `out` follows the last kernel.  (A decode batch that the fused kernel
+// routes itself has them final only when that kernel ends; the side copies
+// then follow it, beside the copy of `out`.)
 static int forward_host(const void* x_host, int T, int H, const void* W_router,
                         const ExpertWeights& W, const void* wg, const void* wu, const void* wd,
                         int E, int K, int I, int norm, const float* bias, int cap,
